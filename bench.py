@@ -1,0 +1,415 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP32 SGEMM on GB300: one JSON line on stdout (rank 0).
+
+A step is one sgemm() call (A-transpose pre-pass + main kernel) on the timed
+workload: M = N = K = 8192, row-major fp32, A, B, C_in ~ U[-1, 1) from seed
+1003, alpha = 1.5, beta = 0.5.  Inputs (805 MB) are larger than the 129 MB L2,
+so no flush is needed between steps.
+
+  value    GFLOP/s = 2MNK / (device time per step), inputs resident in HBM,
+           summed over ranks (replicas: every rank runs the whole workload)
+  e2e      the same metric through the host-buffer entry point sgemm_host():
+           pinned host A, B, C_in copied in and C copied out every step
+  roofline the main kernel against the FP32 FFMA peak (SMs x 128 FFMA/clk x
+           2 FLOP x 2070 MHz), timed with CUDA events on its own stream
+  cpu_baseline  the CPU oracle on this host's cores on a bounded sample of rows
+
+`--impl reference` times the CPU oracle (the only reference this build has) on
+a bounded sample of the same workload per step and prints the same line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SGEMM GFLOP/s (2MNK/t) at M=N=K=8192 FP32; % of GB300 FP32 FFMA peak"
+FFMA_PER_SM_PER_CLK = 128
+SM_MAX_MHZ_FALLBACK = 2070.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None, help="workload name (default: the 8192^3 case)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(world, value, device=None):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 100 ms; only samples inside [t0, t1] are kept."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+        self.windows = []
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        import datetime
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[4], parts[5:]))
+                except ValueError:
+                    continue
+            os.unlink(self.path)
+        inside = [r for r in rows if any(t0 - 0.15 <= r[0] <= t1 + 0.15 for t0, t1 in self.windows)]
+        use = inside or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
+                    "samples": 0}
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in use:
+            for n, v in zip(names, r[4][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        power = []
+        for r in use:
+            try:
+                power.append(float(r[3]))
+            except ValueError:
+                pass
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use),
+                "reasons": sorted(reasons), "samples": len(use),
+                "in_window": bool(inside),
+                "power_w_median": statistics.median(power) if power else None}
+
+
+# ---------------------------------------------------------------------- CPU oracle timing
+def time_oracle_rows(w, A, B, C, row_budget_s=12.0, first=16, max_rows=None):
+    """The oracle as it stands on full rows of the workload; grows the sample
+    until about `row_budget_s` seconds of CPU work.  Returns (gflops, rows, secs)."""
+    import numpy as np
+    import oracle
+    c_in = C if w.beta != 0 else None
+    rows_done, secs, r0 = 0, 0.0, 0
+    n = first
+    max_rows = max_rows or w.M
+    while rows_done < max_rows:
+        n = min(n, max_rows - rows_done)
+        idx = np.arange(r0, r0 + n, dtype=np.int64)
+        t = time.perf_counter()
+        oracle.sgemm_rows(A, B, c_in, w.alpha, w.beta, idx, with_bound=False)
+        secs += time.perf_counter() - t
+        rows_done += n
+        r0 += n
+        if secs >= row_budget_s:
+            break
+        n *= 2
+    gflops = 2.0 * rows_done * w.N * w.K / secs / 1e9
+    return gflops, rows_done, secs
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    import numpy as np  # noqa: F401
+    from dense_fp32_gemm_02_gb300.workloads import BENCH_WORKLOAD, WORKLOADS, workload_inputs
+    w = WORKLOADS[args.workload or BENCH_WORKLOAD]
+    A, B, C = workload_inputs(w)
+    import oracle
+    rows_per_step = 8
+    c_in = C if w.beta != 0 else None
+
+    def step(i):
+        r0 = (i * rows_per_step) % w.M
+        idx = np.arange(r0, min(r0 + rows_per_step, w.M), dtype=np.int64)
+        oracle.sgemm_rows(A, B, c_in, w.alpha, w.beta, idx, with_bound=False)
+        return len(idx)
+
+    for i in range(args.warmup):
+        step(i)
+    t = time.perf_counter()
+    rows = sum(step(args.warmup + i) for i in range(args.steps))
+    secs = time.perf_counter() - t
+    gflops = 2.0 * rows * w.N * w.K / secs / 1e9
+    cores = host_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gflops, 3), "unit": "GFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64-accumulate", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
+                   "beta": w.beta, "sample": f"{rows_per_step} full output rows per step"},
+        "cpu_baseline": {"value": round(gflops, 3), "unit": "GFLOP/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{rows_per_step} rows x {w.N} cols x K={w.K} per step"},
+        "e2e": {"value": round(gflops, 3), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------- our arm
+def load_traffic(workload_name):
+    try:
+        with open(PROFILE_SUMMARY) as f:
+            d = json.load(f)
+        e = d.get(workload_name)
+        if e and e.get("kernel_revision") == kernel_revision():
+            return e.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def kernel_revision():
+    """Hash of the CUDA sources; a stored ncu traffic figure only counts for
+    the kernel it was measured on."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_fp32_gemm_02_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+
+    from dense_fp32_gemm_02_gb300 import binding
+    from dense_fp32_gemm_02_gb300.workloads import BENCH_WORKLOAD, WORKLOADS, workload_inputs
+    w = WORKLOADS[args.workload or BENCH_WORKLOAD]
+    A, B, C = workload_inputs(w)
+    props = torch.cuda.get_device_properties(device)
+    sms = props.multi_processor_count
+    stream = torch.cuda.Stream(device)
+
+    dA = torch.from_numpy(np.ascontiguousarray(A)).to(device)
+    dB = torch.from_numpy(np.ascontiguousarray(B)).to(device)
+    dC = torch.from_numpy(np.ascontiguousarray(C)).to(device) if C is not None else \
+        torch.zeros((w.M, w.N), device=device)
+    torch.cuda.synchronize()
+
+    def step():
+        binding.sgemm_into(dA, dB, dC, w.alpha, w.beta, stream=stream)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    if binding.device_status(stream=stream) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    # ---- timed region (device time, inputs resident)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    binding.profile_collect()
+    binding.profile_enable(True)
+    launches0 = binding.kernel_launch_count()
+    barrier(world, device)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    stop.record(stream)
+    stop.synchronize()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world, device)
+    launches = binding.kernel_launch_count() - launches0
+    binding.profile_enable(False)
+    prof = binding.profile_collect()
+    clocks.mark(t0, t1)
+    ms = start.elapsed_time(stop)
+    ms = max_over_ranks(world, ms, device)
+    if binding.device_status(stream=stream) != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    ms_per_step = ms / args.steps
+    gflops = w.flops / (ms_per_step * 1e-3) / 1e9 * world
+
+    # ---- end to end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        hA = torch.from_numpy(np.ascontiguousarray(A)).pin_memory()
+        hB = torch.from_numpy(np.ascontiguousarray(B)).pin_memory()
+        hC0 = torch.from_numpy(np.ascontiguousarray(C)) if C is not None else None
+        hC = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+        if hC0 is not None:
+            hC.copy_(hC0)
+        binding.sgemm_host(hA, hB, hC, w.alpha, w.beta, stream=stream)   # warm
+        barrier(world, device)
+        t = time.perf_counter()
+        te0 = time.time()
+        for _ in range(args.steps):
+            binding.sgemm_host(hA, hB, hC, w.alpha, w.beta, stream=stream)
+        e2e_s = time.perf_counter() - t
+        clocks.mark(te0, time.time())
+        e2e_s = max_over_ranks(world, e2e_s, device)
+        h2d = (hA.numel() + hB.numel() + (hC.numel() if w.beta != 0 else 0)) * 4
+        d2h = hC.numel() * 4
+        e2e = {"value": round(w.flops * args.steps / e2e_s / 1e9 * world, 3), "unit": "GFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_s / args.steps * 1e3, 3)}
+    clocks.stop()
+    clk = clocks.summary()
+
+    # ---- roofline of the main kernel (FP32 FFMA pipe)
+    main_ms = prof["main_ms"] / max(1, prof["main_launches"])
+    pack_ms = prof["pack_ms"] / max(1, prof["pack_launches"]) if prof["pack_launches"] else 0.0
+    achieved_tflops = w.flops / (main_ms * 1e-3) / 1e12 if main_ms > 0 else None
+    peak_tflops = sms * FFMA_PER_SM_PER_CLK * 2 * SM_MAX_MHZ_FALLBACK * 1e6 / 1e12
+    f_meas = clk.get("sm_mhz")
+    peak_meas = sms * FFMA_PER_SM_PER_CLK * 2 * f_meas * 1e6 / 1e12 if f_meas else None
+    roofline = {
+        "bound": "alu", "kernel": "sgemm_tma_ffma_kernel",
+        "achieved": round(achieved_tflops, 3) if achieved_tflops else None,
+        "peak": round(peak_tflops, 3), "unit": "TFLOP/s",
+        "frac": round(achieved_tflops / peak_tflops, 4) if achieved_tflops else None,
+        "traffic": load_traffic(w.name),
+        "peak_source": f"derived: {sms} SMs x 128 FFMA/clk x 2 FLOP x 2070 MHz max SM clock",
+        "frac_at_measured_clock": (round(achieved_tflops / peak_meas, 4)
+                                   if (achieved_tflops and peak_meas) else None),
+        "main_kernel_ms": round(main_ms, 4), "pack_kernels_ms": round(pack_ms, 4),
+        "algorithmic_flops_per_launch": w.flops,
+    }
+
+    # ---- CPU oracle baseline (rank 0 only, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        g, rows, secs = time_oracle_rows(w, A, B, C)
+        cpu = {"value": round(g, 3), "unit": "GFLOP/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"{rows} full output rows of the {w.M}x{w.N}x{w.K} workload "
+                         f"({secs:.1f} s of CPU work)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(gflops, 3), "unit": "GFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
+                       "beta": w.beta, "seed": w.seed,
+                       "l2": "inputs larger than L2 (A, B, C 805 MB vs 129 MB), no flush",
+                       "parallelism": "replicas" if world > 1 else "single_gpu",
+                       "kernel": binding.config_string(w.M, w.N, w.K)},
+            "pct_of_ffma_peak": round(100.0 * gflops / world / (peak_tflops * 1e3), 2),
+            "sm_count": sms,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": int(launches),
+            "clocks": {"sm_mhz": clk.get("sm_mhz"), "sm_max_mhz": clk.get("sm_max_mhz"),
+                       "reasons": clk.get("reasons"), "samples": clk.get("samples"),
+                       "power_w_median": clk.get("power_w_median")},
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

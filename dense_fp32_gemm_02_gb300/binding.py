@@ -1,0 +1,197 @@
+"""ctypes binding of libsgemm.so (argument marshalling only).
+
+Every computing function here hands pointers, sizes and a stream to the C ABI
+in include/sgemm.h; no arithmetic of the GEMM happens in Python.  Importing
+this module raises ImportError when the library has not been built (there is
+no fallback path).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+library_path = LIB_PATH
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libsgemm.so is not built at {LIB_PATH}; run "
+        "`python -c 'import __graft_entry__ as g; g.build()'` or "
+        "`python -m dense_fp32_gemm_02_gb300.build`")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_i, _f, _p = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+_ull, _ll, _d = ctypes.c_ulonglong, ctypes.c_longlong, ctypes.c_double
+
+lib.sgemm.argtypes = [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]
+lib.sgemm.restype = _i
+lib.sgemm_host.argtypes = [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]
+lib.sgemm_host.restype = _i
+lib.sgemm_status_string.argtypes = [_i]
+lib.sgemm_status_string.restype = ctypes.c_char_p
+lib.sgemm_version.argtypes = []
+lib.sgemm_version.restype = _i
+lib.sgemm_last_cuda_error.argtypes = []
+lib.sgemm_last_cuda_error.restype = _i
+lib.sgemm_device_status.argtypes = [_p]
+lib.sgemm_device_status.restype = _i
+lib.sgemm_set_wait_timeout_ns.argtypes = [_ull]
+lib.sgemm_set_wait_timeout_ns.restype = _i
+lib.sgemm_selftest_wait_timeout.argtypes = [_ull, _p]
+lib.sgemm_selftest_wait_timeout.restype = _i
+lib.sgemm_profile_enable.argtypes = [_i]
+lib.sgemm_profile_enable.restype = _i
+lib.sgemm_profile_collect.argtypes = [ctypes.POINTER(_d), ctypes.POINTER(_ll),
+                                      ctypes.POINTER(_d), ctypes.POINTER(_ll)]
+lib.sgemm_profile_collect.restype = _i
+lib.sgemm_kernel_launch_count.argtypes = []
+lib.sgemm_kernel_launch_count.restype = _ll
+lib.sgemm_config_string.argtypes = [_i, _i, _i]
+lib.sgemm_config_string.restype = ctypes.c_char_p
+
+SGEMM_OK = 0
+SGEMM_ERR_INVALID_ARG = 1
+SGEMM_ERR_UNSUPPORTED_DEVICE = 2
+SGEMM_ERR_CUDA = 3
+SGEMM_ERR_TIMEOUT = 4
+SGEMM_ERR_ALLOC = 5
+
+
+class SgemmError(RuntimeError):
+    def __init__(self, status: int):
+        self.status = status
+        msg = lib.sgemm_status_string(status).decode()
+        if status in (SGEMM_ERR_CUDA, SGEMM_ERR_ALLOC):
+            msg += f" (cuda error {lib.sgemm_last_cuda_error()})"
+        super().__init__(msg)
+
+
+def check(status: int) -> int:
+    if status != SGEMM_OK:
+        raise SgemmError(status)
+    return status
+
+
+def status_string(status: int) -> str:
+    return lib.sgemm_status_string(status).decode()
+
+
+def version() -> int:
+    return lib.sgemm_version()
+
+
+# ------------------------------------------------------------------ tensors
+def _ld(t, width: int) -> int:
+    """Row pitch (elements) of a 2-D row-major tensor/array view."""
+    if t.dim() != 2:
+        raise ValueError("expected a 2-D tensor")
+    if t.numel() > 0 and t.size(1) > 1 and t.stride(1) != 1:
+        raise ValueError("rows must be contiguous (stride(1) == 1)")
+    ld = t.stride(0) if (t.size(0) > 1 and t.numel() > 0) else 0
+    return max(ld, width, 1)
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _shapes(A, B, C):
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: A {tuple(A.shape)}, B {tuple(B.shape)}")
+    if tuple(C.shape) != (M, N):
+        raise ValueError(f"C must be {(M, N)}, got {tuple(C.shape)}")
+    return M, N, K
+
+
+def sgemm_into(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C <- alpha*A@B + beta*C on CUDA float32 tensors (row-major, any row pitch).
+    Asynchronous on `stream` (default: torch's current stream of C's device)."""
+    import torch
+    for name, t in (("A", A), ("B", B), ("C", C)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA float32 tensor")
+    if not (A.device == B.device == C.device):
+        raise ValueError("A, B and C must be on the same device")
+    M, N, K = _shapes(A, B, C)
+    with torch.cuda.device(C.device):
+        st = lib.sgemm(M, N, K, float(alpha), A.data_ptr(), _ld(A, K), B.data_ptr(), _ld(B, N),
+                       float(beta), C.data_ptr(), _ld(C, N), _stream_handle(stream, C.device))
+    check(st)
+    return C
+
+
+def sgemm(A, B, C=None, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """alpha*A@B + beta*C.  With C=None a new tensor is returned (beta must be 0);
+    otherwise C is updated in place and returned."""
+    import torch
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs an input C")
+        C = torch.empty((A.shape[0], B.shape[1]), dtype=torch.float32, device=A.device)
+    return sgemm_into(A, B, C, alpha, beta, stream)
+
+
+def sgemm_host(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None, device=None):
+    """The host-buffer entry point: A, B, C are CPU float32 tensors (pinned for
+    speed).  C is overwritten with alpha*A@B + beta*C; synchronous."""
+    import torch
+    for name, t in (("A", A), ("B", B), ("C", C)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.is_cuda:
+            raise TypeError(f"{name} must be a CPU float32 tensor")
+    M, N, K = _shapes(A, B, C)
+    device = torch.device(device) if device is not None else \
+        torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(device):
+        st = lib.sgemm_host(M, N, K, float(alpha), A.data_ptr(), _ld(A, K), B.data_ptr(),
+                            _ld(B, N), float(beta), C.data_ptr(), _ld(C, N),
+                            _stream_handle(stream, device))
+    check(st)
+    return C
+
+
+# ------------------------------------------------------------------ control
+def device_status(stream=None, device=None) -> int:
+    """Synchronise and read/clear the device error word: 0 or SGEMM_ERR_TIMEOUT."""
+    import torch
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(device):
+        return lib.sgemm_device_status(_stream_handle(stream, device))
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    check(lib.sgemm_set_wait_timeout_ns(int(ns)))
+
+
+def selftest_wait_timeout(ns: int, stream=None, device=None) -> int:
+    import torch
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(device):
+        return lib.sgemm_selftest_wait_timeout(int(ns), _stream_handle(stream, device))
+
+
+def profile_enable(on: bool = True) -> None:
+    check(lib.sgemm_profile_enable(1 if on else 0))
+
+
+def profile_collect() -> dict:
+    mm, pm = ctypes.c_double(0), ctypes.c_double(0)
+    mn, pn = ctypes.c_longlong(0), ctypes.c_longlong(0)
+    check(lib.sgemm_profile_collect(ctypes.byref(mm), ctypes.byref(mn), ctypes.byref(pm),
+                                    ctypes.byref(pn)))
+    return {"main_ms": mm.value, "main_launches": mn.value,
+            "pack_ms": pm.value, "pack_launches": pn.value}
+
+
+def kernel_launch_count() -> int:
+    return lib.sgemm_kernel_launch_count()
+
+
+def config_string(M: int, N: int, K: int) -> str:
+    return lib.sgemm_config_string(M, N, K).decode()

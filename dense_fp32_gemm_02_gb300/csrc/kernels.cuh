@@ -1,0 +1,394 @@
+// kernels.cuh -- device code of the FP32 SGEMM: the A-transpose pre-pass, the
+// B re-pitch copy, the persistent TMA-fed FFMA main kernel, the alpha==0 / K==0
+// scaling kernel and the bounded-wait self test.
+//
+// Design, in terms of the techniques the SGEMM pages describe:
+//  * block tiling with a K slab staged in shared memory per step and an
+//    outer-product register micro-tile per thread ("How to implement matrix
+//    multiplication efficiently?", sections "Tiling" and "Thread-level
+//    optimisation");
+//  * A stored transposed in shared memory so one thread reads its column of A
+//    with 128-bit loads (same article, "Bank conflicts" section; "SGEMM CUDA
+//    kernel (Second Half)", Part 8 "Transposed As").  Here the transpose is a
+//    pre-pass into global memory so that the tensor-memory accelerator (TMA)
+//    can copy A tiles exactly like B tiles;
+//  * double buffering, generalised to an S-stage ring of TMA copies guarded by
+//    full/empty shared-memory barriers, with one producer warp;
+//  * the zig-zag lane map of "SGEMM CUDA kernel (Second Half)" (section
+//    "LDS.128 Shared Memory Transactions"): for A reads lane i and lane i^1
+//    fetch the same address, for B reads lane i and lane i^2 do, so the
+//    quarter-warp transactions of every 128-bit shared load merge in pairs;
+//  * zero-filled edge tiles (the TMA fills out-of-range box elements with 0)
+//    and guarded stores, as in exercise 1 of "3.3 Shared memory and tiling".
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace sg {
+
+// device error word bits
+enum : unsigned {
+    ERR_FULL_WAIT = 1u,    // consumer gave up waiting for a TMA copy
+    ERR_EMPTY_WAIT = 2u,   // producer gave up waiting for a free stage
+    ERR_DRAIN_WAIT = 4u,   // copies still in flight after an abort
+    ERR_SELFTEST = 8u,     // the bounded-wait self test expired (expected)
+};
+
+// One word per device; every kernel of this library reports expiries here.
+__device__ unsigned int g_error_word = 0;
+
+// ------------------------------------------------------------------ configuration
+// Lanes of a warp form a LANES_M x LANES_N = 4 x 8 grid.  A thread owns a
+// TM x TN tile made of (TM/4) x (TN/4) sub-tiles of 4x4 spaced 16 rows and 32
+// columns apart, so a warp covers (4*TM) x (8*TN) outputs.
+template <int BM_, int BN_, int BK_, int STAGES_, int WARPS_M_, int WARPS_N_, int TM_, int TN_,
+          bool PAIRED_>
+struct TileConfig {
+    static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
+    static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_;
+    static constexpr int TM = TM_, TN = TN_;
+    static constexpr int LANES_M = 4, LANES_N = 8;
+    static constexpr int WM = TM * LANES_M, WN = TN * LANES_N;
+    static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
+    static constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
+    // PAIRED: the transposed A holds every element twice (a, a), so one 128-bit
+    // shared load yields two ready-made (a_i, a_i) operand pairs for the packed
+    // FP32x2 fused multiply-add; otherwise scalar FFMA.
+    static constexpr bool PAIRED = PAIRED_;
+    static constexpr int A_ROW = PAIRED ? 2 * BM : BM;   // floats per K-row of the A tile
+    static constexpr int A_STAGE = BK * A_ROW;           // floats
+    static constexpr int B_STAGE = BK * BN;              // floats
+    static constexpr uint32_t STAGE_BYTES = uint32_t(A_STAGE + B_STAGE) * 4u;
+    static constexpr size_t SMEM_BYTES =
+        size_t(STAGES) * STAGE_BYTES + 2 * STAGES * sizeof(uint64_t) + 16 + 1024;
+
+    static_assert(WM * WARPS_M == BM && WN * WARPS_N == BN, "warp grid must cover the tile");
+    static_assert(TM % 4 == 0 && TN % 4 == 0, "thread tile is made of 4x4 sub-tiles");
+    static_assert(A_ROW <= 256 && BN <= 256 && BK <= 256, "TMA box edge is at most 256");
+    static_assert((A_STAGE * 4) % 1024 == 0 && (B_STAGE * 4) % 1024 == 0, "stage alignment");
+};
+
+struct MainParams {
+    float *C;
+    long long ldc;
+    int M, N, K;
+    float alpha, beta;
+    int tiles_m, tiles_n, group_m;
+    int c_vec4;              // C base 16-byte aligned and ldc % 4 == 0
+    unsigned long long timeout_ns;
+};
+
+// Grouped raster: tiles are visited in groups of `group_m` tile-rows, column
+// by column inside a group, so CTAs running at the same time share rows of A
+// and columns of B in L2 (the wave / L2 hit-rate argument of the Hands-on-GEMM
+// article, "Block-level optimisation").
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int group_m,
+                                            int &tm, int &tn) {
+    const int per_group = group_m * tiles_n;
+    const int g = tile / per_group;
+    const int first_m = g * group_m;
+    const int gm = min(tiles_m - first_m, group_m);
+    const int local = tile - g * per_group;
+    tm = first_m + local % gm;
+    tn = local / gm;
+}
+
+// ------------------------------------------------------------------ main kernel
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
+    sgemm_tma_ffma_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB, const MainParams p) {
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
+    constexpr int TM = Cfg::TM, TN = Cfg::TN;
+    constexpr int A_ROW = Cfg::A_ROW;
+
+    extern __shared__ unsigned char smem_raw[];
+    const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
+    float *sA = reinterpret_cast<float *>(base);
+    float *sB = sA + STAGES * Cfg::A_STAGE;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * Cfg::B_STAGE);
+    uint64_t *empty = full + STAGES;
+    int *abort_flag = reinterpret_cast<int *>(empty + STAGES);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], Cfg::CONSUMER_WARPS);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int num_tiles = p.tiles_m * p.tiles_n;
+    const int k_tiles = (p.K + BK - 1) / BK;
+
+    // producer bookkeeping (lane 0 of the producer warp)
+    long long issued = 0;
+
+    if (warp == Cfg::CONSUMER_WARPS) {
+        // ---------------------------------------------------------- producer warp
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                int tm, tn;
+                tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                const int a_x = (Cfg::PAIRED ? 2 : 1) * tm * BM;
+                const int b_x = tn * BN;
+                for (int kt = 0; kt < k_tiles; ++kt) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns)) {
+                        atomicOr(&g_error_word, ERR_EMPTY_WAIT);
+                        *abort_flag = 1;
+                        goto producer_done;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+                    tma_load_2d(sA + stage * Cfg::A_STAGE, &tmA, &full[stage], a_x, kt * BK);
+                    tma_load_2d(sB + stage * Cfg::B_STAGE, &tmB, &full[stage], b_x, kt * BK);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        producer_done:;
+        }
+    } else {
+        // ---------------------------------------------------------- consumer warps
+        const int wm0 = (warp % Cfg::WARPS_M) * Cfg::WM;
+        const int wn0 = (warp / Cfg::WARPS_M) * Cfg::WN;
+        // zig-zag lane map: lane bits {1,4} -> row group, bits {0,2,3} -> column group
+        const int lm = ((lane >> 1) & 1) | ((lane >> 3) & 2);
+        const int ln = (lane & 1) | ((lane >> 1) & 6);
+
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            int tm, tn;
+            tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+
+            float acc[TM][TN];
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+
+            for (int kt = 0; kt < k_tiles; ++kt) {
+                bool ok = mbar_wait(&full[stage], phase, p.timeout_ns);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    if (lane == 0) {
+                        atomicOr(&g_error_word, ERR_FULL_WAIT);
+                        *abort_flag = 1;
+                    }
+                    goto consumer_done;
+                }
+                const float *a_s = sA + stage * Cfg::A_STAGE;
+                const float *b_s = sB + stage * Cfg::B_STAGE;
+#pragma unroll
+                for (int kk = 0; kk < BK; ++kk) {
+                    float b[TN];
+#pragma unroll
+                    for (int t = 0; t < TN / 4; ++t) {
+                        const float4 v = *reinterpret_cast<const float4 *>(
+                            b_s + kk * BN + wn0 + t * 32 + ln * 4);
+                        b[4 * t + 0] = v.x;
+                        b[4 * t + 1] = v.y;
+                        b[4 * t + 2] = v.z;
+                        b[4 * t + 3] = v.w;
+                    }
+                    if constexpr (Cfg::PAIRED) {
+                        // (a_i, a_i) pairs straight from the duplicated layout
+                        float2 a2[TM];
+#pragma unroll
+                        for (int s = 0; s < TM / 4; ++s) {
+                            const float *src = a_s + kk * A_ROW + 2 * (wm0 + s * 16 + lm * 4);
+                            const float4 v0 = *reinterpret_cast<const float4 *>(src);
+                            const float4 v1 = *reinterpret_cast<const float4 *>(src + 4);
+                            a2[4 * s + 0] = make_float2(v0.x, v0.y);
+                            a2[4 * s + 1] = make_float2(v0.z, v0.w);
+                            a2[4 * s + 2] = make_float2(v1.x, v1.y);
+                            a2[4 * s + 3] = make_float2(v1.z, v1.w);
+                        }
+#pragma unroll
+                        for (int i = 0; i < TM; ++i)
+#pragma unroll
+                            for (int j = 0; j < TN; j += 2) {
+                                const float2 r = ffma2(a2[i], make_float2(b[j], b[j + 1]),
+                                                       make_float2(acc[i][j], acc[i][j + 1]));
+                                acc[i][j] = r.x;
+                                acc[i][j + 1] = r.y;
+                            }
+                    } else {
+                        float a[TM];
+#pragma unroll
+                        for (int s = 0; s < TM / 4; ++s) {
+                            const float4 v = *reinterpret_cast<const float4 *>(
+                                a_s + kk * A_ROW + wm0 + s * 16 + lm * 4);
+                            a[4 * s + 0] = v.x;
+                            a[4 * s + 1] = v.y;
+                            a[4 * s + 2] = v.z;
+                            a[4 * s + 3] = v.w;
+                        }
+#pragma unroll
+                        for (int i = 0; i < TM; ++i)
+#pragma unroll
+                            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+
+            // ---------------------------------------------------------- epilogue
+            {
+                const int row0 = tm * BM + wm0 + lm * 4;
+                const int col0 = tn * BN + wn0 + ln * 4;
+                const float alpha = p.alpha, beta = p.beta;
+#pragma unroll
+                for (int s = 0; s < TM / 4; ++s) {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int row = row0 + s * 16 + r;
+                        if (row >= p.M) continue;
+                        float *crow = p.C + (long long)row * p.ldc;
+#pragma unroll
+                        for (int t = 0; t < TN / 4; ++t) {
+                            const int col = col0 + t * 32;
+                            const float *v = &acc[4 * s + r][4 * t];
+                            if (p.c_vec4 && col + 3 < p.N) {
+                                float4 o;
+                                if (beta != 0.0f) {
+                                    const float4 c = __ldcs(reinterpret_cast<const float4 *>(crow + col));
+                                    o.x = fmaf(alpha, v[0], beta * c.x);
+                                    o.y = fmaf(alpha, v[1], beta * c.y);
+                                    o.z = fmaf(alpha, v[2], beta * c.z);
+                                    o.w = fmaf(alpha, v[3], beta * c.w);
+                                } else {
+                                    o.x = alpha * v[0];
+                                    o.y = alpha * v[1];
+                                    o.z = alpha * v[2];
+                                    o.w = alpha * v[3];
+                                }
+                                __stcs(reinterpret_cast<float4 *>(crow + col), o);
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    if (col + e < p.N) {
+                                        const float c = (beta != 0.0f) ? beta * crow[col + e] : 0.0f;
+                                        crow[col + e] = (beta != 0.0f) ? fmaf(alpha, v[e], c)
+                                                                       : alpha * v[e];
+                                    }
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    consumer_done:;
+    }
+
+    __syncthreads();
+    // After an abort, wait (bounded) for every TMA copy this CTA may still have in
+    // flight before the CTA's shared memory is released.
+    if (warp == Cfg::CONSUMER_WARPS && lane == 0 && *abort_flag) {
+        const long long first = issued > STAGES ? issued - STAGES : 0;
+        for (long long q = first; q < issued; ++q) {
+            const int s = int(q % STAGES);
+            const uint32_t ph = uint32_t((q / STAGES) & 1);
+            if (!mbar_wait(&full[s], ph, p.timeout_ns)) {
+                atomicOr(&g_error_word, ERR_DRAIN_WAIT);
+                break;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ pre-pass
+// At[k][x] = A[m][k] with x = m (plain) or x = 2m and 2m+1 (paired).  32x32
+// tiles through shared memory: coalesced reads along k, coalesced writes along m.
+template <bool PAIRED>
+__global__ void __launch_bounds__(256)
+    pack_a_transpose_kernel(const float *__restrict__ A, long long lda, int M, int K,
+                            float *__restrict__ At, long long ldat) {
+    __shared__ float tile[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
+    for (long long m0 = (long long)blockIdx.y * 32; m0 < M; m0 += (long long)gridDim.y * 32) {
+        for (long long k0 = (long long)blockIdx.x * 32; k0 < K; k0 += (long long)gridDim.x * 32) {
+#pragma unroll
+            for (int r = ty; r < 32; r += 8) {
+                const long long m = m0 + r, k = k0 + tx;
+                tile[r][tx] = (m < M && k < K) ? __ldcs(A + m * lda + k) : 0.0f;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int r = ty; r < 32; r += 8) {
+                const long long k = k0 + r, m = m0 + tx;
+                if (k < K && m < M) {
+                    const float v = tile[tx][r];
+                    if constexpr (PAIRED)
+                        *reinterpret_cast<float2 *>(At + k * ldat + 2 * m) = make_float2(v, v);
+                    else
+                        At[k * ldat + m] = v;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// Bp[k][n] = B[k][n] with a 16-byte row pitch (ldbp % 4 == 0) for the TMA.
+__global__ void __launch_bounds__(256)
+    pack_b_copy_kernel(const float *__restrict__ B, long long ldb, int K, int N,
+                       float *__restrict__ Bp, long long ldbp) {
+    const long long total = (long long)K * N;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long k = idx / N, n = idx - k * N;
+        Bp[k * ldbp + n] = B[k * ldb + n];
+    }
+}
+
+// C = beta * C on the M x N block (C not read when beta == 0): the alpha == 0 /
+// K == 0 case, where A and B are not read.
+__global__ void __launch_bounds__(256)
+    scale_c_kernel(float *C, long long ldc, int M, int N, float beta) {
+    const long long total = (long long)M * N;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long i = idx / N, j = idx - i * N;
+        float *c = C + i * ldc + j;
+        *c = (beta == 0.0f) ? 0.0f : beta * *c;
+    }
+}
+
+// One thread waits on a barrier that nothing completes; the bounded wait must
+// expire, record ERR_SELFTEST and return.
+__global__ void wait_timeout_selftest_kernel(unsigned long long timeout_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (!mbar_wait(&bar, 0u, timeout_ns)) atomicOr(&g_error_word, ERR_SELFTEST);
+    }
+}
+
+}  // namespace sg

@@ -1,0 +1,432 @@
+// sgemm.cu -- host side of libsgemm.so: the C ABI declared in include/sgemm.h,
+// argument checks, per-device state, the stream-ordered workspace pool, TMA
+// descriptor encoding, kernel selection and launch, and benchmark timing hooks.
+//
+// Path of one sgemm() call (all on the caller's stream, no host sync):
+//   1. pack_a_transpose_kernel: A (M x K, any lda) -> At (K x M, paired: K x 2M)
+//   2. pack_b_copy_kernel, only when B's address or row pitch is not 16-byte
+//      aligned as the TMA requires
+//   3. sgemm_tma_ffma_kernel: persistent CTAs, TMA ring, FFMA micro-tiles,
+//      alpha/beta epilogue straight to C
+//   4. the workspace goes back to the pool, ordered after step 3.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/sgemm.h"
+#include "kernels.cuh"
+
+#define SGEMM_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+constexpr int kMaxDevices = 64;
+
+thread_local int t_last_cuda_error = 0;
+
+// Kernel configuration used for every shape in this version.
+using MainCfg = sg::TileConfig<128, 128, 16, 6, 4, 2, 8, 8, /*PAIRED=*/true>;
+
+struct DeviceState {
+    bool ready = false;
+    int status = SGEMM_OK;
+    int sm_count = 0;
+    cudaMemPool_t pool = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+std::atomic<long long> g_launches{0};
+
+// ------------------------------------------------------------------ profiling
+struct ProfRecord {
+    cudaEvent_t start, stop;
+    bool is_main;
+};
+std::mutex g_prof_mutex;
+std::atomic<int> g_prof_on{0};
+std::vector<ProfRecord> g_prof_used;
+std::vector<cudaEvent_t> g_prof_free;
+
+cudaEvent_t prof_event() {
+    // caller holds g_prof_mutex
+    if (!g_prof_free.empty()) {
+        cudaEvent_t e = g_prof_free.back();
+        g_prof_free.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+struct ProfScope {
+    cudaEvent_t start = nullptr, stop = nullptr;
+    cudaStream_t stream;
+    bool is_main;
+    ProfScope(cudaStream_t s, bool main) : stream(s), is_main(main) {
+        if (!g_prof_on.load()) return;
+        std::lock_guard<std::mutex> lk(g_prof_mutex);
+        start = prof_event();
+        stop = prof_event();
+        if (start && stop) cudaEventRecord(start, stream);
+    }
+    ~ProfScope() {
+        if (!start || !stop) return;
+        cudaEventRecord(stop, stream);
+        std::lock_guard<std::mutex> lk(g_prof_mutex);
+        g_prof_used.push_back({start, stop, is_main});
+    }
+};
+
+// ------------------------------------------------------------------ helpers
+int cuda_fail(cudaError_t e) {
+    t_last_cuda_error = int(e);
+    return (e == cudaErrorMemoryAllocation) ? SGEMM_ERR_ALLOC : SGEMM_ERR_CUDA;
+}
+
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int checked_args(int M, int N, int K, const float *A, int lda, const float *B, int ldb,
+                 const float *C, int ldc, float alpha, float beta) {
+    if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+    if (lda < std::max(1, K) || ldb < std::max(1, N) || ldc < std::max(1, N))
+        return SGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    if (!C || !aligned4(C)) return SGEMM_ERR_INVALID_ARG;
+    if (K > 0 && alpha != 0.0f) {
+        if (!A || !B || !aligned4(A) || !aligned4(B)) return SGEMM_ERR_INVALID_ARG;
+    }
+    (void)beta;
+    return SGEMM_OK;
+}
+
+// Lazily initialise per-device state for the current device.
+int device_state(DeviceState **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    DeviceState &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if (major != 10 || minor != 3) {
+            d.status = SGEMM_ERR_UNSUPPORTED_DEVICE;
+        } else {
+            if (!g_encode_tiled) {
+                void *fn = nullptr;
+                cudaDriverEntryPointQueryResult q;
+                e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+                if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                    return cuda_fail(e != cudaSuccess ? e : cudaErrorNotSupported);
+                g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+            }
+            cudaMemPoolProps props;
+            std::memset(&props, 0, sizeof(props));
+            props.allocType = cudaMemAllocationTypePinned;
+            props.handleTypes = cudaMemHandleTypeNone;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            if ((e = cudaMemPoolCreate(&d.pool, &props)) != cudaSuccess) return cuda_fail(e);
+            // keep up to 4 GiB of released workspace cached for reuse
+            cuuint64_t keep = 4ull << 30;
+            cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+            e = cudaFuncSetAttribute(sg::sgemm_tma_ffma_kernel<MainCfg>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     int(MainCfg::SMEM_BYTES));
+            if (e != cudaSuccess) return cuda_fail(e);
+            d.status = SGEMM_OK;
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return d.status;
+}
+
+int encode_2d(CUtensorMap *map, const float *ptr, uint64_t inner, uint64_t outer,
+              uint64_t row_pitch_elems, uint32_t box_inner, uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_pitch_elems * sizeof(float)};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = int(r);
+        return SGEMM_ERR_CUDA;
+    }
+    return SGEMM_OK;
+}
+
+int launch_scale(cudaStream_t stream, float *C, int ldc, int M, int N, float beta, int sms) {
+    const long long total = (long long)M * N;
+    const int blocks = int(std::min<long long>((total + 255) / 256, (long long)sms * 8));
+    sg::scale_c_kernel<<<blocks, 256, 0, stream>>>(C, ldc, M, N, beta);
+    g_launches.fetch_add(1);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SGEMM_OK : cuda_fail(e);
+}
+
+long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
+
+int sgemm_device(int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+                 int ldb, float beta, float *C, int ldc, cudaStream_t stream) {
+    int st = checked_args(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta);
+    if (st != SGEMM_OK || M == 0 || N == 0) return st;
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != SGEMM_OK) return st;
+
+    if (K == 0 || alpha == 0.0f) return launch_scale(stream, C, ldc, M, N, beta, dev->sm_count);
+
+    using Cfg = MainCfg;
+    // ---- workspace: transposed (paired) A, and a re-pitched B if needed
+    const long long a_inner = (Cfg::PAIRED ? 2LL : 1LL) * M;
+    const long long ldat = round_up(a_inner, 4);
+    const bool b_direct = aligned16(B) && (ldb % 4 == 0);
+    const long long ldbp = b_direct ? ldb : round_up(N, 4);
+    const size_t at_bytes = size_t(K) * size_t(ldat) * sizeof(float);
+    const size_t bp_bytes = b_direct ? 0 : size_t(K) * size_t(ldbp) * sizeof(float);
+    const size_t ws_bytes = round_up((long long)at_bytes, 256) + bp_bytes;
+
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, ws_bytes, dev->pool, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    float *At = static_cast<float *>(ws);
+    float *Bp = b_direct ? const_cast<float *>(B)
+                         : reinterpret_cast<float *>(static_cast<char *>(ws) +
+                                                     round_up((long long)at_bytes, 256));
+
+    {
+        ProfScope prof(stream, false);
+        dim3 grid(unsigned(std::min<long long>((K + 31) / 32, 1LL << 20)),
+                  unsigned(std::min<long long>((M + 31) / 32, 65535)));
+        sg::pack_a_transpose_kernel<Cfg::PAIRED><<<grid, 256, 0, stream>>>(A, lda, M, K, At, ldat);
+        g_launches.fetch_add(1);
+        if (!b_direct) {
+            const long long total = (long long)K * N;
+            const int blocks = int(std::min<long long>((total + 255) / 256, (long long)dev->sm_count * 16));
+            sg::pack_b_copy_kernel<<<blocks, 256, 0, stream>>>(B, ldb, K, N, Bp, ldbp);
+            g_launches.fetch_add(1);
+        }
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        cudaFreeAsync(ws, stream);
+        return cuda_fail(e);
+    }
+
+    CUtensorMap tmA, tmB;
+    if ((st = encode_2d(&tmA, At, a_inner, K, ldat, Cfg::A_ROW, Cfg::BK)) != SGEMM_OK ||
+        (st = encode_2d(&tmB, Bp, N, K, ldbp, Cfg::BN, Cfg::BK)) != SGEMM_OK) {
+        cudaFreeAsync(ws, stream);
+        return st;
+    }
+
+    sg::MainParams p;
+    p.C = C;
+    p.ldc = ldc;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.tiles_m = int((M + Cfg::BM - 1) / Cfg::BM);
+    p.tiles_n = int((N + Cfg::BN - 1) / Cfg::BN);
+    p.group_m = 16;
+    p.c_vec4 = (aligned16(C) && ldc % 4 == 0) ? 1 : 0;
+    p.timeout_ns = g_timeout_ns.load();
+    const long long tiles = (long long)p.tiles_m * p.tiles_n;
+    const int grid = int(std::min<long long>(tiles, dev->sm_count));
+    {
+        ProfScope prof(stream, true);
+        sg::sgemm_tma_ffma_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        g_launches.fetch_add(1);
+    }
+    e = cudaGetLastError();
+    cudaError_t ef = cudaFreeAsync(ws, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (ef != cudaSuccess) return cuda_fail(ef);
+    return SGEMM_OK;
+}
+
+int read_and_clear_error_word(cudaStream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned v = 0, zero = 0;
+    if ((e = cudaMemcpyFromSymbol(&v, sg::g_error_word, sizeof(v))) != cudaSuccess) return cuda_fail(e);
+    if (v && (e = cudaMemcpyToSymbol(sg::g_error_word, &zero, sizeof(zero))) != cudaSuccess)
+        return cuda_fail(e);
+    return v ? SGEMM_ERR_TIMEOUT : SGEMM_OK;
+}
+
+}  // namespace
+
+// ==================================================================== C ABI
+SGEMM_API int sgemm(int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+                    int ldb, float beta, float *C, int ldc, sgemm_stream_t stream) {
+    return sgemm_device(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+SGEMM_API int sgemm_host(int M, int N, int K, float alpha, const float *A, int lda,
+                         const float *B, int ldb, float beta, float *C, int ldc,
+                         sgemm_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int st = checked_args(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta);
+    if (st != SGEMM_OK || M == 0 || N == 0) return st;
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != SGEMM_OK) return st;
+
+    const bool need_ab = (K > 0 && alpha != 0.0f);
+    const bool need_c_in = (beta != 0.0f);
+    const size_t a_bytes = need_ab ? size_t(M) * K * sizeof(float) : 0;
+    const size_t b_bytes = need_ab ? size_t(K) * N * sizeof(float) : 0;
+    const size_t c_bytes = size_t(M) * N * sizeof(float);
+    const size_t off_b = size_t(round_up((long long)a_bytes, 256));
+    const size_t off_c = off_b + size_t(round_up((long long)b_bytes, 256));
+    void *buf = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&buf, off_c + c_bytes, dev->pool, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    char *base = static_cast<char *>(buf);
+    float *dA = reinterpret_cast<float *>(base);
+    float *dB = reinterpret_cast<float *>(base + off_b);
+    float *dC = reinterpret_cast<float *>(base + off_c);
+
+    if (need_ab) {
+        e = cudaMemcpy2DAsync(dA, size_t(K) * sizeof(float), A, size_t(lda) * sizeof(float),
+                              size_t(K) * sizeof(float), size_t(M), cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(dB, size_t(N) * sizeof(float), B, size_t(ldb) * sizeof(float),
+                                  size_t(N) * sizeof(float), size_t(K), cudaMemcpyHostToDevice,
+                                  stream);
+    }
+    if (e == cudaSuccess && need_c_in)
+        e = cudaMemcpy2DAsync(dC, size_t(N) * sizeof(float), C, size_t(ldc) * sizeof(float),
+                              size_t(N) * sizeof(float), size_t(M), cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) {
+        cudaFreeAsync(buf, stream);
+        cudaStreamSynchronize(stream);
+        return cuda_fail(e);
+    }
+    st = sgemm_device(M, N, K, alpha, need_ab ? dA : nullptr, std::max(1, K),
+                      need_ab ? dB : nullptr, std::max(1, N), beta, dC, N, stream);
+    if (st == SGEMM_OK) {
+        e = cudaMemcpy2DAsync(C, size_t(ldc) * sizeof(float), dC, size_t(N) * sizeof(float),
+                              size_t(N) * sizeof(float), size_t(M), cudaMemcpyDeviceToHost, stream);
+        if (e != cudaSuccess) st = cuda_fail(e);
+    }
+    cudaFreeAsync(buf, stream);
+    e = cudaStreamSynchronize(stream);
+    if (st == SGEMM_OK && e != cudaSuccess) st = cuda_fail(e);
+    return st;
+}
+
+SGEMM_API const char *sgemm_status_string(int status) {
+    switch (status) {
+        case SGEMM_OK: return "SGEMM_OK: success";
+        case SGEMM_ERR_INVALID_ARG: return "SGEMM_ERR_INVALID_ARG: invalid size, leading dimension or pointer";
+        case SGEMM_ERR_UNSUPPORTED_DEVICE: return "SGEMM_ERR_UNSUPPORTED_DEVICE: the current device is not sm_103";
+        case SGEMM_ERR_CUDA: return "SGEMM_ERR_CUDA: a CUDA call failed (see sgemm_last_cuda_error)";
+        case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT: a bounded in-kernel wait expired";
+        case SGEMM_ERR_ALLOC: return "SGEMM_ERR_ALLOC: workspace allocation failed";
+        default: return "unknown sgemm status";
+    }
+}
+
+SGEMM_API int sgemm_version(void) { return kVersion; }
+
+SGEMM_API int sgemm_last_cuda_error(void) { return t_last_cuda_error; }
+
+SGEMM_API int sgemm_device_status(sgemm_stream_t stream) {
+    DeviceState *dev = nullptr;
+    int st = device_state(&dev);
+    if (st != SGEMM_OK) return st;
+    return read_and_clear_error_word(reinterpret_cast<cudaStream_t>(stream));
+}
+
+SGEMM_API int sgemm_set_wait_timeout_ns(unsigned long long ns) {
+    if (ns < 1000ull) return SGEMM_ERR_INVALID_ARG;
+    g_timeout_ns.store(ns);
+    return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_selftest_wait_timeout(unsigned long long ns, sgemm_stream_t stream_) {
+    if (ns < 1000ull || ns > 10000000000ull) return SGEMM_ERR_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    DeviceState *dev = nullptr;
+    int st = device_state(&dev);
+    if (st != SGEMM_OK) return st;
+    // start from a clear error word so the result reflects this launch only
+    st = read_and_clear_error_word(stream);
+    if (st == SGEMM_ERR_CUDA) return st;
+    sg::wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(ns);
+    g_launches.fetch_add(1);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return read_and_clear_error_word(stream);
+}
+
+SGEMM_API int sgemm_profile_enable(int on) {
+    g_prof_on.store(on ? 1 : 0);
+    return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_profile_collect(double *main_ms, long long *main_launches, double *pack_ms,
+                                    long long *pack_launches) {
+    std::lock_guard<std::mutex> lk(g_prof_mutex);
+    double mm = 0.0, pm = 0.0;
+    long long mn = 0, pn = 0;
+    int st = SGEMM_OK;
+    for (auto &r : g_prof_used) {
+        float ms = 0.0f;
+        cudaError_t e = cudaEventSynchronize(r.stop);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.start, r.stop);
+        if (e != cudaSuccess) {
+            st = cuda_fail(e);
+        } else if (r.is_main) {
+            mm += ms;
+            ++mn;
+        } else {
+            pm += ms;
+            ++pn;
+        }
+        g_prof_free.push_back(r.start);
+        g_prof_free.push_back(r.stop);
+    }
+    g_prof_used.clear();
+    if (main_ms) *main_ms = mm;
+    if (main_launches) *main_launches = mn;
+    if (pack_ms) *pack_ms = pm;
+    if (pack_launches) *pack_launches = pn;
+    return st;
+}
+
+SGEMM_API long long sgemm_kernel_launch_count(void) { return g_launches.load(); }
+
+SGEMM_API const char *sgemm_config_string(int M, int N, int K) {
+    (void)M;
+    (void)N;
+    (void)K;
+    return "tma_ffma2 BM=128 BN=128 BK=16 stages=6 warps=4x2(+1 producer) thread_tile=8x8 "
+           "a_layout=transposed_paired";
+}

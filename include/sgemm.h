@@ -1,0 +1,150 @@
+/*
+ * sgemm.h -- C ABI of the GB300 (sm_103a) FP32 SGEMM library, libsgemm.so.
+ *
+ * Operation (all entry points that compute):
+ *
+ *     C[i*ldc + j] = alpha * sum_{k<K} A[i*lda + k] * B[k*ldb + j]  +  beta * C[i*ldc + j]
+ *
+ * for 0 <= i < M, 0 <= j < N: row-major FP32, A is M x K, B is K x N, C is M x N.
+ * This is the computation stated with the naive kernel of "How to implement
+ * matrix multiplication efficiently? An introduction from a CUDA beginner's
+ * view" (makelele.cn repost of the Hands-on-GEMM article, section "Naive GEMM
+ * and prerequisites": row-major A (M rows, K columns), B (K rows, N columns),
+ * C (M rows, N columns), c = alpha*A*B + beta*C with alpha applied after the
+ * k sum), with BLAS-style leading dimensions added.
+ *
+ * Conventions shared by every entry point:
+ *  - Sizes are elements.  lda >= max(1,K), ldb >= max(1,N), ldc >= max(1,N).
+ *  - beta == 0: C is not read on input (NaN/Inf in it do not propagate).
+ *  - alpha == 0 or K == 0: A and B are not read; C = beta*C (0 when beta == 0).
+ *  - M == 0 or N == 0: nothing is read or written; returns SGEMM_OK.
+ *  - Elements of C outside the M x N block (columns N..ldc-1) are never written.
+ *  - Pointers must be 4-byte aligned; no other alignment is required.
+ *  - C must not overlap A or B (not checked).
+ *  - Summation order is fixed per build and shape: results are bitwise
+ *    reproducible run to run.  Each element is one fp32 fused-multiply-add chain
+ *    over k ascending, then alpha and beta are applied once.
+ *  - Nothing here exits or aborts the process: every failure is a status code.
+ */
+#ifndef DENSE_FP32_GEMM_02_GB300_SGEMM_H
+#define DENSE_FP32_GEMM_02_GB300_SGEMM_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; declared here so that this header needs
+ * no CUDA headers.  NULL means the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *sgemm_stream_t;
+
+typedef enum {
+    SGEMM_OK = 0,
+    SGEMM_ERR_INVALID_ARG = 1,        /* a size, leading dimension or pointer is invalid */
+    SGEMM_ERR_UNSUPPORTED_DEVICE = 2, /* the current CUDA device is not sm_103 */
+    SGEMM_ERR_CUDA = 3,               /* a CUDA runtime/driver call failed; see sgemm_last_cuda_error() */
+    SGEMM_ERR_TIMEOUT = 4,            /* a bounded in-kernel wait expired (reported by sgemm_device_status) */
+    SGEMM_ERR_ALLOC = 5               /* device or pinned workspace allocation failed */
+} sgemm_status;
+
+/*
+ * sgemm -- the GEMM on device memory, asynchronous on `stream`.
+ *
+ * A, B, C: device pointers owned by the caller; the library keeps no reference
+ * after the call returns.  The work is enqueued on `stream` and the call returns
+ * without synchronising.  A, B and C must stay valid until that work completes.
+ * The library may use a device workspace for a transposed copy of A (K x M
+ * floats, twice that for the packed-FP32x2 micro-kernel) and, when B's row
+ * pitch or address does not meet the 16-byte rule of the tensor-memory
+ * accelerator, a padded copy of B.  The workspace comes from a stream-ordered
+ * memory pool owned by the library (one per device) and is returned to it on
+ * `stream` after the last kernel that reads it.
+ *
+ * Returns SGEMM_OK once the work is enqueued; errors raised by the device while
+ * the kernels run surface on the caller's next synchronisation of `stream`, and
+ * a bounded-wait expiry inside the kernel through sgemm_device_status().
+ */
+int sgemm(int M, int N, int K, float alpha,
+          const float *A, int lda,
+          const float *B, int ldb,
+          float beta, float *C, int ldc,
+          sgemm_stream_t stream);
+
+/*
+ * sgemm_host -- the same GEMM on HOST buffers; synchronous.
+ *
+ * A, B, C are host pointers (page-locked memory gives the fastest copies, but
+ * pageable memory is accepted).  The call copies A and B (and C when beta != 0)
+ * to device buffers taken from the library pool, runs sgemm() on `stream`,
+ * copies the M x N result back into C (respecting ldc) and synchronises
+ * `stream` before returning, so C holds the result on return.
+ */
+int sgemm_host(int M, int N, int K, float alpha,
+               const float *A, int lda,
+               const float *B, int ldb,
+               float beta, float *C, int ldc,
+               sgemm_stream_t stream);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char *sgemm_status_string(int status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int sgemm_version(void);
+
+/* The cudaError_t value behind the most recent SGEMM_ERR_CUDA / SGEMM_ERR_ALLOC
+ * on the calling thread (0 if none). */
+int sgemm_last_cuda_error(void);
+
+/*
+ * sgemm_device_status -- synchronises `stream`, then reads and clears the
+ * library's device-side error word for the current device.  Returns SGEMM_OK,
+ * or SGEMM_ERR_TIMEOUT if a kernel gave up a bounded wait (it then wrote no
+ * result for the affected tiles), or SGEMM_ERR_CUDA if the synchronisation
+ * itself failed.
+ */
+int sgemm_device_status(sgemm_stream_t stream);
+
+/*
+ * sgemm_set_wait_timeout_ns -- limit (nanoseconds) for every in-kernel wait on
+ * a shared-memory barrier, for launches made after the call.  Default 2e9.
+ * A wait that exceeds it sets the device error word and the kernel returns.
+ * Values below 1000 are rejected with SGEMM_ERR_INVALID_ARG.
+ */
+int sgemm_set_wait_timeout_ns(unsigned long long ns);
+
+/*
+ * sgemm_selftest_wait_timeout -- failure-detection self test.  Launches one
+ * block whose thread waits on a shared-memory barrier that nothing ever
+ * completes, with the given limit (nanoseconds, >= 1000, <= 1e10).  The wait
+ * expires, the kernel records the expiry in the device error word and returns.
+ * The call then behaves like sgemm_device_status(stream): it returns
+ * SGEMM_ERR_TIMEOUT when the expiry was detected and reported (the expected
+ * outcome), and the error word is left cleared.
+ */
+int sgemm_selftest_wait_timeout(unsigned long long ns, sgemm_stream_t stream);
+
+/*
+ * Kernel timing for benchmarks.  sgemm_profile_enable(1) makes later sgemm()
+ * calls record CUDA events on their stream around their main GEMM kernel and
+ * around their packing kernels.  sgemm_profile_collect() synchronises those
+ * events, writes the summed milliseconds and the number of launches of each
+ * kind (any pointer may be NULL), and clears the record.  Disabled by default.
+ */
+int sgemm_profile_enable(int on);
+int sgemm_profile_collect(double *main_ms, long long *main_launches,
+                          double *pack_ms, long long *pack_launches);
+
+/* Number of kernels this library has launched in this process. */
+long long sgemm_kernel_launch_count(void);
+
+/*
+ * sgemm_config_string -- the kernel configuration sgemm() would pick for the
+ * given shape (tile sizes, stages, micro-kernel), as static text.  No GPU work.
+ */
+const char *sgemm_config_string(int M, int N, int K);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_FP32_GEMM_02_GB300_SGEMM_H */

@@ -1,0 +1,126 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must load on a machine without a GPU, export every function that
+include/sgemm.h declares, and reject invalid arguments before touching CUDA.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from dense_fp32_gemm_02_gb300 import build as sgbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = sgbuild.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(sgemm\w*)\s*\(", text, flags=re.M):
+            names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("sgemm", "sgemm_host", "sgemm_status_string", "sgemm_version"):
+        assert required in names, names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared in include/*.h but not exported: {missing}"
+
+
+def test_library_exports_nothing_undeclared():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", sgbuild.LIB_PATH], capture_output=True,
+                         text=True)
+    if out.returncode != 0:
+        pytest.skip("nm not available")
+    exported = {l.split()[-1] for l in out.stdout.splitlines() if " T " in l}
+    assert exported <= set(declared_functions()), exported - set(declared_functions())
+
+
+def test_status_strings_and_version(lib):
+    lib.sgemm_status_string.restype = ctypes.c_char_p
+    for st in range(6):
+        s = lib.sgemm_status_string(st).decode()
+        assert s.startswith("SGEMM_")
+    assert b"unknown" in lib.sgemm_status_string(99)
+    assert lib.sgemm_version() >= 10000
+
+
+def _call(lib, M, N, K, A=1, lda=None, B=1, ldb=None, C=1, ldc=None, alpha=1.0, beta=0.0):
+    f = lib.sgemm
+    f.argtypes = [ctypes.c_int] * 3 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_int,
+                                       ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
+                                       ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    lda = max(1, K) if lda is None else lda
+    ldb = max(1, N) if ldb is None else ldb
+    ldc = max(1, N) if ldc is None else ldc
+    # fake, never-dereferenced but 16-byte aligned addresses (validation happens first)
+    ptr = lambda v: None if v is None else 0x100000 * v
+    return f(M, N, K, alpha, ptr(A), lda, ptr(B), ldb, beta, ptr(C), ldc, None)
+
+
+INVALID = [
+    dict(M=-1, N=4, K=4),
+    dict(M=4, N=-1, K=4),
+    dict(M=4, N=4, K=-1),
+    dict(M=4, N=4, K=8, lda=7),
+    dict(M=4, N=8, K=4, ldb=7),
+    dict(M=4, N=8, K=4, ldc=7),
+    dict(M=4, N=4, K=4, A=None),
+    dict(M=4, N=4, K=4, B=None),
+    dict(M=4, N=4, K=4, C=None),
+    dict(M=4, N=4, K=0, lda=0),
+]
+
+
+@pytest.mark.parametrize("kw", INVALID)
+def test_invalid_arguments_rejected_without_gpu(lib, kw):
+    assert _call(lib, **kw) == 1  # SGEMM_ERR_INVALID_ARG
+
+
+def test_misaligned_pointer_rejected(lib):
+    f = lib.sgemm
+    f.argtypes = [ctypes.c_int] * 3 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_int,
+                                       ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
+                                       ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    assert f(4, 4, 4, 1.0, 0x100001, 4, 0x200000, 4, 0.0, 0x300000, 4, None) == 1
+    assert f(4, 4, 4, 1.0, 0x100000, 4, 0x200000, 4, 0.0, 0x300002, 4, None) == 1
+
+
+@pytest.mark.parametrize("kw", [dict(M=0, N=4, K=4), dict(M=4, N=0, K=4),
+                                dict(M=0, N=0, K=0, A=None, B=None, C=None)])
+def test_empty_output_is_a_no_op_without_gpu(lib, kw):
+    # nothing to compute: success without any CUDA call, pointers not read
+    assert _call(lib, **kw) == 0
+
+
+def test_timeout_setter_validates(lib):
+    lib.sgemm_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+    assert lib.sgemm_set_wait_timeout_ns(10) == 1
+    assert lib.sgemm_set_wait_timeout_ns(2_000_000_000) == 0
+
+
+def test_binding_loads_and_reports_config():
+    from dense_fp32_gemm_02_gb300 import binding
+    assert binding.version() == ctypes.CDLL(sgbuild.LIB_PATH).sgemm_version()
+    assert "BM=" in binding.config_string(8192, 8192, 8192)
+    with pytest.raises(binding.SgemmError) as e:
+        binding.check(1)
+    assert "INVALID_ARG" in str(e.value)

@@ -1,0 +1,212 @@
+"""GPU parity of the SGEMM path against the CPU oracle (small and ragged shapes,
+edge cases, failure detection).  Every call goes through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+from dense_fp32_gemm_02_gb300.workloads import make_inputs
+from _helpers import assert_within_bound, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu(cuda_device):
+    from dense_fp32_gemm_02_gb300 import binding  # noqa: F401  (fails loudly if not built)
+    yield
+
+
+SIZES_MN = [1, 7, 33, 64, 127, 128, 129, 255, 257]
+SIZES_K = [1, 5, 16, 17, 33, 100]
+
+
+@pytest.mark.parametrize("K", SIZES_K)
+def test_integer_inputs_bit_exact_over_shape_grid(K):
+    """Integer inputs in [-4, 4]: every partial sum is an exact integer, so any
+    summation order gives the oracle's bits.  alpha=1.5, beta=0.5 with integer
+    C keeps the epilogue exact too."""
+    for M in SIZES_MN:
+        for N in SIZES_MN:
+            A, B, C = make_inputs(M, N, K, "int4", "int4", "int4", seed=M * 1000 + N * 10 + K)
+            ref, _ = oracle.sgemm(A, B, C, 1.5, 0.5)
+            got = run_gpu(A, B, C, 1.5, 0.5).cpu().numpy()
+            assert np.array_equal(got, ref), (M, N, K)
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 200, 100), (129, 257, 513), (1000, 33, 77),
+                                   (5, 1100, 260), (640, 640, 640)])
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (1.5, 0.5), (-0.75, 1.0), (2.0, -3.0)])
+def test_random_parity_within_bound(M, N, K, alpha, beta):
+    A, B, C = make_inputs(M, N, K, "upm1", "normal", "normal", seed=M + N + K)
+    ref, bound = oracle.sgemm(A, B, C if beta != 0 else None, alpha, beta)
+    got = run_gpu(A, B, C if beta != 0 else None, alpha, beta).cpu().numpy()
+    assert_within_bound(got, ref, bound, f"{M}x{N}x{K} a={alpha} b={beta}")
+
+
+@pytest.mark.parametrize("pads,offsets", [((3, 5, 2), (0, 0, 0)), ((0, 0, 0), (1, 1, 1)),
+                                          ((4, 4, 4), (0, 2, 3)), ((1, 0, 7), (3, 0, 0))])
+def test_leading_dimensions_and_alignment(pads, offsets):
+    """Row pitches above the minimum with NaN padding, and base addresses that
+    are 4-byte but not 16-byte aligned: the TMA rule is met by the packing
+    pass; NaN padding must never reach the result; C padding stays untouched."""
+    M, N, K = 203, 157, 141
+    A, B, C = make_inputs(M, N, K, "upm1", "upm1", "normal", seed=7,
+                          lda=K + pads[0], ldb=N + pads[1], ldc=N + pads[2])
+    ref, bound = oracle.sgemm(A, B, C, 1.0, 1.0)
+    dC = run_gpu(A, B, C, 1.0, 1.0, offsets=offsets)
+    got = dC.cpu().numpy()
+    assert np.isfinite(got).all()
+    assert_within_bound(got, ref, bound, f"pads={pads} offsets={offsets}")
+    if pads[2]:
+        full = dC.as_strided((M, N + pads[2]), (N + pads[2], 1)).cpu().numpy()
+        assert np.isnan(full[:, N:]).all(), "C padding columns were written"
+
+
+def test_edge_rows_and_columns_not_written_outside_block():
+    """Guard band: C is a window inside a NaN-filled buffer; nothing outside the
+    M x N window may change."""
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    M, N, K = 130, 70, 40
+    A, B, _ = make_inputs(M, N, K, "upm1", "upm1", None, seed=3)
+    big = torch.full((M + 4, N + 40), float("nan"), device="cuda")
+    win = big[2:2 + M, 3:3 + N]
+    binding.sgemm_into(to_device(A), to_device(B), win, 1.0, 0.0)
+    torch.cuda.synchronize()
+    ref, bound = oracle.sgemm(A, B, None, 1.0, 0.0)
+    assert_within_bound(win.cpu().numpy(), ref, bound, "window")
+    h = big.cpu().numpy()
+    mask = np.ones_like(h, dtype=bool)
+    mask[2:2 + M, 3:3 + N] = False
+    assert np.isnan(h[mask]).all()
+
+
+def test_beta_zero_does_not_read_c():
+    M, N, K = 150, 140, 130
+    A, B, _ = make_inputs(M, N, K, "upm1", "upm1", None, seed=5)
+    C = np.full((M, N), np.nan, np.float32)
+    ref, bound = oracle.sgemm(A, B, None, 1.0, 0.0)
+    got = run_gpu(A, B, C, 1.0, 0.0).cpu().numpy()
+    assert np.isfinite(got).all()
+    assert_within_bound(got, ref, bound, "beta=0")
+
+
+@pytest.mark.parametrize("K,alpha,beta", [(0, 1.0, 0.5), (0, 1.0, 0.0), (64, 0.0, -2.0),
+                                          (64, 0.0, 0.0)])
+def test_quick_returns_scale_c(K, alpha, beta):
+    M, N = 37, 45
+    A, B, C = make_inputs(M, N, K, "upm1", "upm1", "normal", seed=9)
+    if alpha == 0.0:
+        A = A.copy()
+        A[0, 0] = np.inf       # A must not be read when alpha == 0
+    ref, _ = oracle.sgemm(A, B, C, alpha, beta)
+    got = run_gpu(A, B, C, alpha, beta).cpu().numpy()
+    assert np.array_equal(got, ref)
+
+
+def test_empty_sizes_are_no_ops():
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    for (M, N, K) in [(0, 5, 3), (5, 0, 3), (0, 0, 0)]:
+        A = torch.zeros((M, K), device="cuda")
+        B = torch.zeros((K, N), device="cuda")
+        C = torch.zeros((M, N), device="cuda")
+        binding.sgemm_into(A, B, C, 1.0, 1.0)
+    torch.cuda.synchronize()
+
+
+def test_ones_times_twos_small_shapes_exact():
+    for (M, N, K) in [(1, 1, 1), (7, 13, 29), (128, 128, 128), (129, 255, 511), (512, 512, 512)]:
+        A = np.ones((M, K), np.float32)
+        B = np.full((K, N), 2.0, np.float32)
+        got = run_gpu(A, B, None, 1.0, 0.0).cpu().numpy()
+        assert (got == 2 * K).all(), (M, N, K)
+
+
+def test_bitwise_deterministic_run_to_run():
+    """The race check of the tiling exercise (missing-barrier bug, exercise 5):
+    a race shows up as results that change between runs."""
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    M, N, K = 1031, 777, 1500
+    A, B, C = make_inputs(M, N, K, "normal", "normal", "normal", seed=11)
+    dA, dB = to_device(A), to_device(B)
+    outs = []
+    for _ in range(3):
+        dC = to_device(C)
+        binding.sgemm_into(dA, dB, dC, 1.0, 1.0)
+        outs.append(dC.cpu())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+def test_host_entry_point_matches_device_entry_point():
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    M, N, K = 321, 283, 259
+    A, B, C = make_inputs(M, N, K, "upm1", "upm1", "normal", seed=13)
+    dev = run_gpu(A, B, C, 0.5, 2.0).cpu()
+    hA = torch.from_numpy(np.ascontiguousarray(A)).pin_memory()
+    hB = torch.from_numpy(np.ascontiguousarray(B)).pin_memory()
+    hC = torch.from_numpy(np.ascontiguousarray(C)).pin_memory()
+    binding.sgemm_host(hA, hB, hC, 0.5, 2.0)
+    assert torch.equal(hC, dev)
+    # pageable memory with a row pitch
+    A2, B2, C2 = make_inputs(M, N, K, "upm1", "upm1", "normal", seed=13, lda=K + 3, ldb=N + 1,
+                             ldc=N + 5)
+    tA, tB = torch.from_numpy(A2.base)[:, :K], torch.from_numpy(B2.base)[:, :N]
+    cbuf = torch.from_numpy(C2.base.copy())
+    binding.sgemm_host(tA, tB, cbuf[:, :N], 0.5, 2.0)
+    assert torch.equal(cbuf[:, :N], dev)
+    assert torch.isnan(cbuf[:, N:]).all()
+
+
+def test_runs_on_a_non_default_stream():
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    M, N, K = 260, 250, 240
+    A, B, C = make_inputs(M, N, K, "upm1", "upm1", "normal", seed=17)
+    ref, bound = oracle.sgemm(A, B, C, 1.0, 1.0)
+    s = torch.cuda.Stream()
+    dA, dB, dC = to_device(A), to_device(B), to_device(C)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        binding.sgemm_into(dA, dB, dC, 1.0, 1.0)
+    s.synchronize()
+    assert_within_bound(dC.cpu().numpy(), ref, bound, "side stream")
+
+
+def test_bounded_wait_expiry_is_reported_and_context_survives():
+    """Failure detection without a GPU fault: a barrier wait that nothing
+    completes expires after 2 ms, the kernel reports it and returns; the
+    context stays usable and the next GEMM is correct."""
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    assert binding.device_status() == binding.SGEMM_OK
+    assert binding.selftest_wait_timeout(2_000_000) == binding.SGEMM_ERR_TIMEOUT
+    assert binding.device_status() == binding.SGEMM_OK     # word was cleared
+    M, N, K = 140, 150, 160
+    A, B, _ = make_inputs(M, N, K, "upm1", "upm1", None, seed=19)
+    ref, bound = oracle.sgemm(A, B, None, 1.0, 0.0)
+    got = run_gpu(A, B, None, 1.0, 0.0).cpu().numpy()
+    assert_within_bound(got, ref, bound, "after self test")
+    assert binding.device_status() == binding.SGEMM_OK
+
+
+def test_binding_rejects_bad_tensors():
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    A = torch.zeros((4, 4), device="cuda")
+    with pytest.raises(TypeError):
+        binding.sgemm_into(A.double(), A, A)
+    with pytest.raises(ValueError):
+        binding.sgemm_into(A, torch.zeros((3, 4), device="cuda"), A)
+    with pytest.raises(ValueError):
+        binding.sgemm_into(A, A, A.t())     # C columns not contiguous
+
+
+def test_kernel_launches_are_counted():
+    from dense_fp32_gemm_02_gb300 import binding
+    before = binding.kernel_launch_count()
+    A, B, _ = make_inputs(64, 64, 64, seed=23)
+    run_gpu(A, B, None, 1.0, 0.0)
+    assert binding.kernel_launch_count() - before >= 2     # pack + main
