@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--workload", default=None, help="workload name (default: the 8192^3 case)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--variant", type=int, default=-1,
+                    help="force a kernel variant (tile-configuration sweeps); -1 = automatic")
     return ap.parse_args()
 
 
@@ -271,6 +273,7 @@ def run_ours(args):
     from dense_fp32_gemm_02_gb300 import binding
     from dense_fp32_gemm_02_gb300.workloads import BENCH_WORKLOAD, WORKLOADS, workload_inputs
     w = WORKLOADS[args.workload or BENCH_WORKLOAD]
+    binding.set_variant(args.variant)
     A, B, C = workload_inputs(w)
     props = torch.cuda.get_device_properties(device)
     sms = props.multi_processor_count

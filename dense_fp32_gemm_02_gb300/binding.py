@@ -50,6 +50,12 @@ lib.sgemm_kernel_launch_count.argtypes = []
 lib.sgemm_kernel_launch_count.restype = _ll
 lib.sgemm_config_string.argtypes = [_i, _i, _i]
 lib.sgemm_config_string.restype = ctypes.c_char_p
+lib.sgemm_variant_count.argtypes = []
+lib.sgemm_variant_count.restype = _i
+lib.sgemm_variant_name.argtypes = [_i]
+lib.sgemm_variant_name.restype = ctypes.c_char_p
+lib.sgemm_set_variant.argtypes = [_i]
+lib.sgemm_set_variant.restype = _i
 
 SGEMM_OK = 0
 SGEMM_ERR_INVALID_ARG = 1
@@ -195,3 +201,13 @@ def kernel_launch_count() -> int:
 
 def config_string(M: int, N: int, K: int) -> str:
     return lib.sgemm_config_string(M, N, K).decode()
+
+
+def variants() -> list:
+    """Descriptions of the compiled kernel variants, by index."""
+    return [lib.sgemm_variant_name(i).decode() for i in range(lib.sgemm_variant_count())]
+
+
+def set_variant(variant_id: int) -> None:
+    """Force a kernel variant for later calls (-1: automatic choice)."""
+    check(lib.sgemm_set_variant(int(variant_id)))

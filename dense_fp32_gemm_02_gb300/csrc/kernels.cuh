@@ -13,11 +13,14 @@
 //    pre-pass into global memory so that the tensor-memory accelerator (TMA)
 //    can copy A tiles exactly like B tiles;
 //  * double buffering, generalised to an S-stage ring of TMA copies guarded by
-//    full/empty shared-memory barriers, with one producer warp;
+//    full/empty shared-memory barriers;
 //  * the zig-zag lane map of "SGEMM CUDA kernel (Second Half)" (section
 //    "LDS.128 Shared Memory Transactions"): for A reads lane i and lane i^1
-//    fetch the same address, for B reads lane i and lane i^2 do, so the
-//    quarter-warp transactions of every 128-bit shared load merge in pairs;
+//    fetch the same address, for B reads lane i and lane i^2 do.  The page
+//    expects such pairs to merge quarter-warp transactions; on sm_103 every
+//    128-bit shared load was measured at four wavefronts regardless, so the
+//    map here only keeps each quarter-warp free of bank conflicts, and the
+//    thread tile is sized by shared-memory bytes per FMA instead;
 //  * zero-filled edge tiles (the TMA fills out-of-range box elements with 0)
 //    and guarded stores, as in exercise 1 of "3.3 Shared memory and tiling".
 #pragma once
@@ -42,34 +45,39 @@ enum : unsigned {
 __device__ unsigned int g_error_word = 0;
 
 // ------------------------------------------------------------------ configuration
+// Micro-kernel of the consumer warps.
+enum Micro : int {
+    MICRO_FFMA = 0,    // one scalar fused multiply-add per output per k
+    MICRO_FFMA2 = 1,   // packed FP32x2 FMA on two vertically adjacent outputs:
+                       //   (c[i][j], c[i+1][j]) += (a[i], a[i+1]) * (b[j], b[j])
+};
+
 // Lanes of a warp form a LANES_M x LANES_N = 4 x 8 grid.  A thread owns a
 // TM x TN tile made of (TM/4) x (TN/4) sub-tiles of 4x4 spaced 16 rows and 32
-// columns apart, so a warp covers (4*TM) x (8*TN) outputs.
+// columns apart, so a warp covers (4*TM) x (8*TN) outputs and every fragment
+// load is one 128-bit shared load of four consecutive floats.
 template <int BM_, int BN_, int BK_, int STAGES_, int WARPS_M_, int WARPS_N_, int TM_, int TN_,
-          bool PAIRED_>
+          int MICRO_>
 struct TileConfig {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_;
     static constexpr int TM = TM_, TN = TN_;
+    static constexpr int MICRO = MICRO_;
     static constexpr int LANES_M = 4, LANES_N = 8;
     static constexpr int WM = TM * LANES_M, WN = TN * LANES_N;
     static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
-    static constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
-    // PAIRED: the transposed A holds every element twice (a, a), so one 128-bit
-    // shared load yields two ready-made (a_i, a_i) operand pairs for the packed
-    // FP32x2 fused multiply-add; otherwise scalar FFMA.
-    static constexpr bool PAIRED = PAIRED_;
-    static constexpr int A_ROW = PAIRED ? 2 * BM : BM;   // floats per K-row of the A tile
-    static constexpr int A_STAGE = BK * A_ROW;           // floats
-    static constexpr int B_STAGE = BK * BN;              // floats
+    static constexpr int THREADS = CONSUMER_WARPS * 32;
+    static constexpr int A_STAGE = BK * BM;   // floats: K-rows of the transposed A tile
+    static constexpr int B_STAGE = BK * BN;   // floats: K-rows of the B tile
     static constexpr uint32_t STAGE_BYTES = uint32_t(A_STAGE + B_STAGE) * 4u;
     static constexpr size_t SMEM_BYTES =
         size_t(STAGES) * STAGE_BYTES + 2 * STAGES * sizeof(uint64_t) + 16 + 1024;
 
     static_assert(WM * WARPS_M == BM && WN * WARPS_N == BN, "warp grid must cover the tile");
     static_assert(TM % 4 == 0 && TN % 4 == 0, "thread tile is made of 4x4 sub-tiles");
-    static_assert(A_ROW <= 256 && BN <= 256 && BK <= 256, "TMA box edge is at most 256");
+    static_assert(BM <= 256 && BN <= 256 && BK <= 256, "TMA box edge is at most 256");
     static_assert((A_STAGE * 4) % 1024 == 0 && (B_STAGE * 4) % 1024 == 0, "stage alignment");
+    static_assert(SMEM_BYTES <= 232448, "at most 227 KB of shared memory per CTA");
 };
 
 struct MainParams {
@@ -97,14 +105,69 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
     tn = local / gm;
 }
 
+// Fragment loads for one k: TM values of A (a K-row of the transposed tile)
+// and TN values of B, 128 bits at a time.
+template <class Cfg>
+__device__ __forceinline__ void load_fragments(const float *a_row, const float *b_row,
+                                               float (&fa)[Cfg::TM], float (&fb)[Cfg::TN]) {
+#pragma unroll
+    for (int s = 0; s < Cfg::TM / 4; ++s) {
+        const float4 v = *reinterpret_cast<const float4 *>(a_row + s * 16);
+        fa[4 * s + 0] = v.x;
+        fa[4 * s + 1] = v.y;
+        fa[4 * s + 2] = v.z;
+        fa[4 * s + 3] = v.w;
+    }
+#pragma unroll
+    for (int t = 0; t < Cfg::TN / 4; ++t) {
+        const float4 v = *reinterpret_cast<const float4 *>(b_row + t * 32);
+        fb[4 * t + 0] = v.x;
+        fb[4 * t + 1] = v.y;
+        fb[4 * t + 2] = v.z;
+        fb[4 * t + 3] = v.w;
+    }
+}
+
+// acc += fa (outer product) fb
+template <class Cfg>
+__device__ __forceinline__ void outer_product(float (&acc)[Cfg::TM][Cfg::TN],
+                                              const float (&fa)[Cfg::TM],
+                                              const float (&fb)[Cfg::TN]) {
+    if constexpr (Cfg::MICRO == MICRO_FFMA2) {
+#pragma unroll
+        for (int j = 0; j < Cfg::TN; ++j) {
+            const float2 bb = make_float2(fb[j], fb[j]);
+#pragma unroll
+            for (int i = 0; i < Cfg::TM; i += 2) {
+                const float2 r = ffma2(make_float2(fa[i], fa[i + 1]), bb,
+                                       make_float2(acc[i][j], acc[i + 1][j]));
+                acc[i][j] = r.x;
+                acc[i + 1][j] = r.y;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < Cfg::TM; ++i)
+#pragma unroll
+            for (int j = 0; j < Cfg::TN; ++j) acc[i][j] = fmaf(fa[i], fb[j], acc[i][j]);
+    }
+}
+
 // ------------------------------------------------------------------ main kernel
+// Persistent kernel: CTA b computes tiles b, b + gridDim.x, ...  The k-slabs of
+// all its tiles form one sequence q = 0, 1, 2, ...; slab q lives in ring stage
+// q % STAGES.  Thread 0 issues the TMA copies of slab q + STAGES - 1 when the
+// CTA starts consuming slab q, after every warp has released that stage's
+// previous contents (empty barrier).  Warps wait on the full barrier of a stage
+// (TMA byte count) before reading it and arrive on its empty barrier after.
+// There is no separate producer warp: with 8 warps per CTA each SM sub-
+// partition holds two warps and a thread can keep up to 255 registers.
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     sgemm_tma_ffma_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB, const MainParams p) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int TM = Cfg::TM, TN = Cfg::TN;
-    constexpr int A_ROW = Cfg::A_ROW;
 
     extern __shared__ unsigned char smem_raw[];
     const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
@@ -112,7 +175,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     float *sB = sA + STAGES * Cfg::A_STAGE;
     uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * Cfg::B_STAGE);
     uint64_t *empty = full + STAGES;
-    int *abort_flag = reinterpret_cast<int *>(empty + STAGES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -122,196 +184,148 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], Cfg::CONSUMER_WARPS);
         }
-        *abort_flag = 0;
         fence_barrier_init();
     }
     __syncthreads();
 
     const int num_tiles = p.tiles_m * p.tiles_n;
     const int k_tiles = (p.K + BK - 1) / BK;
+    const int my_tiles = blockIdx.x < num_tiles ? (num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const long long total_slabs = (long long)my_tiles * k_tiles;
+    long long issued = 0;    // thread 0 only: slabs whose copies were issued
+    bool aborted = false;
 
-    // producer bookkeeping (lane 0 of the producer warp)
-    long long issued = 0;
-
-    if (warp == Cfg::CONSUMER_WARPS) {
-        // ---------------------------------------------------------- producer warp
-        if (lane == 0) {
-            tma_prefetch_desc(&tmA);
-            tma_prefetch_desc(&tmB);
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-                int tm, tn;
-                tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-                const int a_x = (Cfg::PAIRED ? 2 : 1) * tm * BM;
-                const int b_x = tn * BN;
-                for (int kt = 0; kt < k_tiles; ++kt) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns)) {
-                        atomicOr(&g_error_word, ERR_EMPTY_WAIT);
-                        *abort_flag = 1;
-                        goto producer_done;
-                    }
-                    mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
-                    tma_load_2d(sA + stage * Cfg::A_STAGE, &tmA, &full[stage], a_x, kt * BK);
-                    tma_load_2d(sB + stage * Cfg::B_STAGE, &tmB, &full[stage], b_x, kt * BK);
-                    ++issued;
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-        producer_done:;
+    // Thread 0: issue the copies of slab q.  Returns false if the wait for the
+    // stage to be released expired.
+    auto issue = [&](long long q) -> bool {
+        const int s = int(q % STAGES);
+        const long long use = q / STAGES;
+        if (use > 0 && !mbar_wait(&empty[s], uint32_t((use - 1) & 1), p.timeout_ns)) {
+            atomicOr(&g_error_word, ERR_EMPTY_WAIT);
+            return false;
         }
-    } else {
-        // ---------------------------------------------------------- consumer warps
-        const int wm0 = (warp % Cfg::WARPS_M) * Cfg::WM;
-        const int wn0 = (warp / Cfg::WARPS_M) * Cfg::WN;
-        // zig-zag lane map: lane bits {1,4} -> row group, bits {0,2,3} -> column group
-        const int lm = ((lane >> 1) & 1) | ((lane >> 3) & 2);
-        const int ln = (lane & 1) | ((lane >> 1) & 6);
+        const int j = int(q / k_tiles);
+        const int kt = int(q - (long long)j * k_tiles);
+        int tm, tn;
+        tile_coords(blockIdx.x + j * gridDim.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
+        tma_load_2d(sA + s * Cfg::A_STAGE, &tmA, &full[s], tm * BM, kt * BK);
+        tma_load_2d(sB + s * Cfg::B_STAGE, &tmB, &full[s], tn * BN, kt * BK);
+        issued = q + 1;
+        return true;
+    };
 
-        int stage = 0;
-        uint32_t phase = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            int tm, tn;
-            tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-
-            float acc[TM][TN];
-#pragma unroll
-            for (int i = 0; i < TM; ++i)
-#pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
-
-            for (int kt = 0; kt < k_tiles; ++kt) {
-                bool ok = mbar_wait(&full[stage], phase, p.timeout_ns);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) {
-                    if (lane == 0) {
-                        atomicOr(&g_error_word, ERR_FULL_WAIT);
-                        *abort_flag = 1;
-                    }
-                    goto consumer_done;
-                }
-                const float *a_s = sA + stage * Cfg::A_STAGE;
-                const float *b_s = sB + stage * Cfg::B_STAGE;
-#pragma unroll
-                for (int kk = 0; kk < BK; ++kk) {
-                    float b[TN];
-#pragma unroll
-                    for (int t = 0; t < TN / 4; ++t) {
-                        const float4 v = *reinterpret_cast<const float4 *>(
-                            b_s + kk * BN + wn0 + t * 32 + ln * 4);
-                        b[4 * t + 0] = v.x;
-                        b[4 * t + 1] = v.y;
-                        b[4 * t + 2] = v.z;
-                        b[4 * t + 3] = v.w;
-                    }
-                    if constexpr (Cfg::PAIRED) {
-                        // (a_i, a_i) pairs straight from the duplicated layout
-                        float2 a2[TM];
-#pragma unroll
-                        for (int s = 0; s < TM / 4; ++s) {
-                            const float *src = a_s + kk * A_ROW + 2 * (wm0 + s * 16 + lm * 4);
-                            const float4 v0 = *reinterpret_cast<const float4 *>(src);
-                            const float4 v1 = *reinterpret_cast<const float4 *>(src + 4);
-                            a2[4 * s + 0] = make_float2(v0.x, v0.y);
-                            a2[4 * s + 1] = make_float2(v0.z, v0.w);
-                            a2[4 * s + 2] = make_float2(v1.x, v1.y);
-                            a2[4 * s + 3] = make_float2(v1.z, v1.w);
-                        }
-#pragma unroll
-                        for (int i = 0; i < TM; ++i)
-#pragma unroll
-                            for (int j = 0; j < TN; j += 2) {
-                                const float2 r = ffma2(a2[i], make_float2(b[j], b[j + 1]),
-                                                       make_float2(acc[i][j], acc[i][j + 1]));
-                                acc[i][j] = r.x;
-                                acc[i][j + 1] = r.y;
-                            }
-                    } else {
-                        float a[TM];
-#pragma unroll
-                        for (int s = 0; s < TM / 4; ++s) {
-                            const float4 v = *reinterpret_cast<const float4 *>(
-                                a_s + kk * A_ROW + wm0 + s * 16 + lm * 4);
-                            a[4 * s + 0] = v.x;
-                            a[4 * s + 1] = v.y;
-                            a[4 * s + 2] = v.z;
-                            a[4 * s + 3] = v.w;
-                        }
-#pragma unroll
-                        for (int i = 0; i < TM; ++i)
-#pragma unroll
-                            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[stage]);
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        for (long long q = 0; q < STAGES - 1 && q < total_slabs; ++q)
+            if (!issue(q)) {
+                aborted = true;
+                break;
             }
-
-            // ---------------------------------------------------------- epilogue
-            {
-                const int row0 = tm * BM + wm0 + lm * 4;
-                const int col0 = tn * BN + wn0 + ln * 4;
-                const float alpha = p.alpha, beta = p.beta;
-#pragma unroll
-                for (int s = 0; s < TM / 4; ++s) {
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int row = row0 + s * 16 + r;
-                        if (row >= p.M) continue;
-                        float *crow = p.C + (long long)row * p.ldc;
-#pragma unroll
-                        for (int t = 0; t < TN / 4; ++t) {
-                            const int col = col0 + t * 32;
-                            const float *v = &acc[4 * s + r][4 * t];
-                            if (p.c_vec4 && col + 3 < p.N) {
-                                float4 o;
-                                if (beta != 0.0f) {
-                                    const float4 c = __ldcs(reinterpret_cast<const float4 *>(crow + col));
-                                    o.x = fmaf(alpha, v[0], beta * c.x);
-                                    o.y = fmaf(alpha, v[1], beta * c.y);
-                                    o.z = fmaf(alpha, v[2], beta * c.z);
-                                    o.w = fmaf(alpha, v[3], beta * c.w);
-                                } else {
-                                    o.x = alpha * v[0];
-                                    o.y = alpha * v[1];
-                                    o.z = alpha * v[2];
-                                    o.w = alpha * v[3];
-                                }
-                                __stcs(reinterpret_cast<float4 *>(crow + col), o);
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    if (col + e < p.N) {
-                                        const float c = (beta != 0.0f) ? beta * crow[col + e] : 0.0f;
-                                        crow[col + e] = (beta != 0.0f) ? fmaf(alpha, v[e], c)
-                                                                       : alpha * v[e];
-                                    }
-                                }
-                            }
-                        }
-                    }
-                }
-            }
-        }
-    consumer_done:;
     }
 
-    __syncthreads();
-    // After an abort, wait (bounded) for every TMA copy this CTA may still have in
-    // flight before the CTA's shared memory is released.
-    if (warp == Cfg::CONSUMER_WARPS && lane == 0 && *abort_flag) {
-        const long long first = issued > STAGES ? issued - STAGES : 0;
-        for (long long q = first; q < issued; ++q) {
+    const int wm0 = (warp % Cfg::WARPS_M) * Cfg::WM;
+    const int wn0 = (warp / Cfg::WARPS_M) * Cfg::WN;
+    // zig-zag lane map: lane bits {1,4} -> row group, bits {0,2,3} -> column group
+    const int lm = ((lane >> 1) & 1) | ((lane >> 3) & 2);
+    const int ln = (lane & 1) | ((lane >> 1) & 6);
+    const int a_off = wm0 + lm * 4;
+    const int b_off = wn0 + ln * 4;
+
+    long long q = 0;    // next slab to consume
+    for (int j = 0; j < my_tiles; ++j) {
+        int tm, tn;
+        tile_coords(blockIdx.x + j * gridDim.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+
+        float acc[TM][TN];
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int jj = 0; jj < TN; ++jj) acc[i][jj] = 0.0f;
+
+        for (int kt = 0; kt < k_tiles; ++kt, ++q) {
+            if (threadIdx.x == 0 && !aborted && q + STAGES - 1 < total_slabs)
+                aborted = !issue(q + STAGES - 1);
             const int s = int(q % STAGES);
-            const uint32_t ph = uint32_t((q / STAGES) & 1);
-            if (!mbar_wait(&full[s], ph, p.timeout_ns)) {
+            bool ok = !aborted && mbar_wait(&full[s], uint32_t((q / STAGES) & 1), p.timeout_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0) atomicOr(&g_error_word, ERR_FULL_WAIT);
+                aborted = true;
+                goto done;
+            }
+            const float *a_s = sA + s * Cfg::A_STAGE + a_off;
+            const float *b_s = sB + s * Cfg::B_STAGE + b_off;
+            // register double buffering of the fragments: the loads for k+1
+            // are issued before the FMAs of k
+            float fa[2][TM], fb[2][TN];
+            load_fragments<Cfg>(a_s, b_s, fa[0], fb[0]);
+#pragma unroll
+            for (int kk = 0; kk < BK; ++kk) {
+                if (kk + 1 < BK)
+                    load_fragments<Cfg>(a_s + (kk + 1) * BM, b_s + (kk + 1) * BN,
+                                        fa[(kk + 1) & 1], fb[(kk + 1) & 1]);
+                outer_product<Cfg>(acc, fa[kk & 1], fb[kk & 1]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+
+        // -------------------------------------------------------------- epilogue
+        {
+            const int row0 = tm * BM + a_off;
+            const int col0 = tn * BN + b_off;
+            const float alpha = p.alpha, beta = p.beta;
+#pragma unroll
+            for (int s4 = 0; s4 < TM / 4; ++s4) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int row = row0 + s4 * 16 + r;
+                    if (row >= p.M) continue;
+                    float *crow = p.C + (long long)row * p.ldc;
+#pragma unroll
+                    for (int t = 0; t < TN / 4; ++t) {
+                        const int col = col0 + t * 32;
+                        const float *v = &acc[4 * s4 + r][4 * t];
+                        if (p.c_vec4 && col + 3 < p.N) {
+                            float4 o;
+                            if (beta != 0.0f) {
+                                const float4 c = __ldcs(reinterpret_cast<const float4 *>(crow + col));
+                                o.x = fmaf(alpha, v[0], beta * c.x);
+                                o.y = fmaf(alpha, v[1], beta * c.y);
+                                o.z = fmaf(alpha, v[2], beta * c.z);
+                                o.w = fmaf(alpha, v[3], beta * c.w);
+                            } else {
+                                o.x = alpha * v[0];
+                                o.y = alpha * v[1];
+                                o.z = alpha * v[2];
+                                o.w = alpha * v[3];
+                            }
+                            __stcs(reinterpret_cast<float4 *>(crow + col), o);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                if (col + e < p.N) {
+                                    const float c = (beta != 0.0f) ? beta * crow[col + e] : 0.0f;
+                                    crow[col + e] = (beta != 0.0f) ? fmaf(alpha, v[e], c)
+                                                                   : alpha * v[e];
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+done:
+    // After an abort, thread 0 waits (bounded) for the copies it issued and no
+    // warp consumed, so no copy is still writing when the CTA exits.
+    if (threadIdx.x == 0 && aborted) {
+        const long long first = issued > STAGES ? issued - STAGES : 0;
+        for (long long qq = first; qq < issued; ++qq) {
+            const int s = int(qq % STAGES);
+            if (!mbar_wait(&full[s], uint32_t((qq / STAGES) & 1), p.timeout_ns)) {
                 atomicOr(&g_error_word, ERR_DRAIN_WAIT);
                 break;
             }
@@ -320,9 +334,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 }
 
 // ------------------------------------------------------------------ pre-pass
-// At[k][x] = A[m][k] with x = m (plain) or x = 2m and 2m+1 (paired).  32x32
-// tiles through shared memory: coalesced reads along k, coalesced writes along m.
-template <bool PAIRED>
+// At[k][m] = A[m][k].  32x32 tiles through shared memory: coalesced reads along
+// k, coalesced writes along m.
 __global__ void __launch_bounds__(256)
     pack_a_transpose_kernel(const float *__restrict__ A, long long lda, int M, int K,
                             float *__restrict__ At, long long ldat) {
@@ -339,13 +352,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
             for (int r = ty; r < 32; r += 8) {
                 const long long k = k0 + r, m = m0 + tx;
-                if (k < K && m < M) {
-                    const float v = tile[tx][r];
-                    if constexpr (PAIRED)
-                        *reinterpret_cast<float2 *>(At + k * ldat + 2 * m) = make_float2(v, v);
-                    else
-                        At[k * ldat + m] = v;
-                }
+                if (k < K && m < M) At[k * ldat + m] = tile[tx][r];
             }
             __syncthreads();
         }

@@ -33,8 +33,60 @@ constexpr int kMaxDevices = 64;
 
 thread_local int t_last_cuda_error = 0;
 
-// Kernel configuration used for every shape in this version.
-using MainCfg = sg::TileConfig<128, 128, 16, 6, 4, 2, 8, 8, /*PAIRED=*/true>;
+// ------------------------------------------------------------------ kernel variants
+// Every variant is the same persistent TMA/FFMA kernel with other tile sizes or
+// micro-kernel.  The default is chosen per shape by pick_variant(); a specific
+// one can be forced for tile-configuration sweeps with sgemm_set_variant().
+struct Variant {
+    const char *name;
+    int bm, bn, bk;
+    cudaError_t (*set_attr)();
+    void (*launch)(int grid, cudaStream_t s, const CUtensorMap &a, const CUtensorMap &b,
+                   const sg::MainParams &p);
+};
+
+template <class Cfg>
+cudaError_t set_attr_t() {
+    return cudaFuncSetAttribute(sg::sgemm_tma_ffma_kernel<Cfg>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::SMEM_BYTES));
+}
+
+template <class Cfg>
+void launch_t(int grid, cudaStream_t s, const CUtensorMap &a, const CUtensorMap &b,
+              const sg::MainParams &p) {
+    sg::sgemm_tma_ffma_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(a, b, p);
+}
+
+template <class Cfg>
+constexpr Variant make_variant(const char *name) {
+    return Variant{name, Cfg::BM, Cfg::BN, Cfg::BK, &set_attr_t<Cfg>, &launch_t<Cfg>};
+}
+
+using sg::MICRO_FFMA;
+using sg::MICRO_FFMA2;
+const Variant kVariants[] = {
+    make_variant<sg::TileConfig<256, 128, 16, 6, 4, 2, 16, 8, MICRO_FFMA2>>(
+        "ffma2 tile=256x128x16 stages=6 warps=4x2 thread=16x8"),
+    make_variant<sg::TileConfig<256, 128, 16, 6, 4, 2, 16, 8, MICRO_FFMA>>(
+        "ffma tile=256x128x16 stages=6 warps=4x2 thread=16x8"),
+    make_variant<sg::TileConfig<128, 256, 16, 6, 2, 4, 16, 8, MICRO_FFMA2>>(
+        "ffma2 tile=128x256x16 stages=6 warps=2x4 thread=16x8"),
+    make_variant<sg::TileConfig<256, 128, 32, 4, 4, 2, 16, 8, MICRO_FFMA2>>(
+        "ffma2 tile=256x128x32 stages=4 warps=4x2 thread=16x8"),
+    make_variant<sg::TileConfig<128, 128, 16, 6, 4, 2, 8, 8, MICRO_FFMA2>>(
+        "ffma2 tile=128x128x16 stages=6 warps=4x2 thread=8x8"),
+};
+constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
+std::atomic<int> g_forced_variant{-1};
+
+int pick_variant(int M, int N, int K) {
+    const int forced = g_forced_variant.load();
+    if (forced >= 0 && forced < kNumVariants) return forced;
+    (void)M;
+    (void)N;
+    (void)K;
+    return 0;
+}
 
 struct DeviceState {
     bool ready = false;
@@ -149,10 +201,8 @@ int device_state(DeviceState **out) {
             // keep up to 4 GiB of released workspace cached for reuse
             cuuint64_t keep = 4ull << 30;
             cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
-            e = cudaFuncSetAttribute(sg::sgemm_tma_ffma_kernel<MainCfg>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     int(MainCfg::SMEM_BYTES));
-            if (e != cudaSuccess) return cuda_fail(e);
+            for (const Variant &v : kVariants)
+                if ((e = v.set_attr()) != cudaSuccess) return cuda_fail(e);
             d.status = SGEMM_OK;
         }
         d.ready = true;
@@ -198,10 +248,9 @@ int sgemm_device(int M, int N, int K, float alpha, const float *A, int lda, cons
 
     if (K == 0 || alpha == 0.0f) return launch_scale(stream, C, ldc, M, N, beta, dev->sm_count);
 
-    using Cfg = MainCfg;
-    // ---- workspace: transposed (paired) A, and a re-pitched B if needed
-    const long long a_inner = (Cfg::PAIRED ? 2LL : 1LL) * M;
-    const long long ldat = round_up(a_inner, 4);
+    const Variant &var = kVariants[pick_variant(M, N, K)];
+    // ---- workspace: transposed A, and a re-pitched B if needed
+    const long long ldat = round_up(M, 4);
     const bool b_direct = aligned16(B) && (ldb % 4 == 0);
     const long long ldbp = b_direct ? ldb : round_up(N, 4);
     const size_t at_bytes = size_t(K) * size_t(ldat) * sizeof(float);
@@ -220,7 +269,7 @@ int sgemm_device(int M, int N, int K, float alpha, const float *A, int lda, cons
         ProfScope prof(stream, false);
         dim3 grid(unsigned(std::min<long long>((K + 31) / 32, 1LL << 20)),
                   unsigned(std::min<long long>((M + 31) / 32, 65535)));
-        sg::pack_a_transpose_kernel<Cfg::PAIRED><<<grid, 256, 0, stream>>>(A, lda, M, K, At, ldat);
+        sg::pack_a_transpose_kernel<<<grid, 256, 0, stream>>>(A, lda, M, K, At, ldat);
         g_launches.fetch_add(1);
         if (!b_direct) {
             const long long total = (long long)K * N;
@@ -236,8 +285,8 @@ int sgemm_device(int M, int N, int K, float alpha, const float *A, int lda, cons
     }
 
     CUtensorMap tmA, tmB;
-    if ((st = encode_2d(&tmA, At, a_inner, K, ldat, Cfg::A_ROW, Cfg::BK)) != SGEMM_OK ||
-        (st = encode_2d(&tmB, Bp, N, K, ldbp, Cfg::BN, Cfg::BK)) != SGEMM_OK) {
+    if ((st = encode_2d(&tmA, At, M, K, ldat, var.bm, var.bk)) != SGEMM_OK ||
+        (st = encode_2d(&tmB, Bp, N, K, ldbp, var.bn, var.bk)) != SGEMM_OK) {
         cudaFreeAsync(ws, stream);
         return st;
     }
@@ -250,16 +299,16 @@ int sgemm_device(int M, int N, int K, float alpha, const float *A, int lda, cons
     p.K = K;
     p.alpha = alpha;
     p.beta = beta;
-    p.tiles_m = int((M + Cfg::BM - 1) / Cfg::BM);
-    p.tiles_n = int((N + Cfg::BN - 1) / Cfg::BN);
-    p.group_m = 16;
+    p.tiles_m = int((M + var.bm - 1) / var.bm);
+    p.tiles_n = int((N + var.bn - 1) / var.bn);
+    p.group_m = 8;
     p.c_vec4 = (aligned16(C) && ldc % 4 == 0) ? 1 : 0;
     p.timeout_ns = g_timeout_ns.load();
     const long long tiles = (long long)p.tiles_m * p.tiles_n;
     const int grid = int(std::min<long long>(tiles, dev->sm_count));
     {
         ProfScope prof(stream, true);
-        sg::sgemm_tma_ffma_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        var.launch(grid, stream, tmA, tmB, p);
         g_launches.fetch_add(1);
     }
     e = cudaGetLastError();
@@ -424,9 +473,18 @@ SGEMM_API int sgemm_profile_collect(double *main_ms, long long *main_launches, d
 SGEMM_API long long sgemm_kernel_launch_count(void) { return g_launches.load(); }
 
 SGEMM_API const char *sgemm_config_string(int M, int N, int K) {
-    (void)M;
-    (void)N;
-    (void)K;
-    return "tma_ffma2 BM=128 BN=128 BK=16 stages=6 warps=4x2(+1 producer) thread_tile=8x8 "
-           "a_layout=transposed_paired";
+    return kVariants[pick_variant(M, N, K)].name;
+}
+
+SGEMM_API int sgemm_variant_count(void) { return kNumVariants; }
+
+SGEMM_API const char *sgemm_variant_name(int id) {
+    if (id < 0 || id >= kNumVariants) return "";
+    return kVariants[id].name;
+}
+
+SGEMM_API int sgemm_set_variant(int id) {
+    if (id < -1 || id >= kNumVariants) return SGEMM_ERR_INVALID_ARG;
+    g_forced_variant.store(id);
+    return SGEMM_OK;
 }

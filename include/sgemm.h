@@ -143,6 +143,19 @@ long long sgemm_kernel_launch_count(void);
  */
 const char *sgemm_config_string(int M, int N, int K);
 
+/*
+ * Kernel variants, for tile-configuration sweeps.  Every variant computes the
+ * same result within the tolerance above; they differ in tile sizes, pipeline
+ * depth and micro-kernel.  sgemm_variant_count() gives their number,
+ * sgemm_variant_name(i) a static description ("" for an invalid index), and
+ * sgemm_set_variant(i) forces variant i for later calls in this process
+ * (-1 restores the automatic choice; anything else out of range gives
+ * SGEMM_ERR_INVALID_ARG).
+ */
+int sgemm_variant_count(void);
+const char *sgemm_variant_name(int id);
+int sgemm_set_variant(int id);
+
 #ifdef __cplusplus
 }
 #endif

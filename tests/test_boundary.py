@@ -111,6 +111,15 @@ def test_empty_output_is_a_no_op_without_gpu(lib, kw):
     assert _call(lib, **kw) == 0
 
 
+def test_variant_selection_validates(lib):
+    lib.sgemm_variant_name.restype = ctypes.c_char_p
+    n = lib.sgemm_variant_count()
+    assert n >= 1
+    assert lib.sgemm_variant_name(n) == b"" and lib.sgemm_variant_name(-1) == b""
+    assert lib.sgemm_set_variant(n) == 1 and lib.sgemm_set_variant(-2) == 1
+    assert lib.sgemm_set_variant(n - 1) == 0 and lib.sgemm_set_variant(-1) == 0
+
+
 def test_timeout_setter_validates(lib):
     lib.sgemm_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
     assert lib.sgemm_set_wait_timeout_ns(10) == 1
@@ -120,7 +129,10 @@ def test_timeout_setter_validates(lib):
 def test_binding_loads_and_reports_config():
     from dense_fp32_gemm_02_gb300 import binding
     assert binding.version() == ctypes.CDLL(sgbuild.LIB_PATH).sgemm_version()
-    assert "BM=" in binding.config_string(8192, 8192, 8192)
+    assert "tile=" in binding.config_string(8192, 8192, 8192)
+    names = binding.variants()
+    assert len(names) >= 1 and all("tile=" in n for n in names)
+    assert binding.config_string(8192, 8192, 8192) in names
     with pytest.raises(binding.SgemmError) as e:
         binding.check(1)
     assert "INVALID_ARG" in str(e.value)

@@ -210,3 +210,23 @@ def test_kernel_launches_are_counted():
     A, B, _ = make_inputs(64, 64, 64, seed=23)
     run_gpu(A, B, None, 1.0, 0.0)
     assert binding.kernel_launch_count() - before >= 2     # pack + main
+
+
+@pytest.mark.parametrize("M,N,K", [(600, 520, 300), (257, 1031, 95), (1, 300, 17)])
+def test_every_kernel_variant_matches_oracle(M, N, K):
+    """Each compiled tile configuration, forced in turn: integer inputs bit-exact
+    and random inputs within the bound, on shapes that leave ragged tiles."""
+    from dense_fp32_gemm_02_gb300 import binding
+    try:
+        for v in range(len(binding.variants())):
+            binding.set_variant(v)
+            A, B, C = make_inputs(M, N, K, "int4", "int4", "int4", seed=v + 100)
+            ref, _ = oracle.sgemm(A, B, C, 1.5, 0.5)
+            got = run_gpu(A, B, C, 1.5, 0.5).cpu().numpy()
+            assert np.array_equal(got, ref), (v, M, N, K)
+            A, B, C = make_inputs(M, N, K, "normal", "upm1", "normal", seed=v + 200)
+            ref, bound = oracle.sgemm(A, B, C, -1.25, 0.75)
+            got = run_gpu(A, B, C, -1.25, 0.75).cpu().numpy()
+            assert_within_bound(got, ref, bound, f"variant {v}")
+    finally:
+        binding.set_variant(-1)
