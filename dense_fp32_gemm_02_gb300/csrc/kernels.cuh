@@ -134,12 +134,16 @@ __device__ __forceinline__ void outer_product(float (&acc)[Cfg::TM][Cfg::TN],
                                               const float (&fa)[Cfg::TM],
                                               const float (&fb)[Cfg::TN]) {
     if constexpr (Cfg::MICRO == MICRO_FFMA2) {
+        // Row pair outer, column inner: the (a[i], a[i+1]) operand stays the same
+        // over TN consecutive instructions.  Measured on sm_103 (16x8 tile, two
+        // warps per sub-partition, fragments from registers): 127 FMA/clk/SM in
+        // this order against 118 with the column loop outside.
 #pragma unroll
-        for (int j = 0; j < Cfg::TN; ++j) {
-            const float2 bb = make_float2(fb[j], fb[j]);
+        for (int i = 0; i < Cfg::TM; i += 2) {
+            const float2 aa = make_float2(fa[i], fa[i + 1]);
 #pragma unroll
-            for (int i = 0; i < Cfg::TM; i += 2) {
-                const float2 r = ffma2(make_float2(fa[i], fa[i + 1]), bb,
+            for (int j = 0; j < Cfg::TN; ++j) {
+                const float2 r = ffma2(aa, make_float2(fb[j], fb[j]),
                                        make_float2(acc[i][j], acc[i + 1][j]));
                 acc[i][j] = r.x;
                 acc[i + 1][j] = r.y;
@@ -158,7 +162,7 @@ __device__ __forceinline__ void outer_product(float (&acc)[Cfg::TM][Cfg::TN],
 // all its tiles form one sequence q = 0, 1, 2, ...; slab q lives in ring stage
 // q % STAGES.  Thread 0 issues the TMA copies of slab q + STAGES - 1 when the
 // CTA starts consuming slab q, after every warp has released that stage's
-// previous contents (empty barrier).  Warps wait on the full barrier of a stage
+// previous contents (empty barrier), so STAGES - 1 slabs are in flight.  Warps wait on the full barrier of a stage
 // (TMA byte count) before reading it and arrive on its empty barrier after.
 // There is no separate producer warp: with 8 warps per CTA each SM sub-
 // partition holds two warps and a thread can keep up to 255 registers.
@@ -192,34 +196,47 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const int k_tiles = (p.K + BK - 1) / BK;
     const int my_tiles = blockIdx.x < num_tiles ? (num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const long long total_slabs = (long long)my_tiles * k_tiles;
-    long long issued = 0;    // thread 0 only: slabs whose copies were issued
-    bool aborted = false;
 
-    // Thread 0: issue the copies of slab q.  Returns false if the wait for the
-    // stage to be released expired.
-    auto issue = [&](long long q) -> bool {
-        const int s = int(q % STAGES);
-        const long long use = q / STAGES;
-        if (use > 0 && !mbar_wait(&empty[s], uint32_t((use - 1) & 1), p.timeout_ns)) {
+    // Issue state, used by thread 0 only: the next slab to copy is k-slab
+    // `pkt` of this CTA's tile number `pj`, into stage `pstage` whose empty
+    // barrier is in phase parity `pphase`.
+    long long issued = 0;
+    int pj = 0, pkt = 0, pstage = 0, ptm = 0, ptn = 0;
+    uint32_t pphase = 0;
+    bool aborted = false;
+    if (threadIdx.x == 0 && my_tiles > 0) tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, ptm, ptn);
+
+    // Thread 0: issue the copies of the next slab.  Returns false if the wait
+    // for its stage to be released expired.
+    auto issue_next = [&]() -> bool {
+        // first use of a stage: parity 1 refers to the phase before the
+        // barrier's first one and counts as complete
+        if (!mbar_wait(&empty[pstage], pphase ^ 1u, p.timeout_ns)) {
             atomicOr(&g_error_word, ERR_EMPTY_WAIT);
             return false;
         }
-        const int j = int(q / k_tiles);
-        const int kt = int(q - (long long)j * k_tiles);
-        int tm, tn;
-        tile_coords(blockIdx.x + j * gridDim.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-        mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
-        tma_load_2d(sA + s * Cfg::A_STAGE, &tmA, &full[s], tm * BM, kt * BK);
-        tma_load_2d(sB + s * Cfg::B_STAGE, &tmB, &full[s], tn * BN, kt * BK);
-        issued = q + 1;
+        mbar_arrive_expect_tx(&full[pstage], Cfg::STAGE_BYTES);
+        tma_load_2d(sA + pstage * Cfg::A_STAGE, &tmA, &full[pstage], ptm * BM, pkt * BK);
+        tma_load_2d(sB + pstage * Cfg::B_STAGE, &tmB, &full[pstage], ptn * BN, pkt * BK);
+        ++issued;
+        if (++pstage == STAGES) {
+            pstage = 0;
+            pphase ^= 1u;
+        }
+        if (++pkt == k_tiles) {
+            pkt = 0;
+            ++pj;
+            if (pj < my_tiles)
+                tile_coords(blockIdx.x + pj * gridDim.x, p.tiles_m, p.tiles_n, p.group_m, ptm, ptn);
+        }
         return true;
     };
 
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        for (long long q = 0; q < STAGES - 1 && q < total_slabs; ++q)
-            if (!issue(q)) {
+        while (issued < STAGES - 1 && issued < total_slabs)
+            if (!issue_next()) {
                 aborted = true;
                 break;
             }
@@ -233,7 +250,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const int a_off = wm0 + lm * 4;
     const int b_off = wn0 + ln * 4;
 
-    long long q = 0;    // next slab to consume
+    int stage = 0;          // stage of the next slab to consume
+    uint32_t phase = 0;     // parity of that stage's full barrier
     for (int j = 0; j < my_tiles; ++j) {
         int tm, tn;
         tile_coords(blockIdx.x + j * gridDim.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
@@ -244,11 +262,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
             for (int jj = 0; jj < TN; ++jj) acc[i][jj] = 0.0f;
 
-        for (int kt = 0; kt < k_tiles; ++kt, ++q) {
-            if (threadIdx.x == 0 && !aborted && q + STAGES - 1 < total_slabs)
-                aborted = !issue(q + STAGES - 1);
-            const int s = int(q % STAGES);
-            bool ok = !aborted && mbar_wait(&full[s], uint32_t((q / STAGES) & 1), p.timeout_ns);
+        for (int kt = 0; kt < k_tiles; ++kt) {
+            if (threadIdx.x == 0 && !aborted && issued < total_slabs) aborted = !issue_next();
+            const int s = stage;
+            bool ok = !aborted && mbar_wait(&full[s], phase, p.timeout_ns);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 if (lane == 0) atomicOr(&g_error_word, ERR_FULL_WAIT);
@@ -270,6 +287,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
         }
 
         // -------------------------------------------------------------- epilogue
