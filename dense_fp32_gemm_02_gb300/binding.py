@@ -29,6 +29,8 @@ lib.sgemm.argtypes = [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]
 lib.sgemm.restype = _i
 lib.sgemm_host.argtypes = [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]
 lib.sgemm_host.restype = _i
+lib.sgemm_noalloc.argtypes = [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]
+lib.sgemm_noalloc.restype = _i
 lib.sgemm_status_string.argtypes = [_i]
 lib.sgemm_status_string.restype = ctypes.c_char_p
 lib.sgemm_version.argtypes = []
@@ -63,6 +65,7 @@ SGEMM_ERR_UNSUPPORTED_DEVICE = 2
 SGEMM_ERR_CUDA = 3
 SGEMM_ERR_TIMEOUT = 4
 SGEMM_ERR_ALLOC = 5
+SGEMM_ERR_TOO_LARGE = 6
 
 
 class SgemmError(RuntimeError):
@@ -131,6 +134,28 @@ def sgemm_into(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
                        float(beta), C.data_ptr(), _ld(C, N), _stream_handle(stream, C.device))
     check(st)
     return C
+
+
+def sgemm_noalloc_into(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """Like sgemm_into(), through the entry point that allocates no device
+    memory (its workspace is a fixed array; see include/sgemm.h)."""
+    import torch
+    for name, t in (("A", A), ("B", B), ("C", C)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA float32 tensor")
+    if not (A.device == B.device == C.device):
+        raise ValueError("A, B and C must be on the same device")
+    M, N, K = _shapes(A, B, C)
+    with torch.cuda.device(C.device):
+        st = lib.sgemm_noalloc(M, N, K, float(alpha), A.data_ptr(), _ld(A, K), B.data_ptr(),
+                               _ld(B, N), float(beta), C.data_ptr(), _ld(C, N),
+                               _stream_handle(stream, C.device))
+    check(st)
+    return C
+
+
+# floats in the fixed scratch array of sgemm_noalloc (see include/sgemm.h)
+NOALLOC_SCRATCH_FLOATS = 8 * 1024 * 1024
 
 
 def sgemm(A, B, C=None, alpha: float = 1.0, beta: float = 0.0, stream=None):

@@ -328,6 +328,126 @@ int read_and_clear_error_word(cudaStream_t stream) {
     return v ? SGEMM_ERR_TIMEOUT : SGEMM_OK;
 }
 
+// ------------------------------------------------------------------ no-allocation path
+// Scratch of sgemm_noalloc(): a fixed device array instead of pool memory.  It
+// holds the transposed copy of A and, when B does not meet the TMA's 16-byte
+// rule, the re-pitched copy of B.  Every device that loads this library keeps
+// it (32 MiB) until the process exits.
+constexpr size_t kNoAllocScratchFloats = size_t(8) << 20;
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+
+struct NoAllocState {
+    bool ready = false;
+    int status = SGEMM_OK;
+    int sm_count = 0;
+    float *scratch = nullptr;   // device address of g_noalloc_scratch on this device
+};
+NoAllocState g_noalloc[kMaxDevices];
+
+// Per-device set-up of the no-allocation path, done on the first call on each
+// device with that device current: device checks, kernel attributes and the
+// device address of the scratch array.  Allocates nothing.
+int noalloc_state(NoAllocState **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    NoAllocState &d = g_noalloc[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if (major != 10 || minor != 3) {
+            d.status = SGEMM_ERR_UNSUPPORTED_DEVICE;
+        } else {
+            if (!g_encode_tiled) {
+                void *fn = nullptr;
+                cudaDriverEntryPointQueryResult q;
+                e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+                if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                    return cuda_fail(e != cudaSuccess ? e : cudaErrorNotSupported);
+                g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+            }
+            for (const Variant &v : kVariants)
+                if ((e = v.set_attr()) != cudaSuccess) return cuda_fail(e);
+            // In host code the array's name is only a host-side stand-in: the
+            // kernels must be given its device address.
+            void *ptr = nullptr;
+            if ((e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch)) != cudaSuccess)
+                return cuda_fail(e);
+            d.scratch = static_cast<float *>(ptr);
+            d.status = SGEMM_OK;
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return d.status;
+}
+
+int sgemm_device_noalloc(int M, int N, int K, float alpha, const float *A, int lda,
+                         const float *B, int ldb, float beta, float *C, int ldc,
+                         cudaStream_t stream) {
+    int st = checked_args(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta);
+    if (st != SGEMM_OK || M == 0 || N == 0) return st;
+    NoAllocState *dev = nullptr;
+    if ((st = noalloc_state(&dev)) != SGEMM_OK) return st;
+
+    if (K == 0 || alpha == 0.0f) return launch_scale(stream, C, ldc, M, N, beta, dev->sm_count);
+
+    const Variant &var = kVariants[pick_variant(M, N, K)];
+    const long long ldat = round_up(M, 4);
+    const bool b_direct = aligned16(B) && (ldb % 4 == 0);
+    const long long ldbp = b_direct ? ldb : round_up(N, 4);
+    const long long at_floats = round_up((long long)K * ldat, 64);   // 256-byte aligned
+    const long long bp_floats = b_direct ? 0 : (long long)K * ldbp;
+    if ((unsigned long long)(at_floats + bp_floats) > kNoAllocScratchFloats)
+        return SGEMM_ERR_TOO_LARGE;
+    float *At = dev->scratch;
+    float *Bp = b_direct ? const_cast<float *>(B) : dev->scratch + at_floats;
+
+    dim3 grid(unsigned(std::min<long long>((K + 31) / 32, 1LL << 20)),
+              unsigned(std::min<long long>((M + 31) / 32, 65535)));
+    sg::pack_a_transpose_kernel<<<grid, 256, 0, stream>>>(A, lda, M, K, At, ldat);
+    g_launches.fetch_add(1);
+    if (!b_direct) {
+        const long long total = (long long)K * N;
+        const int blocks = int(std::min<long long>((total + 255) / 256, (long long)dev->sm_count * 16));
+        sg::pack_b_copy_kernel<<<blocks, 256, 0, stream>>>(B, ldb, K, N, Bp, ldbp);
+        g_launches.fetch_add(1);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    CUtensorMap tmA, tmB;
+    if ((st = encode_2d(&tmA, At, M, K, ldat, var.bm, var.bk)) != SGEMM_OK ||
+        (st = encode_2d(&tmB, Bp, N, K, ldbp, var.bn, var.bk)) != SGEMM_OK)
+        return st;
+
+    sg::MainParams p;
+    p.C = C;
+    p.ldc = ldc;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.tiles_m = int((M + var.bm - 1) / var.bm);
+    p.tiles_n = int((N + var.bn - 1) / var.bn);
+    p.group_m = 8;
+    p.c_vec4 = (aligned16(C) && ldc % 4 == 0) ? 1 : 0;
+    p.timeout_ns = g_timeout_ns.load();
+    const long long tiles = (long long)p.tiles_m * p.tiles_n;
+    const int grid_main = int(std::min<long long>(tiles, dev->sm_count));
+    var.launch(grid_main, stream, tmA, tmB, p);
+    g_launches.fetch_add(1);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? SGEMM_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 // ==================================================================== C ABI
@@ -398,6 +518,7 @@ SGEMM_API const char *sgemm_status_string(int status) {
         case SGEMM_ERR_CUDA: return "SGEMM_ERR_CUDA: a CUDA call failed (see sgemm_last_cuda_error)";
         case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT: a bounded in-kernel wait expired";
         case SGEMM_ERR_ALLOC: return "SGEMM_ERR_ALLOC: workspace allocation failed";
+        case SGEMM_ERR_TOO_LARGE: return "SGEMM_ERR_TOO_LARGE: the problem needs more scratch than the fixed array of sgemm_noalloc holds";
         default: return "unknown sgemm status";
     }
 }
@@ -487,4 +608,11 @@ SGEMM_API int sgemm_set_variant(int id) {
     if (id < -1 || id >= kNumVariants) return SGEMM_ERR_INVALID_ARG;
     g_forced_variant.store(id);
     return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_noalloc(int M, int N, int K, float alpha, const float *A, int lda,
+                            const float *B, int ldb, float beta, float *C, int ldc,
+                            sgemm_stream_t stream) {
+    return sgemm_device_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                                reinterpret_cast<cudaStream_t>(stream));
 }

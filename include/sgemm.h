@@ -44,7 +44,8 @@ typedef enum {
     SGEMM_ERR_UNSUPPORTED_DEVICE = 2, /* the current CUDA device is not sm_103 */
     SGEMM_ERR_CUDA = 3,               /* a CUDA runtime/driver call failed; see sgemm_last_cuda_error() */
     SGEMM_ERR_TIMEOUT = 4,            /* a bounded in-kernel wait expired (reported by sgemm_device_status) */
-    SGEMM_ERR_ALLOC = 5               /* device or pinned workspace allocation failed */
+    SGEMM_ERR_ALLOC = 5,              /* device or pinned workspace allocation failed */
+    SGEMM_ERR_TOO_LARGE = 6           /* sgemm_noalloc: the problem does not fit its fixed scratch */
 } sgemm_status;
 
 /*
@@ -155,6 +156,45 @@ const char *sgemm_config_string(int M, int N, int K);
 int sgemm_variant_count(void);
 const char *sgemm_variant_name(int id);
 int sgemm_set_variant(int id);
+
+/*
+ * sgemm_noalloc -- the same GEMM as sgemm(), for callers that cannot allocate
+ * device memory.  The pages this library follows have no counterpart to it.
+ *
+ * Who needs it: code that runs where allocating is not allowed or not safe,
+ * for instance inside a host framework that has already handed all device
+ * memory to its own allocator, or on a latency-critical path where a
+ * cudaMalloc (which can synchronise the device or fail under memory pressure)
+ * must not happen.  sgemm() takes its workspace from a memory pool, which is
+ * an allocation; this entry point never allocates: no cudaMalloc, cudaFree,
+ * pool or library allocation.
+ *
+ * How: the workspace (the transposed copy of A, plus a re-pitched copy of B
+ * when B's address or row pitch is not a multiple of 16 bytes) lives in one
+ * fixed array in device memory of 8,388,608 floats (32 MiB), which every
+ * device that loads this library keeps until the process exits.
+ * A, B and C are the caller's device pointers, as for sgemm().
+ *
+ * Limit: K * roundup(M, 4), rounded up to a multiple of 64, plus
+ * K * roundup(N, 4) when B needs the re-pitched copy, must not exceed that
+ * number of floats; otherwise the call returns SGEMM_ERR_TOO_LARGE and does
+ * nothing.  Problems with alpha == 0 or K == 0 need no scratch.
+ *
+ * Set-up: the first call on each device (made with that device current) looks
+ * up the array's device address and configures the kernels; make that first
+ * call before any stream capture.
+ *
+ * Sharing: every call on a device uses the same array, and it keeps whatever
+ * the previous call left there; each call overwrites the part it reads before
+ * reading it.  Calls whose work overlaps on the GPU (on different streams, or
+ * from several host threads) race on the array: order them on one stream or
+ * synchronise between them.  Results and errors are otherwise as for sgemm().
+ */
+int sgemm_noalloc(int M, int N, int K, float alpha,
+                  const float *A, int lda,
+                  const float *B, int ldb,
+                  float beta, float *C, int ldc,
+                  sgemm_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -55,7 +55,7 @@ def test_library_exports_nothing_undeclared():
 
 def test_status_strings_and_version(lib):
     lib.sgemm_status_string.restype = ctypes.c_char_p
-    for st in range(6):
+    for st in range(7):
         s = lib.sgemm_status_string(st).decode()
         assert s.startswith("SGEMM_")
     assert b"unknown" in lib.sgemm_status_string(99)
