@@ -57,7 +57,7 @@ enum Micro : int {
 // columns apart, so a warp covers (4*TM) x (8*TN) outputs and every fragment
 // load is one 128-bit shared load of four consecutive floats.
 template <int BM_, int BN_, int BK_, int STAGES_, int WARPS_M_, int WARPS_N_, int TM_, int TN_,
-          int MICRO_>
+          int MICRO_, bool WS_>
 struct TileConfig {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_;
@@ -66,18 +66,36 @@ struct TileConfig {
     static constexpr int LANES_M = 4, LANES_N = 8;
     static constexpr int WM = TM * LANES_M, WN = TN * LANES_N;
     static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
-    static constexpr int THREADS = CONSUMER_WARPS * 32;
+    static constexpr int CONSUMER_THREADS = CONSUMER_WARPS * 32;
+    // WS: a producer warpgroup in front of the consumer warps issues the TMA
+    // copies; otherwise consumer thread 0 issues them between its own slabs.
+    static constexpr bool WS = WS_;
+    static constexpr int PRODUCER_THREADS = WS ? 128 : 0;
+    static constexpr int THREADS = PRODUCER_THREADS + CONSUMER_THREADS;
+    // Register split (setmaxnreg, WS only): the launch gives every thread
+    // LAUNCH_REGS; the producer warpgroup drops to PRODUCER_REGS and the
+    // consumers rise to CONSUMER_REGS.  The split must fit the launch's total.
+    static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8;
+    static constexpr int PRODUCER_REGS = 40;
+    static constexpr int CONSUMER_REGS_FIT =
+        ((LAUNCH_REGS * THREADS - PRODUCER_REGS * PRODUCER_THREADS) / CONSUMER_THREADS) / 8 * 8;
+    static constexpr int CONSUMER_REGS = CONSUMER_REGS_FIT > 248 ? 248 : CONSUMER_REGS_FIT;
     static constexpr int A_STAGE = BK * BM;   // floats: K-rows of the transposed A tile
     static constexpr int B_STAGE = BK * BN;   // floats: K-rows of the B tile
     static constexpr uint32_t STAGE_BYTES = uint32_t(A_STAGE + B_STAGE) * 4u;
     static constexpr size_t SMEM_BYTES =
         size_t(STAGES) * STAGE_BYTES + 2 * STAGES * sizeof(uint64_t) + 16 + 1024;
+    static constexpr int TILE_FLOATS = BM * BN;
 
     static_assert(WM * WARPS_M == BM && WN * WARPS_N == BN, "warp grid must cover the tile");
     static_assert(TM % 4 == 0 && TN % 4 == 0, "thread tile is made of 4x4 sub-tiles");
     static_assert(BM <= 256 && BN <= 256 && BK <= 256, "TMA box edge is at most 256");
     static_assert((A_STAGE * 4) % 1024 == 0 && (B_STAGE * 4) % 1024 == 0, "stage alignment");
     static_assert(SMEM_BYTES <= 232448, "at most 227 KB of shared memory per CTA");
+    static_assert(CONSUMER_WARPS == 8, "two consumer warpgroups");
+    static_assert(!WS || PRODUCER_REGS * PRODUCER_THREADS + CONSUMER_REGS * CONSUMER_THREADS <=
+                             LAUNCH_REGS * THREADS,
+                  "register split exceeds the launch allocation");
 };
 
 struct MainParams {
@@ -88,6 +106,14 @@ struct MainParams {
     int tiles_m, tiles_n, group_m;
     int c_vec4;              // C base 16-byte aligned and ldc % 4 == 0
     unsigned long long timeout_ns;
+    // Work split.  Tiles [0, dp_tiles) are whole-tile work, CTA b taking tiles
+    // b, b + gridDim.x, ...  The k-slabs of the remaining tiles, in tile-major
+    // order, form one range of sk_slabs slabs cut into gridDim.x contiguous,
+    // nearly equal pieces, one per CTA (stream-K).
+    int dp_tiles;
+    long long sk_slabs;
+    float *partials;         // 2 * gridDim.x slots of BM*BN floats (sk_slabs > 0)
+    int *counters;           // one per stream-K tile, zero at launch (sk_slabs > 0)
 };
 
 // Grouped raster: tiles are visited in groups of `group_m` tile-rows, column
@@ -105,14 +131,28 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
     tn = local / gm;
 }
 
+// 128-bit shared-memory load from a 32-bit shared-window address.  Explicit
+// shared addressing keeps fragment addresses in one 32-bit register each; with
+// generic 64-bit pointers the consumer loop needed 255 registers instead of 222
+// and ran 7% slower on sm_103.  The memory clobber keeps the loads between the
+// barrier wait and release that guard the stage they read.
+__device__ __forceinline__ float4 lds128(uint32_t addr) {
+    float4 v;
+    asm("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "r"(addr)
+        : "memory");
+    return v;
+}
+
 // Fragment loads for one k: TM values of A (a K-row of the transposed tile)
-// and TN values of B, 128 bits at a time.
+// and TN values of B, 128 bits at a time.  a_row, b_row: shared addresses.
 template <class Cfg>
-__device__ __forceinline__ void load_fragments(const float *a_row, const float *b_row,
+__device__ __forceinline__ void load_fragments(uint32_t a_row, uint32_t b_row,
                                                float (&fa)[Cfg::TM], float (&fb)[Cfg::TN]) {
 #pragma unroll
     for (int s = 0; s < Cfg::TM / 4; ++s) {
-        const float4 v = *reinterpret_cast<const float4 *>(a_row + s * 16);
+        const float4 v = lds128(a_row + s * 16 * 4);
         fa[4 * s + 0] = v.x;
         fa[4 * s + 1] = v.y;
         fa[4 * s + 2] = v.z;
@@ -120,7 +160,7 @@ __device__ __forceinline__ void load_fragments(const float *a_row, const float *
     }
 #pragma unroll
     for (int t = 0; t < Cfg::TN / 4; ++t) {
-        const float4 v = *reinterpret_cast<const float4 *>(b_row + t * 32);
+        const float4 v = lds128(b_row + t * 32 * 4);
         fb[4 * t + 0] = v.x;
         fb[4 * t + 1] = v.y;
         fb[4 * t + 2] = v.z;
@@ -157,104 +197,352 @@ __device__ __forceinline__ void outer_product(float (&acc)[Cfg::TM][Cfg::TN],
     }
 }
 
-// ------------------------------------------------------------------ main kernel
-// Persistent kernel: CTA b computes tiles b, b + gridDim.x, ...  The k-slabs of
-// all its tiles form one sequence q = 0, 1, 2, ...; slab q lives in ring stage
-// q % STAGES.  Thread 0 issues the TMA copies of slab q + STAGES - 1 when the
-// CTA starts consuming slab q, after every warp has released that stage's
-// previous contents (empty barrier), so STAGES - 1 slabs are in flight.  Warps wait on the full barrier of a stage
-// (TMA byte count) before reading it and arrive on its empty barrier after.
-// There is no separate producer warp: with 8 warps per CTA each SM sub-
-// partition holds two warps and a thread can keep up to 255 registers.
+// ------------------------------------------------------------------ warp specialisation
+template <int N>
+__device__ __forceinline__ void regs_decrease() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_increase() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+// Named CTA barrier `id` over `count` threads (whole, converged warps).
+__device__ __forceinline__ void named_barrier(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ------------------------------------------------------------------ work split
+// One contiguous run of k-slabs of one tile that a CTA computes.
+struct Segment {
+    int tile;     // tile index in raster order
+    int kb, ke;   // slab range [kb, ke)
+    int slot;     // partial-sum slot, or -1 when the segment is the whole tile
+};
+
+// First stream-K slab of CTA b (relative to the stream-K region).
+__device__ __forceinline__ long long sk_start(int b, long long sk_slabs, int grid) {
+    return ((long long)b * sk_slabs) / grid;
+}
+
+// The CTA whose stream-K range holds slab x: the largest b with sk_start(b) <= x.
+__device__ __forceinline__ int sk_owner(long long x, long long sk_slabs, int grid) {
+    int b = int(((x + 1) * grid - 1) / sk_slabs);
+    if (b > grid - 1) b = grid - 1;
+    while (b > 0 && sk_start(b, sk_slabs, grid) > x) --b;
+    while (b + 1 < grid && sk_start(b + 1, sk_slabs, grid) <= x) ++b;
+    return b;
+}
+
+// Segments of one CTA, in the order it computes them: its whole tiles, then
+// the pieces of its stream-K range (at most one partial piece at each end).
+// A partial piece at the start of the range uses slot 2b, one at the end 2b+1.
+struct SegmentIter {
+    int next_dp;
+    long long x, end;
+    bool at_first_sk;
+
+    __device__ void init(const MainParams &p) {
+        next_dp = blockIdx.x;
+        x = sk_start(blockIdx.x, p.sk_slabs, gridDim.x);
+        end = sk_start(blockIdx.x + 1, p.sk_slabs, gridDim.x);
+        at_first_sk = true;
+    }
+
+    __device__ bool next(const MainParams &p, int k_tiles, Segment &seg) {
+        if (next_dp < p.dp_tiles) {
+            seg.tile = next_dp;
+            seg.kb = 0;
+            seg.ke = k_tiles;
+            seg.slot = -1;
+            next_dp += gridDim.x;
+            return true;
+        }
+        if (x >= end) return false;
+        const long long rel = x / k_tiles;
+        seg.tile = p.dp_tiles + int(rel);
+        seg.kb = int(x - rel * k_tiles);
+        seg.ke = int(min((long long)k_tiles, (long long)seg.kb + (end - x)));
+        const bool whole = (seg.kb == 0 && seg.ke == k_tiles);
+        seg.slot = whole ? -1 : 2 * int(blockIdx.x) + (at_first_sk ? 0 : 1);
+        at_first_sk = false;
+        x += seg.ke - seg.kb;
+        return true;
+    }
+};
+
+// Segment number `si` of this CTA (the same sequence SegmentIter yields),
+// computed from scratch so a caller keeps only the counter between segments.
+__device__ __forceinline__ bool segment_at(const MainParams &p, int k_tiles, int si, Segment &seg) {
+    const int b = blockIdx.x, G = gridDim.x;
+    const int n_dp = p.dp_tiles > b ? (p.dp_tiles - 1 - b) / G + 1 : 0;
+    if (si < n_dp) {
+        seg.tile = b + si * G;
+        seg.kb = 0;
+        seg.ke = k_tiles;
+        seg.slot = -1;
+        return true;
+    }
+    const int j = si - n_dp;
+    const long long x0 = sk_start(b, p.sk_slabs, G), x1 = sk_start(b + 1, p.sk_slabs, G);
+    const long long x = j == 0 ? x0 : (x0 / k_tiles + j) * (long long)k_tiles;
+    if (x >= x1) return false;
+    const long long rel = x / k_tiles;
+    seg.tile = p.dp_tiles + int(rel);
+    seg.kb = int(x - rel * k_tiles);
+    seg.ke = int(min((long long)k_tiles, (long long)seg.kb + (x1 - x)));
+    const bool whole = (seg.kb == 0 && seg.ke == k_tiles);
+    seg.slot = whole ? -1 : 2 * b + (j == 0 ? 0 : 1);
+    return true;
+}
+
+// ------------------------------------------------------------------ epilogue
+// C = alpha * acc + beta * C for this thread's outputs of tile (tm, tn);
+// C is not read when beta == 0.  Rows >= M and columns >= N are not written.
 template <class Cfg>
-__global__ void __launch_bounds__(Cfg::THREADS, 1)
-    sgemm_tma_ffma_kernel(const __grid_constant__ CUtensorMap tmA,
-                          const __grid_constant__ CUtensorMap tmB, const MainParams p) {
+__device__ __forceinline__ void store_tile(const float (&acc)[Cfg::TM][Cfg::TN], const MainParams &p,
+                                           int tm, int tn, int a_off, int b_off) {
+    const int row0 = tm * Cfg::BM + a_off;
+    const int col0 = tn * Cfg::BN + b_off;
+    const float alpha = p.alpha, beta = p.beta;
+#pragma unroll
+    for (int s4 = 0; s4 < Cfg::TM / 4; ++s4) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int row = row0 + s4 * 16 + r;
+            if (row >= p.M) continue;
+            float *crow = p.C + (long long)row * p.ldc;
+#pragma unroll
+            for (int t = 0; t < Cfg::TN / 4; ++t) {
+                const int col = col0 + t * 32;
+                const float *v = &acc[4 * s4 + r][4 * t];
+                if (p.c_vec4 && col + 3 < p.N) {
+                    float4 o;
+                    if (beta != 0.0f) {
+                        const float4 c = __ldcs(reinterpret_cast<const float4 *>(crow + col));
+                        o.x = fmaf(alpha, v[0], beta * c.x);
+                        o.y = fmaf(alpha, v[1], beta * c.y);
+                        o.z = fmaf(alpha, v[2], beta * c.z);
+                        o.w = fmaf(alpha, v[3], beta * c.w);
+                    } else {
+                        o.x = alpha * v[0];
+                        o.y = alpha * v[1];
+                        o.z = alpha * v[2];
+                        o.w = alpha * v[3];
+                    }
+                    __stcs(reinterpret_cast<float4 *>(crow + col), o);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (col + e < p.N) {
+                            const float c = (beta != 0.0f) ? beta * crow[col + e] : 0.0f;
+                            crow[col + e] = (beta != 0.0f) ? fmaf(alpha, v[e], c) : alpha * v[e];
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Partial-sum slot layout: float4 number v of consumer thread t sits at
+// (v * CONSUMER_THREADS + t),
+// so each warp store or load of one float4 per lane covers 512 contiguous bytes.
+template <class Cfg>
+__device__ __forceinline__ void write_partial(const float (&acc)[Cfg::TM][Cfg::TN], float *slot,
+                                              int ctid) {
+#pragma unroll
+    for (int i = 0; i < Cfg::TM; ++i)
+#pragma unroll
+        for (int j4 = 0; j4 < Cfg::TN / 4; ++j4) {
+            const int v = i * (Cfg::TN / 4) + j4;
+            __stcg(reinterpret_cast<float4 *>(slot) + (size_t)v * Cfg::CONSUMER_THREADS + ctid,
+                   make_float4(acc[i][4 * j4], acc[i][4 * j4 + 1], acc[i][4 * j4 + 2],
+                               acc[i][4 * j4 + 3]));
+        }
+}
+
+// Row i of the thread tile, summed over the tile's pieces in k order: pieces
+// are the non-empty stream-K ranges of CTAs b_lo..b_hi; sk_start advances by
+// sk_q plus a carry from sk_r (no division).  The piece of CTA b sits in slot
+// 2b when the tile is b's first one, else in slot 2b+1.
+template <class Cfg>
+__device__ __forceinline__ void sum_pieces_row(float (&row)[Cfg::TN], const float *partials, int i,
+                                               int ctid, int b_lo, int b_hi, long long q0, int r0,
+                                               long long sk_q, int sk_r, long long tile_start) {
+    float4 sum[Cfg::TN / 4];
+    bool first = true;
+    long long b0 = q0;
+    int r = r0;
+    for (int b = b_lo; b <= b_hi; ++b) {
+        long long b1 = b0 + sk_q;
+        r += sk_r;
+        if (r >= int(gridDim.x)) {
+            r -= gridDim.x;
+            ++b1;
+        }
+        if (b0 < b1) {
+            const int slot = 2 * b + (b0 >= tile_start ? 0 : 1);
+            const float4 *src = reinterpret_cast<const float4 *>(partials + (size_t)slot * Cfg::TILE_FLOATS);
+#pragma unroll
+            for (int j4 = 0; j4 < Cfg::TN / 4; ++j4) {
+                const float4 q =
+                    __ldcg(src + (size_t)(i * (Cfg::TN / 4) + j4) * Cfg::CONSUMER_THREADS + ctid);
+                if (first) {
+                    sum[j4] = q;
+                } else {
+                    sum[j4].x += q.x;
+                    sum[j4].y += q.y;
+                    sum[j4].z += q.z;
+                    sum[j4].w += q.w;
+                }
+            }
+            first = false;
+        }
+        b0 = b1;
+    }
+#pragma unroll
+    for (int j4 = 0; j4 < Cfg::TN / 4; ++j4) {
+        row[4 * j4] = sum[j4].x;
+        row[4 * j4 + 1] = sum[j4].y;
+        row[4 * j4 + 2] = sum[j4].z;
+        row[4 * j4 + 3] = sum[j4].w;
+    }
+}
+
+// ------------------------------------------------------------------ main kernel
+// Shared-memory ring and flags of one CTA.
+struct Ring {
+    float *sA, *sB;
+    uint64_t *full, *empty;
+    volatile int *abort_flag;
+};
+
+// State of the TMA issuer: the next slab to copy is slab `slab` of segment
+// `seg` (tile coordinates tm, tn) into ring stage `stage`, whose empty barrier
+// is in phase parity `phase`.
+struct IssueState {
+    SegmentIter iter;
+    Segment seg;
+    long long issued;
+    int have, slab, tm, tn, stage;
+    uint32_t phase;
+
+    __device__ void init(const MainParams &p) {
+        iter.init(p);
+        issued = 0;
+        have = 0;
+        slab = tm = tn = stage = 0;
+        phase = 0;
+    }
+};
+
+// Issue the copies of the next slab.  Returns false when there is none left or
+// the wait for the stage to be released expired (abort).
+template <class Cfg>
+__device__ __forceinline__ bool issue_one(IssueState &st, const Ring &ring,
+                                          const CUtensorMap *tmA, const CUtensorMap *tmB,
+                                          const MainParams &p, int k_tiles) {
+    if (*ring.abort_flag) return false;
+    if (!st.have) {
+        Segment sg;
+        if (!st.iter.next(p, k_tiles, sg)) return false;
+        st.seg = sg;
+        st.have = 1;
+        st.slab = sg.kb;
+        int tm, tn;
+        tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        st.tm = tm;
+        st.tn = tn;
+    }
+    const int s = st.stage;
+    // first use of a stage: parity 1 refers to the phase before the barrier's
+    // first one and counts as complete
+    if (!mbar_wait(&ring.empty[s], st.phase ^ 1u, p.timeout_ns)) {
+        atomicOr(&g_error_word, ERR_EMPTY_WAIT);
+        *ring.abort_flag = 1;
+        return false;
+    }
+    mbar_arrive_expect_tx(&ring.full[s], Cfg::STAGE_BYTES);
+    tma_load_2d(ring.sA + s * Cfg::A_STAGE, tmA, &ring.full[s], st.tm * Cfg::BM, st.slab * Cfg::BK);
+    tma_load_2d(ring.sB + s * Cfg::B_STAGE, tmB, &ring.full[s], st.tn * Cfg::BN, st.slab * Cfg::BK);
+    st.issued = st.issued + 1;
+    if (s + 1 == Cfg::STAGES) {
+        st.stage = 0;
+        st.phase ^= 1u;
+    } else {
+        st.stage = s + 1;
+    }
+    if (++st.slab == st.seg.ke) st.have = 0;
+    return true;
+}
+
+// After an abort: wait (bounded) for the last copies issued, so none is still
+// writing shared memory when the CTA exits.
+template <class Cfg>
+__device__ __forceinline__ void drain_copies(const Ring &ring, long long issued, const MainParams &p) {
+    const long long first = issued > Cfg::STAGES ? issued - Cfg::STAGES : 0;
+    for (long long q = first; q < issued; ++q) {
+        const int s = int(q % Cfg::STAGES);
+        if (!mbar_wait(&ring.full[s], uint32_t((q / Cfg::STAGES) & 1), p.timeout_ns)) {
+            atomicOr(&g_error_word, ERR_DRAIN_WAIT);
+            break;
+        }
+    }
+}
+
+// Stream-K fixup data of the current segment, written by consumer thread 0
+// at the segment's start (where the integer divisions cost no accumulator
+// registers) and read by all consumers after the segment's main loop.
+struct FixInfo {
+    long long tile_start;   // first slab of the tile in the stream-K range
+    long long q0;           // sk_start(b_lo)
+    int r0;                 // (b_lo * sk_slabs) mod gridDim.x
+    int b_lo, b_hi;         // CTAs holding pieces of the tile
+    int pieces;             // CTAs among them with a non-empty range
+    int last;               // this CTA's piece completed the tile
+};
+
+// The consumer warps: FFMA micro-tiles over the ring, stream-K fixup and the
+// epilogue.  `before_slab` runs at the start of every slab (the issuer hook of
+// the non-warp-specialised kernel).
+template <class Cfg, class Hook>
+__device__ __forceinline__ void consumer_loop(const Ring &ring, const MainParams &p, int k_tiles,
+                                              int cw, int ctid, FixInfo &fix, Hook &&before_slab) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int TM = Cfg::TM, TN = Cfg::TN;
-
-    extern __shared__ unsigned char smem_raw[];
-    const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
-    float *sA = reinterpret_cast<float *>(base);
-    float *sB = sA + STAGES * Cfg::A_STAGE;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * Cfg::B_STAGE);
-    uint64_t *empty = full + STAGES;
-
-    const int warp = threadIdx.x >> 5;
+    constexpr int BAR_CONSUMERS = 1;
     const int lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], Cfg::CONSUMER_WARPS);
-        }
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    const int num_tiles = p.tiles_m * p.tiles_n;
-    const int k_tiles = (p.K + BK - 1) / BK;
-    const int my_tiles = blockIdx.x < num_tiles ? (num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-    const long long total_slabs = (long long)my_tiles * k_tiles;
-
-    // Issue state, used by thread 0 only: the next slab to copy is k-slab
-    // `pkt` of this CTA's tile number `pj`, into stage `pstage` whose empty
-    // barrier is in phase parity `pphase`.
-    long long issued = 0;
-    int pj = 0, pkt = 0, pstage = 0, ptm = 0, ptn = 0;
-    uint32_t pphase = 0;
-    bool aborted = false;
-    if (threadIdx.x == 0 && my_tiles > 0) tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, ptm, ptn);
-
-    // Thread 0: issue the copies of the next slab.  Returns false if the wait
-    // for its stage to be released expired.
-    auto issue_next = [&]() -> bool {
-        // first use of a stage: parity 1 refers to the phase before the
-        // barrier's first one and counts as complete
-        if (!mbar_wait(&empty[pstage], pphase ^ 1u, p.timeout_ns)) {
-            atomicOr(&g_error_word, ERR_EMPTY_WAIT);
-            return false;
-        }
-        mbar_arrive_expect_tx(&full[pstage], Cfg::STAGE_BYTES);
-        tma_load_2d(sA + pstage * Cfg::A_STAGE, &tmA, &full[pstage], ptm * BM, pkt * BK);
-        tma_load_2d(sB + pstage * Cfg::B_STAGE, &tmB, &full[pstage], ptn * BN, pkt * BK);
-        ++issued;
-        if (++pstage == STAGES) {
-            pstage = 0;
-            pphase ^= 1u;
-        }
-        if (++pkt == k_tiles) {
-            pkt = 0;
-            ++pj;
-            if (pj < my_tiles)
-                tile_coords(blockIdx.x + pj * gridDim.x, p.tiles_m, p.tiles_n, p.group_m, ptm, ptn);
-        }
-        return true;
-    };
-
-    if (threadIdx.x == 0) {
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
-        while (issued < STAGES - 1 && issued < total_slabs)
-            if (!issue_next()) {
-                aborted = true;
-                break;
-            }
-    }
-
-    const int wm0 = (warp % Cfg::WARPS_M) * Cfg::WM;
-    const int wn0 = (warp / Cfg::WARPS_M) * Cfg::WN;
+    const int wm0 = (cw % Cfg::WARPS_M) * Cfg::WM;
+    const int wn0 = (cw / Cfg::WARPS_M) * Cfg::WN;
     // zig-zag lane map: lane bits {1,4} -> row group, bits {0,2,3} -> column group
     const int lm = ((lane >> 1) & 1) | ((lane >> 3) & 2);
     const int ln = (lane & 1) | ((lane >> 1) & 6);
     const int a_off = wm0 + lm * 4;
     const int b_off = wn0 + ln * 4;
+    // sk_start(b + 1) = sk_start(b) + sk_q + carry, carry from sk_r: additions only
+    const long long sk_q = p.sk_slabs / gridDim.x;
+    const int sk_r = int(p.sk_slabs % gridDim.x);
+    const uint32_t sA_addr = smem_addr(ring.sA), sB_addr = smem_addr(ring.sB);
 
     int stage = 0;          // stage of the next slab to consume
     uint32_t phase = 0;     // parity of that stage's full barrier
-    for (int j = 0; j < my_tiles; ++j) {
+    for (int si = 0;; ++si) {
+        Segment seg;
+        if (!segment_at(p, k_tiles, si, seg)) break;
         int tm, tn;
-        tile_coords(blockIdx.x + j * gridDim.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        if (seg.slot >= 0 && ctid == 0) {
+            const long long rel = seg.tile - p.dp_tiles;
+            fix.tile_start = rel * k_tiles;
+            fix.b_lo = sk_owner(fix.tile_start, p.sk_slabs, gridDim.x);
+            fix.b_hi = sk_owner(fix.tile_start + k_tiles - 1, p.sk_slabs, gridDim.x);
+            fix.q0 = sk_start(fix.b_lo, p.sk_slabs, gridDim.x);
+            fix.r0 = int(((long long)fix.b_lo * p.sk_slabs) % gridDim.x);
+            int pieces = 0;
+            for (int b = fix.b_lo; b <= fix.b_hi; ++b)
+                pieces += sk_start(b, p.sk_slabs, gridDim.x) < sk_start(b + 1, p.sk_slabs, gridDim.x);
+            fix.pieces = pieces;
+        }
 
         float acc[TM][TN];
 #pragma unroll
@@ -262,18 +550,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
             for (int jj = 0; jj < TN; ++jj) acc[i][jj] = 0.0f;
 
-        for (int kt = 0; kt < k_tiles; ++kt) {
-            if (threadIdx.x == 0 && !aborted && issued < total_slabs) aborted = !issue_next();
+        const int slot = seg.slot;
+        const int rel_tile = seg.tile - p.dp_tiles;
+        for (int n = seg.ke - seg.kb; n > 0; --n) {
+            before_slab();
             const int s = stage;
-            bool ok = !aborted && mbar_wait(&full[s], phase, p.timeout_ns);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
-                if (lane == 0) atomicOr(&g_error_word, ERR_FULL_WAIT);
-                aborted = true;
-                goto done;
+            // warp-uniform view of the abort flag, so the vote below is reached
+            // by all lanes or by none
+            if (!__any_sync(0xffffffffu, *ring.abort_flag)) {
+                bool ok = mbar_wait(&ring.full[s], phase, p.timeout_ns);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    if (lane == 0) atomicOr(&g_error_word, ERR_FULL_WAIT);
+                    *ring.abort_flag = 1;
+                }
             }
-            const float *a_s = sA + s * Cfg::A_STAGE + a_off;
-            const float *b_s = sB + s * Cfg::B_STAGE + b_off;
+            const uint32_t a_s = sA_addr + uint32_t(s * Cfg::A_STAGE + a_off) * 4u;
+            const uint32_t b_s = sB_addr + uint32_t(s * Cfg::B_STAGE + b_off) * 4u;
             // register double buffering of the fragments: the loads for k+1
             // are issued before the FMAs of k
             float fa[2][TM], fb[2][TN];
@@ -281,87 +574,157 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < BK; ++kk) {
                 if (kk + 1 < BK)
-                    load_fragments<Cfg>(a_s + (kk + 1) * BM, b_s + (kk + 1) * BN,
+                    load_fragments<Cfg>(a_s + (kk + 1) * BM * 4, b_s + (kk + 1) * BN * 4,
                                         fa[(kk + 1) & 1], fb[(kk + 1) & 1]);
                 outer_product<Cfg>(acc, fa[kk & 1], fb[kk & 1]);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
+            if (lane == 0) mbar_arrive(&ring.empty[s]);
             if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
 
-        // -------------------------------------------------------------- epilogue
-        {
-            const int row0 = tm * BM + a_off;
-            const int col0 = tn * BN + b_off;
-            const float alpha = p.alpha, beta = p.beta;
+        bool finish = true;
+        if (slot >= 0) {
+            // ---- stream-K piece: publish the partial sums; the piece that
+            // completes the tile's count adds all pieces in k order
+            write_partial<Cfg>(acc, p.partials + (size_t)slot * (BM * BN), ctid);
+            __threadfence();
+            named_barrier(BAR_CONSUMERS, Cfg::CONSUMER_THREADS);
+            if (ctid == 0) {
+                const int before = atomicAdd(&p.counters[rel_tile], 1);
+                fix.last = (before == fix.pieces - 1);
+            }
+            named_barrier(BAR_CONSUMERS, Cfg::CONSUMER_THREADS);
+            finish = fix.last;
+            const long long tile_start = fix.tile_start, q0 = fix.q0;
+            const int r0 = fix.r0, b_lo = fix.b_lo, b_hi = fix.b_hi;
+            // everyone has read `fix` before thread 0 can write it again
+            named_barrier(BAR_CONSUMERS, Cfg::CONSUMER_THREADS);
+            if (finish) {
+                __threadfence();
+                // this CTA's own piece is read back too, so the sum order is the
+                // k order whichever piece arrived last
 #pragma unroll
-            for (int s4 = 0; s4 < TM / 4; ++s4) {
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int row = row0 + s4 * 16 + r;
-                    if (row >= p.M) continue;
-                    float *crow = p.C + (long long)row * p.ldc;
-#pragma unroll
-                    for (int t = 0; t < TN / 4; ++t) {
-                        const int col = col0 + t * 32;
-                        const float *v = &acc[4 * s4 + r][4 * t];
-                        if (p.c_vec4 && col + 3 < p.N) {
-                            float4 o;
-                            if (beta != 0.0f) {
-                                const float4 c = __ldcs(reinterpret_cast<const float4 *>(crow + col));
-                                o.x = fmaf(alpha, v[0], beta * c.x);
-                                o.y = fmaf(alpha, v[1], beta * c.y);
-                                o.z = fmaf(alpha, v[2], beta * c.z);
-                                o.w = fmaf(alpha, v[3], beta * c.w);
-                            } else {
-                                o.x = alpha * v[0];
-                                o.y = alpha * v[1];
-                                o.z = alpha * v[2];
-                                o.w = alpha * v[3];
-                            }
-                            __stcs(reinterpret_cast<float4 *>(crow + col), o);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                if (col + e < p.N) {
-                                    const float c = (beta != 0.0f) ? beta * crow[col + e] : 0.0f;
-                                    crow[col + e] = (beta != 0.0f) ? fmaf(alpha, v[e], c)
-                                                                   : alpha * v[e];
-                                }
-                            }
-                        }
-                    }
+                for (int i = 0; i < TM; ++i)
+                    sum_pieces_row<Cfg>(acc[i], p.partials, i, ctid, b_lo, b_hi, q0, r0, sk_q, sk_r,
+                                        tile_start);
+            }
+        }
+        if (finish && !*ring.abort_flag) store_tile<Cfg>(acc, p, tm, tn, a_off, b_off);
+    }
+}
+
+// Persistent kernel.  Each CTA walks its segments (SegmentIter); the k-slabs of
+// all its segments form one sequence q = 0, 1, 2, ...; slab q lives in ring
+// stage q % STAGES.  The issuer copies a slab into a stage once every consumer
+// warp has released the stage's previous contents (empty barrier); consumer
+// warps wait on the full barrier of a stage (TMA byte count) before reading it.
+//
+// WS (warp-specialised): warpgroup 0 is the producer; it gives back registers
+// (setmaxnreg.dec) and one of its threads issues all copies, STAGES ahead.  The
+// 8 consumer warps take the registers (setmaxnreg.inc).  Otherwise the CTA is
+// the 8 consumer warps alone (two per SM sub-partition, up to 255 registers a
+// thread) and consumer thread 0 issues slab q + STAGES - 1 when starting slab q.
+//
+// A stream-K piece that is not a whole tile writes its partial sums to its
+// slot and increments the tile's counter; the piece that brings the counter to
+// the tile's piece count adds all pieces' slots in k order (so the result does
+// not depend on which piece finishes last) and runs the epilogue.  No CTA ever
+// waits for another.
+//
+// Expiry of a bounded wait sets a CTA-wide abort flag: from then on no thread
+// waits again and nothing more is written to C; every consumer still passes
+// the consumer barriers, and at the end the issuing thread waits (bounded) for
+// the copies it issued.
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
+    sgemm_tma_ffma_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB, const MainParams p) {
+    constexpr int STAGES = Cfg::STAGES;
+    constexpr int BAR_END = 2;
+
+    extern __shared__ unsigned char smem_raw[];
+    const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
+    Ring ring;
+    ring.sA = reinterpret_cast<float *>(base);
+    ring.sB = ring.sA + STAGES * Cfg::A_STAGE;
+    ring.full = reinterpret_cast<uint64_t *>(ring.sB + STAGES * Cfg::B_STAGE);
+    ring.empty = ring.full + STAGES;
+    ring.abort_flag = reinterpret_cast<volatile int *>(ring.empty + STAGES);
+    __shared__ FixInfo fix;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&ring.full[s], 1);
+            mbar_init(&ring.empty[s], Cfg::CONSUMER_WARPS);
+        }
+        *ring.abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int k_tiles = (p.K + Cfg::BK - 1) / Cfg::BK;
+
+    if constexpr (Cfg::WS) {
+        if (warp < Cfg::PRODUCER_THREADS / 32) {
+            // ======================================================== producer
+            regs_decrease<Cfg::PRODUCER_REGS>();
+            if (warp != 0) return;
+            IssueState st;
+            st.init(p);
+            if (lane == 0) {
+                tma_prefetch_desc(&tmA);
+                tma_prefetch_desc(&tmB);
+                while (issue_one<Cfg>(st, ring, &tmA, &tmB, p, k_tiles)) {
                 }
             }
+            __syncwarp();
+            // wait until every consumer is done, then (after an abort) make
+            // sure no copy is still writing shared memory when the CTA exits
+            named_barrier(BAR_END, 32 + Cfg::CONSUMER_THREADS);
+            if (lane == 0 && *ring.abort_flag) drain_copies<Cfg>(ring, st.issued, p);
+            return;
         }
-    }
-done:
-    // After an abort, thread 0 waits (bounded) for the copies it issued and no
-    // warp consumed, so no copy is still writing when the CTA exits.
-    if (threadIdx.x == 0 && aborted) {
-        const long long first = issued > STAGES ? issued - STAGES : 0;
-        for (long long qq = first; qq < issued; ++qq) {
-            const int s = int(qq % STAGES);
-            if (!mbar_wait(&full[s], uint32_t((qq / STAGES) & 1), p.timeout_ns)) {
-                atomicOr(&g_error_word, ERR_DRAIN_WAIT);
-                break;
-            }
+        // ============================================================ consumers
+        regs_increase<Cfg::CONSUMER_REGS>();
+        consumer_loop<Cfg>(ring, p, k_tiles, warp - Cfg::PRODUCER_THREADS / 32,
+                           threadIdx.x - Cfg::PRODUCER_THREADS, fix, [] {});
+        named_barrier(BAR_END, 32 + Cfg::CONSUMER_THREADS);
+    } else {
+        // issue state in shared memory: only thread 0 touches it, and keeping
+        // it out of registers leaves them to the accumulators
+        __shared__ IssueState ist;
+        if (threadIdx.x == 0) {
+            ist.init(p);
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            for (int i = 0; i < STAGES - 1; ++i) issue_one<Cfg>(ist, ring, &tmA, &tmB, p, k_tiles);
         }
+        consumer_loop<Cfg>(ring, p, k_tiles, warp, threadIdx.x, fix, [&] {
+            if (threadIdx.x == 0) issue_one<Cfg>(ist, ring, &tmA, &tmB, p, k_tiles);
+        });
+        if (threadIdx.x == 0 && *ring.abort_flag) drain_copies<Cfg>(ring, ist.issued, p);
     }
 }
 
 // ------------------------------------------------------------------ pre-pass
 // At[k][m] = A[m][k].  32x32 tiles through shared memory: coalesced reads along
 // k, coalesced writes along m.
+// Block (0,0) also zeroes `zero_count` ints at `zero` (the stream-K tile
+// counters of the GEMM that follows on the same stream).
 __global__ void __launch_bounds__(256)
     pack_a_transpose_kernel(const float *__restrict__ A, long long lda, int M, int K,
-                            float *__restrict__ At, long long ldat) {
+                            float *__restrict__ At, long long ldat, int *zero, int zero_count) {
     __shared__ float tile[32][33];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        for (int i = threadIdx.x; i < zero_count; i += blockDim.x) zero[i] = 0;
     for (long long m0 = (long long)blockIdx.y * 32; m0 < M; m0 += (long long)gridDim.y * 32) {
         for (long long k0 = (long long)blockIdx.x * 32; k0 < K; k0 += (long long)gridDim.x * 32) {
 #pragma unroll

@@ -40,6 +40,7 @@ thread_local int t_last_cuda_error = 0;
 struct Variant {
     const char *name;
     int bm, bn, bk;
+    bool stream_k;
     cudaError_t (*set_attr)();
     void (*launch)(int grid, cudaStream_t s, const CUtensorMap &a, const CUtensorMap &b,
                    const sg::MainParams &p);
@@ -58,23 +59,27 @@ void launch_t(int grid, cudaStream_t s, const CUtensorMap &a, const CUtensorMap 
 }
 
 template <class Cfg>
-constexpr Variant make_variant(const char *name) {
-    return Variant{name, Cfg::BM, Cfg::BN, Cfg::BK, &set_attr_t<Cfg>, &launch_t<Cfg>};
+constexpr Variant make_variant(const char *name, bool stream_k) {
+    return Variant{name, Cfg::BM, Cfg::BN, Cfg::BK, stream_k, &set_attr_t<Cfg>, &launch_t<Cfg>};
 }
 
 using sg::MICRO_FFMA;
 using sg::MICRO_FFMA2;
 const Variant kVariants[] = {
-    make_variant<sg::TileConfig<256, 128, 16, 6, 4, 2, 16, 8, MICRO_FFMA2>>(
-        "ffma2 tile=256x128x16 stages=6 warps=4x2 thread=16x8"),
-    make_variant<sg::TileConfig<256, 128, 16, 6, 4, 2, 16, 8, MICRO_FFMA>>(
-        "ffma tile=256x128x16 stages=6 warps=4x2 thread=16x8"),
-    make_variant<sg::TileConfig<128, 256, 16, 6, 2, 4, 16, 8, MICRO_FFMA2>>(
-        "ffma2 tile=128x256x16 stages=6 warps=2x4 thread=16x8"),
-    make_variant<sg::TileConfig<256, 128, 32, 4, 4, 2, 16, 8, MICRO_FFMA2>>(
-        "ffma2 tile=256x128x32 stages=4 warps=4x2 thread=16x8"),
-    make_variant<sg::TileConfig<128, 128, 16, 6, 4, 2, 8, 8, MICRO_FFMA2>>(
-        "ffma2 tile=128x128x16 stages=6 warps=4x2 thread=8x8"),
+    make_variant<sg::TileConfig<256, 128, 32, 4, 4, 2, 16, 8, MICRO_FFMA2, true>>(
+        "ffma2 tile=256x128x32 stages=4 warps=8+producer_wg thread=16x8 stream_k", true),
+    make_variant<sg::TileConfig<128, 256, 32, 4, 2, 4, 16, 8, MICRO_FFMA2, true>>(
+        "ffma2 tile=128x256x32 stages=4 warps=8+producer_wg thread=16x8 stream_k", true),
+    make_variant<sg::TileConfig<256, 128, 16, 6, 4, 2, 16, 8, MICRO_FFMA2, true>>(
+        "ffma2 tile=256x128x16 stages=6 warps=8+producer_wg thread=16x8 stream_k", true),
+    make_variant<sg::TileConfig<256, 128, 32, 4, 4, 2, 16, 8, MICRO_FFMA2, false>>(
+        "ffma2 tile=256x128x32 stages=4 warps=8 issuer=thread0 thread=16x8 stream_k", true),
+    make_variant<sg::TileConfig<256, 128, 32, 4, 4, 2, 16, 8, MICRO_FFMA2, true>>(
+        "ffma2 tile=256x128x32 stages=4 warps=8+producer_wg thread=16x8 no_stream_k", false),
+    make_variant<sg::TileConfig<256, 128, 32, 4, 4, 2, 16, 8, MICRO_FFMA, true>>(
+        "ffma tile=256x128x32 stages=4 warps=8+producer_wg thread=16x8 stream_k", true),
+    make_variant<sg::TileConfig<128, 128, 32, 4, 4, 2, 8, 8, MICRO_FFMA2, true>>(
+        "ffma2 tile=128x128x32 stages=4 warps=8+producer_wg thread=8x8 stream_k", true),
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 std::atomic<int> g_forced_variant{-1};
@@ -249,27 +254,43 @@ int sgemm_device(int M, int N, int K, float alpha, const float *A, int lda, cons
     if (K == 0 || alpha == 0.0f) return launch_scale(stream, C, ldc, M, N, beta, dev->sm_count);
 
     const Variant &var = kVariants[pick_variant(M, N, K)];
-    // ---- workspace: transposed A, and a re-pitched B if needed
+    // ---- work split: whole-tile waves, then the leftover tiles' k-slabs spread
+    // evenly over all CTAs (stream-K) so the last wave is not partly idle
+    const long long tiles_m = (M + var.bm - 1) / var.bm, tiles_n = (N + var.bn - 1) / var.bn;
+    const long long tiles = tiles_m * tiles_n;
+    const long long k_tiles = (K + var.bk - 1) / var.bk;
+    const int grid = var.stream_k ? int(std::min<long long>(dev->sm_count, tiles * k_tiles))
+                                  : int(std::min<long long>(dev->sm_count, tiles));
+    const long long dp_tiles = var.stream_k ? (tiles / grid) * grid : tiles;
+    const long long sk_tiles = tiles - dp_tiles;
+    const long long sk_slabs = sk_tiles * k_tiles;
+
+    // ---- workspace: transposed A, a re-pitched B if needed, stream-K partial
+    // sums and tile counters
     const long long ldat = round_up(M, 4);
     const bool b_direct = aligned16(B) && (ldb % 4 == 0);
     const long long ldbp = b_direct ? ldb : round_up(N, 4);
-    const size_t at_bytes = size_t(K) * size_t(ldat) * sizeof(float);
-    const size_t bp_bytes = b_direct ? 0 : size_t(K) * size_t(ldbp) * sizeof(float);
-    const size_t ws_bytes = round_up((long long)at_bytes, 256) + bp_bytes;
+    const size_t at_bytes = round_up((long long)K * ldat * 4, 256);
+    const size_t bp_bytes = b_direct ? 0 : round_up((long long)K * ldbp * 4, 256);
+    const size_t part_bytes = sk_slabs ? size_t(2) * grid * var.bm * var.bn * 4 : 0;
+    const size_t cnt_bytes = size_t(sk_tiles) * 4;
+    const size_t ws_bytes = at_bytes + bp_bytes + part_bytes + cnt_bytes;
 
     void *ws = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&ws, ws_bytes, dev->pool, stream);
     if (e != cudaSuccess) return cuda_fail(e);
-    float *At = static_cast<float *>(ws);
-    float *Bp = b_direct ? const_cast<float *>(B)
-                         : reinterpret_cast<float *>(static_cast<char *>(ws) +
-                                                     round_up((long long)at_bytes, 256));
+    char *wsb = static_cast<char *>(ws);
+    float *At = reinterpret_cast<float *>(wsb);
+    float *Bp = b_direct ? const_cast<float *>(B) : reinterpret_cast<float *>(wsb + at_bytes);
+    float *partials = sk_slabs ? reinterpret_cast<float *>(wsb + at_bytes + bp_bytes) : nullptr;
+    int *counters = sk_slabs ? reinterpret_cast<int *>(wsb + at_bytes + bp_bytes + part_bytes) : nullptr;
 
     {
         ProfScope prof(stream, false);
-        dim3 grid(unsigned(std::min<long long>((K + 31) / 32, 1LL << 20)),
-                  unsigned(std::min<long long>((M + 31) / 32, 65535)));
-        sg::pack_a_transpose_kernel<<<grid, 256, 0, stream>>>(A, lda, M, K, At, ldat);
+        dim3 pgrid(unsigned(std::min<long long>((K + 31) / 32, 1LL << 20)),
+                   unsigned(std::min<long long>((M + 31) / 32, 65535)));
+        sg::pack_a_transpose_kernel<<<pgrid, 256, 0, stream>>>(A, lda, M, K, At, ldat, counters,
+                                                               int(sk_tiles));
         g_launches.fetch_add(1);
         if (!b_direct) {
             const long long total = (long long)K * N;
@@ -299,13 +320,15 @@ int sgemm_device(int M, int N, int K, float alpha, const float *A, int lda, cons
     p.K = K;
     p.alpha = alpha;
     p.beta = beta;
-    p.tiles_m = int((M + var.bm - 1) / var.bm);
-    p.tiles_n = int((N + var.bn - 1) / var.bn);
+    p.tiles_m = int(tiles_m);
+    p.tiles_n = int(tiles_n);
     p.group_m = 8;
     p.c_vec4 = (aligned16(C) && ldc % 4 == 0) ? 1 : 0;
     p.timeout_ns = g_timeout_ns.load();
-    const long long tiles = (long long)p.tiles_m * p.tiles_n;
-    const int grid = int(std::min<long long>(tiles, dev->sm_count));
+    p.dp_tiles = int(dp_tiles);
+    p.sk_slabs = sk_slabs;
+    p.partials = partials;
+    p.counters = counters;
     {
         ProfScope prof(stream, true);
         var.launch(grid, stream, tmA, tmB, p);
@@ -411,7 +434,7 @@ int sgemm_device_noalloc(int M, int N, int K, float alpha, const float *A, int l
 
     dim3 grid(unsigned(std::min<long long>((K + 31) / 32, 1LL << 20)),
               unsigned(std::min<long long>((M + 31) / 32, 65535)));
-    sg::pack_a_transpose_kernel<<<grid, 256, 0, stream>>>(A, lda, M, K, At, ldat);
+    sg::pack_a_transpose_kernel<<<grid, 256, 0, stream>>>(A, lda, M, K, At, ldat, nullptr, 0);
     g_launches.fetch_add(1);
     if (!b_direct) {
         const long long total = (long long)K * N;
@@ -442,6 +465,10 @@ int sgemm_device_noalloc(int M, int N, int K, float alpha, const float *A, int l
     p.timeout_ns = g_timeout_ns.load();
     const long long tiles = (long long)p.tiles_m * p.tiles_n;
     const int grid_main = int(std::min<long long>(tiles, dev->sm_count));
+    p.dp_tiles = int(tiles);     // whole tiles only: no partial-sum scratch needed
+    p.sk_slabs = 0;
+    p.partials = nullptr;
+    p.counters = nullptr;
     var.launch(grid_main, stream, tmA, tmB, p);
     g_launches.fetch_add(1);
     e = cudaGetLastError();

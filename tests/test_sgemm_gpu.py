@@ -230,3 +230,27 @@ def test_every_kernel_variant_matches_oracle(M, N, K):
             assert_within_bound(got, ref, bound, f"variant {v}")
     finally:
         binding.set_variant(-1)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (5120, 1152, 512),    # 180 tiles of 256x128: one whole-tile wave, 28 tiles split over all CTAs
+    (512, 256, 64),       # 4 tiles, 2 slabs each: every tile split in two pieces
+    (300, 4000, 16),      # one slab per tile: stream-K pieces are whole tiles, some CTAs idle
+    (2048, 2048, 1056),   # 128 tiles, 33 slabs: the whole problem is stream-K
+])
+def test_stream_k_split_matches_oracle(M, N, K):
+    """Shapes whose leftover tiles are split along k between CTAs: integer
+    inputs must stay bit-exact (any order of exact partial sums), random inputs
+    within the bound, and two runs must agree bitwise (the partial sums are
+    added in a fixed order whichever piece finishes last)."""
+    import torch
+    A, B, C = make_inputs(M, N, K, "int4", "int4", "int4", seed=M + K)
+    ref, _ = oracle.sgemm(A, B, C, 1.5, 0.5, with_bound=False)
+    got = run_gpu(A, B, C, 1.5, 0.5).cpu().numpy()
+    assert np.array_equal(got, ref)
+    A, B, C = make_inputs(M, N, K, "normal", "normal", "normal", seed=M + K + 1)
+    ref, bound = oracle.sgemm(A, B, C, 0.5, -1.5)
+    g1 = run_gpu(A, B, C, 0.5, -1.5).cpu()
+    g2 = run_gpu(A, B, C, 0.5, -1.5).cpu()
+    assert torch.equal(g1, g2)
+    assert_within_bound(g1.numpy(), ref, bound, f"stream-K {M}x{N}x{K}")
