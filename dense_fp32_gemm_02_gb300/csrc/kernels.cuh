@@ -92,7 +92,7 @@ struct TileConfig {
     static_assert(BM <= 256 && BN <= 256 && BK <= 256, "TMA box edge is at most 256");
     static_assert((A_STAGE * 4) % 1024 == 0 && (B_STAGE * 4) % 1024 == 0, "stage alignment");
     static_assert(SMEM_BYTES <= 232448, "at most 227 KB of shared memory per CTA");
-    static_assert(CONSUMER_WARPS == 8, "two consumer warpgroups");
+    static_assert(CONSUMER_WARPS % 4 == 0, "whole consumer warpgroups");
     static_assert(!WS || PRODUCER_REGS * PRODUCER_THREADS + CONSUMER_REGS * CONSUMER_THREADS <=
                              LAUNCH_REGS * THREADS,
                   "register split exceeds the launch allocation");
@@ -555,9 +555,11 @@ __device__ __forceinline__ void consumer_loop(const Ring &ring, const MainParams
         for (int n = seg.ke - seg.kb; n > 0; --n) {
             before_slab();
             const int s = stage;
-            // warp-uniform view of the abort flag, so the vote below is reached
-            // by all lanes or by none
-            if (!__any_sync(0xffffffffu, *ring.abort_flag)) {
+            // Fast path: one try_wait that finds the slab already copied.  Only
+            // if some lane misses it does the warp take a warp-uniform look at
+            // the abort flag and enter the bounded wait.
+            if (!__all_sync(0xffffffffu, mbar_try_wait(&ring.full[s], phase)) &&
+                !__any_sync(0xffffffffu, *ring.abort_flag)) {
                 bool ok = mbar_wait(&ring.full[s], phase, p.timeout_ns);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) {

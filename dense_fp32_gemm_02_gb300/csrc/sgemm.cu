@@ -41,6 +41,7 @@ struct Variant {
     const char *name;
     int bm, bn, bk;
     bool stream_k;
+    int group_m;
     cudaError_t (*set_attr)();
     void (*launch)(int grid, cudaStream_t s, const CUtensorMap &a, const CUtensorMap &b,
                    const sg::MainParams &p);
@@ -59,27 +60,36 @@ void launch_t(int grid, cudaStream_t s, const CUtensorMap &a, const CUtensorMap 
 }
 
 template <class Cfg>
-constexpr Variant make_variant(const char *name, bool stream_k) {
-    return Variant{name, Cfg::BM, Cfg::BN, Cfg::BK, stream_k, &set_attr_t<Cfg>, &launch_t<Cfg>};
+constexpr Variant make_variant(const char *name, bool stream_k, int group_m = 8) {
+    return Variant{name, Cfg::BM, Cfg::BN, Cfg::BK, stream_k, group_m, &set_attr_t<Cfg>,
+                   &launch_t<Cfg>};
 }
 
 using sg::MICRO_FFMA;
 using sg::MICRO_FFMA2;
+// Variant 0 is the default for every shape: it was the fastest or within 1%
+// of the fastest on every measured workload.  The others stay for sweeps and
+// as evidence for the design choices (stream-K, warp specialisation, packed
+// FP32x2 FMA, thread-tile size).
 const Variant kVariants[] = {
+    make_variant<sg::TileConfig<128, 192, 64, 2, 4, 3, 8, 8, MICRO_FFMA2, true>>(
+        "ffma2 tile=128x192x64 stages=2 warps=12+producer_wg thread=8x8 stream_k", true),
+    make_variant<sg::TileConfig<192, 128, 64, 2, 6, 2, 8, 8, MICRO_FFMA2, true>>(
+        "ffma2 tile=192x128x64 stages=2 warps=12+producer_wg thread=8x8 stream_k", true),
+    make_variant<sg::TileConfig<128, 128, 48, 4, 4, 2, 8, 8, MICRO_FFMA2, true>>(
+        "ffma2 tile=128x128x48 stages=4 warps=8+producer_wg thread=8x8 stream_k", true),
+    make_variant<sg::TileConfig<128, 128, 64, 3, 4, 2, 8, 8, MICRO_FFMA2, true>>(
+        "ffma2 tile=128x128x64 stages=3 warps=8+producer_wg thread=8x8 stream_k", true),
     make_variant<sg::TileConfig<256, 128, 32, 4, 4, 2, 16, 8, MICRO_FFMA2, true>>(
         "ffma2 tile=256x128x32 stages=4 warps=8+producer_wg thread=16x8 stream_k", true),
-    make_variant<sg::TileConfig<128, 256, 32, 4, 2, 4, 16, 8, MICRO_FFMA2, true>>(
-        "ffma2 tile=128x256x32 stages=4 warps=8+producer_wg thread=16x8 stream_k", true),
-    make_variant<sg::TileConfig<256, 128, 16, 6, 4, 2, 16, 8, MICRO_FFMA2, true>>(
-        "ffma2 tile=256x128x16 stages=6 warps=8+producer_wg thread=16x8 stream_k", true),
+    make_variant<sg::TileConfig<128, 192, 64, 2, 4, 3, 8, 8, MICRO_FFMA2, true>>(
+        "ffma2 tile=128x192x64 stages=2 warps=12+producer_wg thread=8x8 no_stream_k", false),
+    make_variant<sg::TileConfig<128, 192, 64, 2, 4, 3, 8, 8, MICRO_FFMA2, false>>(
+        "ffma2 tile=128x192x64 stages=2 warps=12 issuer=thread0 thread=8x8 stream_k", true),
+    make_variant<sg::TileConfig<128, 128, 48, 4, 4, 2, 8, 8, MICRO_FFMA, true>>(
+        "ffma tile=128x128x48 stages=4 warps=8+producer_wg thread=8x8 stream_k", true),
     make_variant<sg::TileConfig<256, 128, 32, 4, 4, 2, 16, 8, MICRO_FFMA2, false>>(
-        "ffma2 tile=256x128x32 stages=4 warps=8 issuer=thread0 thread=16x8 stream_k", true),
-    make_variant<sg::TileConfig<256, 128, 32, 4, 4, 2, 16, 8, MICRO_FFMA2, true>>(
-        "ffma2 tile=256x128x32 stages=4 warps=8+producer_wg thread=16x8 no_stream_k", false),
-    make_variant<sg::TileConfig<256, 128, 32, 4, 4, 2, 16, 8, MICRO_FFMA, true>>(
-        "ffma tile=256x128x32 stages=4 warps=8+producer_wg thread=16x8 stream_k", true),
-    make_variant<sg::TileConfig<128, 128, 32, 4, 4, 2, 8, 8, MICRO_FFMA2, true>>(
-        "ffma2 tile=128x128x32 stages=4 warps=8+producer_wg thread=8x8 stream_k", true),
+        "ffma2 tile=256x128x32 stages=4 warps=8 issuer=thread0 thread=16x8 no_stream_k", false),
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 std::atomic<int> g_forced_variant{-1};
@@ -322,7 +332,7 @@ int sgemm_device(int M, int N, int K, float alpha, const float *A, int lda, cons
     p.beta = beta;
     p.tiles_m = int(tiles_m);
     p.tiles_n = int(tiles_n);
-    p.group_m = 8;
+    p.group_m = var.group_m;
     p.c_vec4 = (aligned16(C) && ldc % 4 == 0) ? 1 : 0;
     p.timeout_ns = g_timeout_ns.load();
     p.dp_tiles = int(dp_tiles);
