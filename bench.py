@@ -202,7 +202,8 @@ def run_reference(args):
     w = WORKLOADS[args.workload or BENCH_WORKLOAD]
     A, B, C = workload_inputs(w)
     import oracle
-    rows_per_step = 8
+    # enough full rows per step for every host core to get two
+    rows_per_step = max(16, 2 * host_cores())
     c_in = C if w.beta != 0 else None
 
     def step(i):

