@@ -86,6 +86,12 @@ def max_over_ranks(world, value, device=None):
     return float(t.item())
 
 
+def aggregate_gflops(flops_per_step, ms_per_step_max, world):
+    """Whole-job rate: every rank runs the full workload (replicas), the step
+    time is the slowest rank's, so the job does world x flops per step."""
+    return flops_per_step / (ms_per_step_max * 1e-3) / 1e9 * world
+
+
 # ---------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples every 100 ms; only samples inside [t0, t1] are kept."""
@@ -324,7 +330,7 @@ def run_ours(args):
         raise RuntimeError("device error word set during the timed region")
 
     ms_per_step = ms / args.steps
-    gflops = w.flops / (ms_per_step * 1e-3) / 1e9 * world
+    gflops = aggregate_gflops(w.flops, ms_per_step, world)
 
     # ---- end to end through the host-buffer entry point
     e2e = None

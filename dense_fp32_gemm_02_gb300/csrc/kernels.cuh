@@ -715,29 +715,42 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 }
 
 // ------------------------------------------------------------------ pre-pass
-// At[k][m] = A[m][k].  32x32 tiles through shared memory: coalesced reads along
-// k, coalesced writes along m.
-// Block (0,0) also zeroes `zero_count` ints at `zero` (the stream-K tile
-// counters of the GEMM that follows on the same stream).
+// At[k][m] = A[m][k].  64x64 tiles through shared memory, 256 threads: each
+// thread has 16 independent loads in flight (coalesced along k) and then 16
+// stores (coalesced along m).  Block (0,0) also zeroes `zero_count` ints at
+// `zero` (the stream-K tile counters of the GEMM that follows on the stream).
 __global__ void __launch_bounds__(256)
     pack_a_transpose_kernel(const float *__restrict__ A, long long lda, int M, int K,
                             float *__restrict__ At, long long ldat, int *zero, int zero_count) {
-    __shared__ float tile[32][33];
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
+    __shared__ float tile[64][65];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;   // 8 warps
     if (blockIdx.x == 0 && blockIdx.y == 0)
         for (int i = threadIdx.x; i < zero_count; i += blockDim.x) zero[i] = 0;
-    for (long long m0 = (long long)blockIdx.y * 32; m0 < M; m0 += (long long)gridDim.y * 32) {
-        for (long long k0 = (long long)blockIdx.x * 32; k0 < K; k0 += (long long)gridDim.x * 32) {
+    for (long long m0 = (long long)blockIdx.y * 64; m0 < M; m0 += (long long)gridDim.y * 64) {
+        for (long long k0 = (long long)blockIdx.x * 64; k0 < K; k0 += (long long)gridDim.x * 64) {
+            float v[16];
 #pragma unroll
-            for (int r = ty; r < 32; r += 8) {
-                const long long m = m0 + r, k = k0 + tx;
-                tile[r][tx] = (m < M && k < K) ? __ldcs(A + m * lda + k) : 0.0f;
+            for (int r = 0; r < 8; ++r) {
+                const long long m = m0 + w * 8 + r;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const long long k = k0 + lane + 32 * h;
+                    v[2 * r + h] = (m < M && k < K) ? __ldcs(A + m * lda + k) : 0.0f;
+                }
             }
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) tile[w * 8 + r][lane + 32 * h] = v[2 * r + h];
             __syncthreads();
 #pragma unroll
-            for (int r = ty; r < 32; r += 8) {
-                const long long k = k0 + r, m = m0 + tx;
-                if (k < K && m < M) At[k * ldat + m] = tile[tx][r];
+            for (int r = 0; r < 8; ++r) {
+                const long long k = k0 + w * 8 + r;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const long long m = m0 + lane + 32 * h;
+                    if (k < K && m < M) At[k * ldat + m] = tile[lane + 32 * h][w * 8 + r];
+                }
             }
             __syncthreads();
         }
@@ -745,14 +758,16 @@ __global__ void __launch_bounds__(256)
 }
 
 // Bp[k][n] = B[k][n] with a 16-byte row pitch (ldbp % 4 == 0) for the TMA.
+// One block row per k (grid-stride), threads along n.
 __global__ void __launch_bounds__(256)
     pack_b_copy_kernel(const float *__restrict__ B, long long ldb, int K, int N,
                        float *__restrict__ Bp, long long ldbp) {
-    const long long total = (long long)K * N;
-    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (long long)gridDim.x * blockDim.x) {
-        const long long k = idx / N, n = idx - k * N;
-        Bp[k * ldbp + n] = B[k * ldb + n];
+    for (long long k = blockIdx.y; k < K; k += gridDim.y) {
+        const float *src = B + k * ldb;
+        float *dst = Bp + k * ldbp;
+        for (long long n = (long long)blockIdx.x * blockDim.x + threadIdx.x; n < N;
+             n += (long long)gridDim.x * blockDim.x)
+            dst[n] = __ldcs(src + n);
     }
 }
 

@@ -297,15 +297,15 @@ int sgemm_device(int M, int N, int K, float alpha, const float *A, int lda, cons
 
     {
         ProfScope prof(stream, false);
-        dim3 pgrid(unsigned(std::min<long long>((K + 31) / 32, 1LL << 20)),
-                   unsigned(std::min<long long>((M + 31) / 32, 65535)));
+        dim3 pgrid(unsigned(std::min<long long>((K + 63) / 64, 1LL << 20)),
+                   unsigned(std::min<long long>((M + 63) / 64, 65535)));
         sg::pack_a_transpose_kernel<<<pgrid, 256, 0, stream>>>(A, lda, M, K, At, ldat, counters,
                                                                int(sk_tiles));
         g_launches.fetch_add(1);
         if (!b_direct) {
-            const long long total = (long long)K * N;
-            const int blocks = int(std::min<long long>((total + 255) / 256, (long long)dev->sm_count * 16));
-            sg::pack_b_copy_kernel<<<blocks, 256, 0, stream>>>(B, ldb, K, N, Bp, ldbp);
+            dim3 bgrid(unsigned(std::min<long long>((N + 255) / 256, 64)),
+                       unsigned(std::min<long long>(K, 65535)));
+            sg::pack_b_copy_kernel<<<bgrid, 256, 0, stream>>>(B, ldb, K, N, Bp, ldbp);
             g_launches.fetch_add(1);
         }
     }
@@ -442,14 +442,14 @@ int sgemm_device_noalloc(int M, int N, int K, float alpha, const float *A, int l
     float *At = dev->scratch;
     float *Bp = b_direct ? const_cast<float *>(B) : dev->scratch + at_floats;
 
-    dim3 grid(unsigned(std::min<long long>((K + 31) / 32, 1LL << 20)),
-              unsigned(std::min<long long>((M + 31) / 32, 65535)));
+    dim3 grid(unsigned(std::min<long long>((K + 63) / 64, 1LL << 20)),
+              unsigned(std::min<long long>((M + 63) / 64, 65535)));
     sg::pack_a_transpose_kernel<<<grid, 256, 0, stream>>>(A, lda, M, K, At, ldat, nullptr, 0);
     g_launches.fetch_add(1);
     if (!b_direct) {
-        const long long total = (long long)K * N;
-        const int blocks = int(std::min<long long>((total + 255) / 256, (long long)dev->sm_count * 16));
-        sg::pack_b_copy_kernel<<<blocks, 256, 0, stream>>>(B, ldb, K, N, Bp, ldbp);
+        dim3 bgrid(unsigned(std::min<long long>((N + 255) / 256, 64)),
+                   unsigned(std::min<long long>(K, 65535)));
+        sg::pack_b_copy_kernel<<<bgrid, 256, 0, stream>>>(B, ldb, K, N, Bp, ldbp);
         g_launches.fetch_add(1);
     }
     cudaError_t e = cudaGetLastError();
