@@ -48,6 +48,9 @@ def parse_args():
     ap.add_argument("--workload", default=None, help="workload name (default: the 8192^3 case)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--path", choices=["ffma", "tf32x3"], default="ffma",
+                    help="ffma: the FP32 FFMA kernel (the headline); tf32x3: the 3xTF32 "
+                         "tensor-core entry point, same tolerance, its own roofline")
     ap.add_argument("--variant", type=int, default=-1,
                     help="force a kernel variant (tile-configuration sweeps); -1 = automatic")
     return ap.parse_args()
@@ -292,8 +295,10 @@ def run_ours(args):
         torch.zeros((w.M, w.N), device=device)
     torch.cuda.synchronize()
 
+    gemm = binding.sgemm_into if args.path == "ffma" else binding.sgemm_3xtf32_into
+
     def step():
-        binding.sgemm_into(dA, dB, dC, w.alpha, w.beta, stream=stream)
+        gemm(dA, dB, dC, w.alpha, w.beta, stream=stream)
 
     clocks = ClockSampler(local)
     clocks.start()

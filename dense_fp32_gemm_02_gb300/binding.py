@@ -31,6 +31,8 @@ lib.sgemm_host.argtypes = [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]
 lib.sgemm_host.restype = _i
 lib.sgemm_noalloc.argtypes = [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]
 lib.sgemm_noalloc.restype = _i
+lib.sgemm_3xtf32.argtypes = [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]
+lib.sgemm_3xtf32.restype = _i
 lib.sgemm_status_string.argtypes = [_i]
 lib.sgemm_status_string.restype = ctypes.c_char_p
 lib.sgemm_version.argtypes = []
@@ -132,6 +134,24 @@ def sgemm_into(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
     with torch.cuda.device(C.device):
         st = lib.sgemm(M, N, K, float(alpha), A.data_ptr(), _ld(A, K), B.data_ptr(), _ld(B, N),
                        float(beta), C.data_ptr(), _ld(C, N), _stream_handle(stream, C.device))
+    check(st)
+    return C
+
+
+def sgemm_3xtf32_into(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """Like sgemm_into(), on the tensor cores by the 3xTF32 split (same FP32
+    tolerance, not bitwise equal to sgemm_into)."""
+    import torch
+    for name, t in (("A", A), ("B", B), ("C", C)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA float32 tensor")
+    if not (A.device == B.device == C.device):
+        raise ValueError("A, B and C must be on the same device")
+    M, N, K = _shapes(A, B, C)
+    with torch.cuda.device(C.device):
+        st = lib.sgemm_3xtf32(M, N, K, float(alpha), A.data_ptr(), _ld(A, K), B.data_ptr(),
+                              _ld(B, N), float(beta), C.data_ptr(), _ld(C, N),
+                              _stream_handle(stream, C.device))
     check(st)
     return C
 

@@ -23,6 +23,7 @@
 
 #include "../../include/sgemm.h"
 #include "kernels.cuh"
+#include "tf32x3.cuh"
 
 #define SGEMM_API extern "C" __attribute__((visibility("default")))
 
@@ -218,6 +219,10 @@ int device_state(DeviceState **out) {
             cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
             for (const Variant &v : kVariants)
                 if ((e = v.set_attr()) != cudaSuccess) return cuda_fail(e);
+            e = cudaFuncSetAttribute(sg::t3::sgemm_3xtf32_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     int(sg::t3::SMEM_BYTES));
+            if (e != cudaSuccess) return cuda_fail(e);
             d.status = SGEMM_OK;
         }
         d.ready = true;
@@ -227,14 +232,15 @@ int device_state(DeviceState **out) {
 }
 
 int encode_2d(CUtensorMap *map, const float *ptr, uint64_t inner, uint64_t outer,
-              uint64_t row_pitch_elems, uint32_t box_inner, uint32_t box_outer) {
+              uint64_t row_pitch_elems, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {row_pitch_elems * sizeof(float)};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr),
                                 dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         t_last_cuda_error = int(r);
@@ -342,6 +348,83 @@ int sgemm_device(int M, int N, int K, float alpha, const float *A, int lda, cons
     {
         ProfScope prof(stream, true);
         var.launch(grid, stream, tmA, tmB, p);
+        g_launches.fetch_add(1);
+    }
+    e = cudaGetLastError();
+    cudaError_t ef = cudaFreeAsync(ws, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (ef != cudaSuccess) return cuda_fail(ef);
+    return SGEMM_OK;
+}
+
+// The 3xTF32 tensor-core path: split A and B into tf32 hi/lo parts (B
+// transposed), then one CTA per 128 x 256 tile runs three TF32 MMAs per k step.
+int sgemm_device_3xtf32(int M, int N, int K, float alpha, const float *A, int lda,
+                        const float *B, int ldb, float beta, float *C, int ldc,
+                        cudaStream_t stream) {
+    int st = checked_args(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta);
+    if (st != SGEMM_OK || M == 0 || N == 0) return st;
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != SGEMM_OK) return st;
+    if (K == 0 || alpha == 0.0f) return launch_scale(stream, C, ldc, M, N, beta, dev->sm_count);
+
+    namespace t3 = sg::t3;
+    const long long ldk = round_up(K, 4);
+    const size_t a_bytes = round_up((long long)M * ldk * 4, 256);
+    const size_t b_bytes = round_up((long long)N * ldk * 4, 256);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, 2 * a_bytes + 2 * b_bytes, dev->pool, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    char *w = static_cast<char *>(ws);
+    float *Ah = reinterpret_cast<float *>(w);
+    float *Al = reinterpret_cast<float *>(w + a_bytes);
+    float *Bh = reinterpret_cast<float *>(w + 2 * a_bytes);
+    float *Bl = reinterpret_cast<float *>(w + 2 * a_bytes + b_bytes);
+    {
+        ProfScope prof(stream, false);
+        dim3 ga(unsigned(std::min<long long>((K + 255) / 256, 64)), unsigned(std::min(M, 65535)));
+        t3::split_a_kernel<<<ga, 256, 0, stream>>>(A, lda, M, K, Ah, Al, ldk);
+        dim3 gb(unsigned(std::min<long long>((N + 63) / 64, 1LL << 20)),
+                unsigned(std::min<long long>((K + 63) / 64, 65535)));
+        t3::split_bt_kernel<<<gb, 256, 0, stream>>>(B, ldb, K, N, Bh, Bl, ldk);
+        g_launches.fetch_add(2);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        cudaFreeAsync(ws, stream);
+        return cuda_fail(e);
+    }
+    CUtensorMap mAh, mAl, mBh, mBl;
+    const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    if ((st = encode_2d(&mAh, Ah, K, M, ldk, t3::BK, t3::BM, sw)) != SGEMM_OK ||
+        (st = encode_2d(&mAl, Al, K, M, ldk, t3::BK, t3::BM, sw)) != SGEMM_OK ||
+        (st = encode_2d(&mBh, Bh, K, N, ldk, t3::BK, t3::BN, sw)) != SGEMM_OK ||
+        (st = encode_2d(&mBl, Bl, K, N, ldk, t3::BK, t3::BN, sw)) != SGEMM_OK) {
+        cudaFreeAsync(ws, stream);
+        return st;
+    }
+    t3::Params p;
+    p.C = C;
+    p.ldc = ldc;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.tiles_m = int((M + t3::BM - 1) / t3::BM);
+    p.tiles_n = int((N + t3::BN - 1) / t3::BN);
+    p.group_m = 8;
+    p.c_vec4 = (aligned16(C) && ldc % 4 == 0) ? 1 : 0;
+    p.timeout_ns = g_timeout_ns.load();
+    const long long tiles = (long long)p.tiles_m * p.tiles_n;
+    if (tiles > 0x7fffffffLL) {
+        cudaFreeAsync(ws, stream);
+        return SGEMM_ERR_INVALID_ARG;
+    }
+    {
+        ProfScope prof(stream, true);
+        t3::sgemm_3xtf32_kernel<<<unsigned(tiles), t3::THREADS, t3::SMEM_BYTES, stream>>>(
+            mAh, mAl, mBh, mBl, p);
         g_launches.fetch_add(1);
     }
     e = cudaGetLastError();
@@ -652,4 +735,11 @@ SGEMM_API int sgemm_noalloc(int M, int N, int K, float alpha, const float *A, in
                             sgemm_stream_t stream) {
     return sgemm_device_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+SGEMM_API int sgemm_3xtf32(int M, int N, int K, float alpha, const float *A, int lda,
+                           const float *B, int ldb, float beta, float *C, int ldc,
+                           sgemm_stream_t stream) {
+    return sgemm_device_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                               reinterpret_cast<cudaStream_t>(stream));
 }

@@ -1,0 +1,383 @@
+// tf32x3.cuh -- FP32 GEMM on the 5th-generation tensor cores by the 3xTF32
+// split: every fp32 operand x is written as x = hi + lo with hi = tf32(x) and
+// lo = tf32(x - hi); the product A*B is taken as
+//     A_hi*B_hi + A_hi*B_lo + A_lo*B_hi
+// (the dropped A_lo*B_lo term is below 2^-22 of |A||B|), each a TF32 MMA with
+// fp32 accumulation in tensor memory.  Per product the relative error is about
+// 3 * 2^-22, inside the FP32 tolerance 1e-6*K*|alpha|*sum|A||B| for every K.
+//
+// Kernel layout (one CTA per 128 x 256 output tile, 256 threads):
+//   warp 0    thread 0 issues TMA copies of A_hi, A_lo (128 x 32) and B_hi,
+//             B_lo (256 x 32, B transposed so both operands are K-major) into
+//             a 2-stage ring, 128-byte swizzled;
+//   warp 1    allocates 256 TMEM columns; thread 32 issues tcgen05.mma
+//             (M 128, N 256, K 8) three times per 8-wide k step and commits
+//             each stage back to the producer through its empty barrier;
+//   warps 4-7 read the accumulator from TMEM (32 lanes each) and apply
+//             alpha/beta on the way to C.
+// Every barrier wait is bounded; after an expiry the CTA stops issuing,
+// waits (bounded) for its copies and MMAs in flight, and always frees TMEM.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace sg {
+namespace t3 {
+
+constexpr int BM = 128, BN = 256, BK = 32, STAGES = 2;
+constexpr int A_TILE = BM * BK;                       // floats, 16 KB
+constexpr int B_TILE = BN * BK;                       // floats, 32 KB
+constexpr int STAGE_FLOATS = 2 * A_TILE + 2 * B_TILE; // A_hi, A_lo, B_hi, B_lo
+constexpr uint32_t STAGE_BYTES = STAGE_FLOATS * 4u;   // 96 KB
+constexpr int THREADS = 256;
+constexpr uint32_t TMEM_COLS = 256;                   // 128 lanes x 256 fp32 columns
+// ring + 1 KB alignment slack + barriers, and an unused tail so the CTA owns
+// more shared memory than the ring (and one CTA per SM keeps TMEM uncontended)
+constexpr size_t SMEM_BYTES = size_t(STAGES) * STAGE_BYTES + 1024 + 256 + 16 * 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+static_assert(SMEM_BYTES > 232448 / 2, "one CTA per SM");
+
+// Instruction descriptor of tcgen05.mma.kind::tf32: D f32, A and B tf32, both
+// K-major, N = 256, M = 128.
+constexpr uint32_t IDESC = (1u << 4)                    // D format: f32
+                           | (2u << 7)                  // A format: tf32
+                           | (2u << 10)                 // B format: tf32
+                           | (uint32_t(BN >> 3) << 17)  // N / 8
+                           | (uint32_t(BM >> 4) << 24); // M / 16
+
+// Shared-memory matrix descriptor: K-major operand, rows of 128 bytes with the
+// 128-byte swizzle (the layout the TMA writes), 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= uint64_t((saddr & 0x3FFFFu) >> 4);     // start address, 16-byte units
+    d |= uint64_t(1) << 16;                     // leading offset (unused for this layout)
+    d |= uint64_t(1024 >> 4) << 32;             // stride between 8-row groups
+    d |= uint64_t(1) << 46;                     // descriptor version
+    d |= uint64_t(2) << 61;                     // 128-byte swizzle
+    return d;
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(dst)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// D (tmem) = A * B (+ D when accumulate != 0)
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(IDESC), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// tf32 rounding (round to nearest, ties away from zero) of an fp32 value.
+__device__ __forceinline__ float to_tf32(float x) {
+    uint32_t t;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(t) : "f"(x));
+    return __uint_as_float(t);
+}
+
+__device__ __forceinline__ void split(float x, float &hi, float &lo) {
+    hi = to_tf32(x);
+    // x - hi is exact in fp32; a non-finite x keeps everything in hi
+    lo = isfinite(x) ? to_tf32(x - hi) : 0.0f;
+}
+
+struct Params {
+    float *C;
+    long long ldc;
+    int M, N, K;
+    float alpha, beta;
+    int tiles_m, tiles_n, group_m;
+    int c_vec4;
+    unsigned long long timeout_ns;
+};
+
+__global__ void __launch_bounds__(THREADS, 1)
+    sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
+                        const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl,
+                        const Params p) {
+    extern __shared__ unsigned char smem_raw[];
+    const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
+    float *ring = reinterpret_cast<float *>(base);
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + STAGES * STAGE_FLOATS);
+    uint64_t *empty = full + STAGES;
+    uint64_t *acc_full = empty + STAGES;
+    uint64_t *drain = acc_full + 1;
+    uint32_t *tmem_base = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_base, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t taddr = *tmem_base;
+
+    int tm, tn;
+    tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    const int k_tiles = (p.K + BK - 1) / BK;
+
+    if (warp == 0) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmAh);
+            tma_prefetch_desc(&tmAl);
+            tma_prefetch_desc(&tmBh);
+            tma_prefetch_desc(&tmBl);
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            for (int kb = 0; kb < k_tiles; ++kb) {
+                if (*abort_flag) break;
+                if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns)) {
+                    atomicOr(&g_error_word, ERR_EMPTY_WAIT);
+                    *abort_flag = 1;
+                    break;
+                }
+                float *st = ring + stage * STAGE_FLOATS;
+                mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                tma_load_2d(st, &tmAh, &full[stage], kb * BK, tm * BM);
+                tma_load_2d(st + A_TILE, &tmAl, &full[stage], kb * BK, tm * BM);
+                tma_load_2d(st + 2 * A_TILE, &tmBh, &full[stage], kb * BK, tn * BN);
+                tma_load_2d(st + 2 * A_TILE + B_TILE, &tmBl, &full[stage], kb * BK, tn * BN);
+                ++issued;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            // after an abort: let the copies already issued land before exit
+            if (*abort_flag) {
+                for (int q = (issued > STAGES ? issued - STAGES : 0); q < issued; ++q)
+                    if (!mbar_wait(&full[q % STAGES], uint32_t((q / STAGES) & 1), p.timeout_ns)) {
+                        atomicOr(&g_error_word, ERR_DRAIN_WAIT);
+                        break;
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            const uint32_t ring_s = smem_addr(ring);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int kb = 0; kb < k_tiles; ++kb) {
+                if (!mbar_wait(&full[stage], phase, p.timeout_ns)) {
+                    atomicOr(&g_error_word, ERR_FULL_WAIT);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t ah = ring_s + uint32_t(stage * STAGE_FLOATS) * 4u;
+                const uint32_t al = ah + A_TILE * 4u;
+                const uint32_t bh = ah + 2u * A_TILE * 4u;
+                const uint32_t bl = bh + B_TILE * 4u;
+#pragma unroll
+                for (int kk = 0; kk < BK / 8; ++kk) {
+                    const uint32_t off = uint32_t(kk) * 32u;   // 8 tf32 = 32 bytes along K
+                    const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                    mma_tf32(taddr, smem_desc_sw128(al + off), smem_desc_sw128(bh + off), acc);
+                    mma_tf32(taddr, smem_desc_sw128(ah + off), smem_desc_sw128(bl + off), 1u);
+                    mma_tf32(taddr, smem_desc_sw128(ah + off), smem_desc_sw128(bh + off), 1u);
+                }
+                mma_commit(&empty[stage]);     // stage free once these MMAs have read it
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (ok) {
+                mma_commit(acc_full);          // accumulator complete
+            } else {
+                // no MMA may still run when TMEM is freed
+                mma_commit(drain);
+                if (!mbar_wait(drain, 0u, p.timeout_ns)) atomicOr(&g_error_word, ERR_DRAIN_WAIT);
+            }
+        }
+    } else if (warp >= 4) {
+        // ================================================================ epilogue
+        const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
+        bool ready = false;
+        if (!__any_sync(0xffffffffu, *abort_flag)) {
+            ready = mbar_wait(acc_full, 0u, p.timeout_ns);
+            ready = __all_sync(0xffffffffu, ready);
+            if (!ready && lane == 0) {
+                atomicOr(&g_error_word, ERR_FULL_WAIT);
+                *abort_flag = 1;
+            }
+        }
+        if (ready) {
+            tc_fence_after();
+            const int row = tm * BM + quarter * 32 + lane;
+            const bool row_ok = row < p.M;
+            float *crow = p.C + (long long)row * p.ldc;
+            const float alpha = p.alpha, beta = p.beta;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                float v[32];
+                __syncwarp();   // tcgen05.ld is warp-collective
+                tmem_load32(taddr + (uint32_t(quarter * 32) << 16) + uint32_t(c * 32), v);
+                const int col0 = tn * BN + c * 32;
+                if (!row_ok || col0 >= p.N) continue;
+                if (p.c_vec4 && col0 + 31 < p.N) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        float4 o;
+                        float4 *dst = reinterpret_cast<float4 *>(crow + col0) + q;
+                        if (beta != 0.0f) {
+                            const float4 cin = __ldcs(dst);
+                            o.x = fmaf(alpha, v[4 * q + 0], beta * cin.x);
+                            o.y = fmaf(alpha, v[4 * q + 1], beta * cin.y);
+                            o.z = fmaf(alpha, v[4 * q + 2], beta * cin.z);
+                            o.w = fmaf(alpha, v[4 * q + 3], beta * cin.w);
+                        } else {
+                            o.x = alpha * v[4 * q + 0];
+                            o.y = alpha * v[4 * q + 1];
+                            o.z = alpha * v[4 * q + 2];
+                            o.w = alpha * v[4 * q + 3];
+                        }
+                        __stcs(dst, o);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int col = col0 + e;
+                        if (col < p.N) {
+                            const float cin = (beta != 0.0f) ? beta * crow[col] : 0.0f;
+                            crow[col] = (beta != 0.0f) ? fmaf(alpha, v[e], cin) : alpha * v[e];
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(taddr, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ split pre-pass
+// A (M x K, row pitch lda) -> Ah, Al (M x K, row pitch ldk): same layout, K-major.
+__global__ void __launch_bounds__(256)
+    split_a_kernel(const float *__restrict__ A, long long lda, int M, int K, float *__restrict__ Ah,
+                   float *__restrict__ Al, long long ldk) {
+    for (long long m = blockIdx.y; m < M; m += gridDim.y) {
+        const float *src = A + m * lda;
+        for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < K;
+             k += (long long)gridDim.x * blockDim.x) {
+            float hi, lo;
+            split(__ldcs(src + k), hi, lo);
+            Ah[m * ldk + k] = hi;
+            Al[m * ldk + k] = lo;
+        }
+    }
+}
+
+// B (K x N, row pitch ldb) -> Bh, Bl (N x K, row pitch ldk): transposed so B is
+// K-major too.  64x64 tiles through shared memory, 16 loads in flight per thread.
+__global__ void __launch_bounds__(256)
+    split_bt_kernel(const float *__restrict__ B, long long ldb, int K, int N, float *__restrict__ Bh,
+                    float *__restrict__ Bl, long long ldk) {
+    __shared__ float tile[64][65];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    for (long long k0 = (long long)blockIdx.y * 64; k0 < K; k0 += (long long)gridDim.y * 64) {
+        for (long long n0 = (long long)blockIdx.x * 64; n0 < N; n0 += (long long)gridDim.x * 64) {
+            float v[16];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const long long k = k0 + w * 8 + r;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const long long n = n0 + lane + 32 * h;
+                    v[2 * r + h] = (k < K && n < N) ? __ldcs(B + k * ldb + n) : 0.0f;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) tile[w * 8 + r][lane + 32 * h] = v[2 * r + h];
+            __syncthreads();
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const long long n = n0 + w * 8 + r;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const long long k = k0 + lane + 32 * h;
+                    if (n < N && k < K) {
+                        float hi, lo;
+                        split(tile[lane + 32 * h][w * 8 + r], hi, lo);
+                        Bh[n * ldk + k] = hi;
+                        Bl[n * ldk + k] = lo;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+}  // namespace t3
+}  // namespace sg

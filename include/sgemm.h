@@ -86,6 +86,25 @@ int sgemm_host(int M, int N, int K, float alpha,
                float beta, float *C, int ldc,
                sgemm_stream_t stream);
 
+/*
+ * sgemm_3xtf32 -- the same GEMM on the tensor cores (tcgen05, TF32 inputs,
+ * fp32 accumulation in tensor memory) by the 3xTF32 split: each operand is
+ * x = hi + lo with hi = tf32(x), lo = tf32(x - hi), and A*B is taken as
+ * A_hi*B_hi + A_hi*B_lo + A_lo*B_hi.  The result meets the same FP32
+ * tolerance as sgemm() (about 3 * 2^-22 relative error per product, fp32
+ * accumulation) but is not bitwise equal to it.  Arguments, ownership, stream
+ * behaviour and errors as for sgemm().  Workspace: the hi and lo parts of A
+ * (2 x M x roundup(K,4) floats) and of B transposed (2 x N x roundup(K,4)),
+ * from the library's stream-ordered pool.  Non-finite inputs give NaN or Inf
+ * results as IEEE arithmetic on the parts does; an input of magnitude near
+ * FLT_MAX may overflow in its tf32 part.
+ */
+int sgemm_3xtf32(int M, int N, int K, float alpha,
+                 const float *A, int lda,
+                 const float *B, int ldb,
+                 float beta, float *C, int ldc,
+                 sgemm_stream_t stream);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char *sgemm_status_string(int status);
 
