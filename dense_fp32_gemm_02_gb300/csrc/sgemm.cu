@@ -382,8 +382,9 @@ int sgemm_device_3xtf32(int M, int N, int K, float alpha, const float *A, int ld
     float *Bl = reinterpret_cast<float *>(w + 2 * a_bytes + b_bytes);
     {
         ProfScope prof(stream, false);
-        dim3 ga(unsigned(std::min<long long>((K + 255) / 256, 64)), unsigned(std::min(M, 65535)));
-        t3::split_a_kernel<<<ga, 256, 0, stream>>>(A, lda, M, K, Ah, Al, ldk);
+        const int vec4 = (aligned16(A) && lda % 4 == 0 && K % 4 == 0) ? 1 : 0;
+        dim3 ga(unsigned(std::min<long long>((K + 4095) / 4096, 64)), unsigned(std::min(M, 65535)));
+        t3::split_a_kernel<<<ga, 256, 0, stream>>>(A, lda, M, K, Ah, Al, ldk, vec4);
         dim3 gb(unsigned(std::min<long long>((N + 63) / 64, 1LL << 20)),
                 unsigned(std::min<long long>((K + 63) / 64, 65535)));
         t3::split_bt_kernel<<<gb, 256, 0, stream>>>(B, ldb, K, N, Bh, Bl, ldk);
@@ -414,17 +415,17 @@ int sgemm_device_3xtf32(int M, int N, int K, float alpha, const float *A, int ld
     p.tiles_m = int((M + t3::BM - 1) / t3::BM);
     p.tiles_n = int((N + t3::BN - 1) / t3::BN);
     p.group_m = 8;
-    p.c_vec4 = (aligned16(C) && ldc % 4 == 0) ? 1 : 0;
     p.timeout_ns = g_timeout_ns.load();
     const long long tiles = (long long)p.tiles_m * p.tiles_n;
     if (tiles > 0x7fffffffLL) {
         cudaFreeAsync(ws, stream);
         return SGEMM_ERR_INVALID_ARG;
     }
+    const unsigned grid = unsigned(std::min<long long>(tiles, dev->sm_count));
     {
         ProfScope prof(stream, true);
-        t3::sgemm_3xtf32_kernel<<<unsigned(tiles), t3::THREADS, t3::SMEM_BYTES, stream>>>(
-            mAh, mAl, mBh, mBl, p);
+        t3::sgemm_3xtf32_kernel<<<grid, t3::THREADS, t3::SMEM_BYTES, stream>>>(mAh, mAl, mBh,
+                                                                               mBl, p);
         g_launches.fetch_add(1);
     }
     e = cudaGetLastError();

@@ -6,15 +6,19 @@
 // fp32 accumulation in tensor memory.  Per product the relative error is about
 // 3 * 2^-22, inside the FP32 tolerance 1e-6*K*|alpha|*sum|A||B| for every K.
 //
-// Kernel layout (one CTA per 128 x 256 output tile, 256 threads):
+// Kernel layout (persistent: one CTA per SM walks 128 x 256 output tiles
+// b, b + gridDim.x, ...; 256 threads):
 //   warp 0    thread 0 issues TMA copies of A_hi, A_lo (128 x 32) and B_hi,
 //             B_lo (256 x 32, B transposed so both operands are K-major) into
 //             a 2-stage ring, 128-byte swizzled;
-//   warp 1    allocates 256 TMEM columns; thread 32 issues tcgen05.mma
-//             (M 128, N 256, K 8) three times per 8-wide k step and commits
-//             each stage back to the producer through its empty barrier;
-//   warps 4-7 read the accumulator from TMEM (32 lanes each) and apply
-//             alpha/beta on the way to C.
+//   warp 1    allocates all 512 TMEM columns (two 128 x 256 fp32
+//             accumulators); thread 32 issues tcgen05.mma (M 128, N 256, K 8)
+//             three times per 8-wide k step into the tile's accumulator and
+//             commits each stage back to the producer through its empty barrier;
+//   warps 4-7 read a finished accumulator from TMEM (32 lanes each), hand it
+//             back, and apply alpha/beta on the way to C, staged through
+//             shared memory for coalesced rows -- while the MMAs of the next
+//             tile already run in the other accumulator.
 // Every barrier wait is bounded; after an expiry the CTA stops issuing,
 // waits (bounded) for its copies and MMAs in flight, and always frees TMEM.
 #pragma once
@@ -34,10 +38,13 @@ constexpr int B_TILE = BN * BK;                       // floats, 32 KB
 constexpr int STAGE_FLOATS = 2 * A_TILE + 2 * B_TILE; // A_hi, A_lo, B_hi, B_lo
 constexpr uint32_t STAGE_BYTES = STAGE_FLOATS * 4u;   // 96 KB
 constexpr int THREADS = 256;
-constexpr uint32_t TMEM_COLS = 256;                   // 128 lanes x 256 fp32 columns
-// ring + 1 KB alignment slack + barriers, and an unused tail so the CTA owns
-// more shared memory than the ring (and one CTA per SM keeps TMEM uncontended)
-constexpr size_t SMEM_BYTES = size_t(STAGES) * STAGE_BYTES + 1024 + 256 + 16 * 1024;
+constexpr int EPI_WARPS = 4;                          // warps 4..7
+constexpr uint32_t ACC_COLS = 256;                    // 128 lanes x 256 fp32 columns
+constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;          // two accumulators: all of TMEM
+constexpr int EPI_FLOATS = EPI_WARPS * 32 * 33;       // per-warp 32 x 33 staging blocks
+// ring + staging + 1 KB alignment slack + barriers; more than half the SM's
+// shared memory, so one CTA per SM and the whole TMEM is this CTA's
+constexpr size_t SMEM_BYTES = size_t(STAGES) * STAGE_BYTES + size_t(EPI_FLOATS) * 4 + 1024 + 256;
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 static_assert(SMEM_BYTES > 232448 / 2, "one CTA per SM");
 
@@ -135,7 +142,6 @@ struct Params {
     int M, N, K;
     float alpha, beta;
     int tiles_m, tiles_n, group_m;
-    int c_vec4;
     unsigned long long timeout_ns;
 };
 
@@ -146,10 +152,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     extern __shared__ unsigned char smem_raw[];
     const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
     float *ring = reinterpret_cast<float *>(base);
-    uint64_t *full = reinterpret_cast<uint64_t *>(ring + STAGES * STAGE_FLOATS);
+    float *epi = ring + STAGES * STAGE_FLOATS;
+    uint64_t *full = reinterpret_cast<uint64_t *>(epi + EPI_FLOATS);
     uint64_t *empty = full + STAGES;
-    uint64_t *acc_full = empty + STAGES;
-    uint64_t *drain = acc_full + 1;
+    uint64_t *acc_full = empty + STAGES;     // [2] MMA -> epilogue
+    uint64_t *acc_empty = acc_full + 2;      // [2] epilogue -> MMA
+    uint64_t *drain = acc_empty + 2;
     uint32_t *tmem_base = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base + 1);
 
@@ -159,7 +167,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(acc_full, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], EPI_WARPS);
+        }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -170,8 +181,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t taddr = *tmem_base;
 
-    int tm, tn;
-    tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    const int num_tiles = p.tiles_m * p.tiles_n;
+    const int my_tiles = blockIdx.x < num_tiles ? (num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const int k_tiles = (p.K + BK - 1) / BK;
 
     if (warp == 0) {
@@ -183,29 +194,34 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_prefetch_desc(&tmBl);
             int stage = 0;
             uint32_t phase = 0;
-            int issued = 0;
-            for (int kb = 0; kb < k_tiles; ++kb) {
-                if (*abort_flag) break;
-                if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns)) {
-                    atomicOr(&g_error_word, ERR_EMPTY_WAIT);
-                    *abort_flag = 1;
-                    break;
-                }
-                float *st = ring + stage * STAGE_FLOATS;
-                mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-                tma_load_2d(st, &tmAh, &full[stage], kb * BK, tm * BM);
-                tma_load_2d(st + A_TILE, &tmAl, &full[stage], kb * BK, tm * BM);
-                tma_load_2d(st + 2 * A_TILE, &tmBh, &full[stage], kb * BK, tn * BN);
-                tma_load_2d(st + 2 * A_TILE + B_TILE, &tmBl, &full[stage], kb * BK, tn * BN);
-                ++issued;
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
+            long long issued = 0;
+            for (int j = 0; j < my_tiles && !*abort_flag; ++j) {
+                int tm, tn;
+                tile_coords(blockIdx.x + j * gridDim.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                for (int kb = 0; kb < k_tiles; ++kb) {
+                    if (*abort_flag) break;
+                    // first use of a stage: parity 1 counts as complete
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns)) {
+                        atomicOr(&g_error_word, ERR_EMPTY_WAIT);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    float *st = ring + stage * STAGE_FLOATS;
+                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                    tma_load_2d(st, &tmAh, &full[stage], kb * BK, tm * BM);
+                    tma_load_2d(st + A_TILE, &tmAl, &full[stage], kb * BK, tm * BM);
+                    tma_load_2d(st + 2 * A_TILE, &tmBh, &full[stage], kb * BK, tn * BN);
+                    tma_load_2d(st + 2 * A_TILE + B_TILE, &tmBl, &full[stage], kb * BK, tn * BN);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
             // after an abort: let the copies already issued land before exit
             if (*abort_flag) {
-                for (int q = (issued > STAGES ? issued - STAGES : 0); q < issued; ++q)
+                for (long long q = (issued > STAGES ? issued - STAGES : 0); q < issued; ++q)
                     if (!mbar_wait(&full[q % STAGES], uint32_t((q / STAGES) & 1), p.timeout_ns)) {
                         atomicOr(&g_error_word, ERR_DRAIN_WAIT);
                         break;
@@ -219,35 +235,46 @@ __global__ void __launch_bounds__(THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int kb = 0; kb < k_tiles; ++kb) {
-                if (!mbar_wait(&full[stage], phase, p.timeout_ns)) {
-                    atomicOr(&g_error_word, ERR_FULL_WAIT);
+            for (int j = 0; j < my_tiles && ok; ++j) {
+                const int a = j & 1;
+                // the epilogue has handed this accumulator back (first use: free)
+                if (!mbar_wait(&acc_empty[a], (uint32_t(j >> 1) & 1u) ^ 1u, p.timeout_ns)) {
+                    atomicOr(&g_error_word, ERR_EMPTY_WAIT);
                     *abort_flag = 1;
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t ah = ring_s + uint32_t(stage * STAGE_FLOATS) * 4u;
-                const uint32_t al = ah + A_TILE * 4u;
-                const uint32_t bh = ah + 2u * A_TILE * 4u;
-                const uint32_t bl = bh + B_TILE * 4u;
+                const uint32_t d = taddr + uint32_t(a) * ACC_COLS;
+                for (int kb = 0; kb < k_tiles; ++kb) {
+                    if (*abort_flag || !mbar_wait(&full[stage], phase, p.timeout_ns)) {
+                        if (!*abort_flag) atomicOr(&g_error_word, ERR_FULL_WAIT);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ah = ring_s + uint32_t(stage * STAGE_FLOATS) * 4u;
+                    const uint32_t al = ah + A_TILE * 4u;
+                    const uint32_t bh = ah + 2u * A_TILE * 4u;
+                    const uint32_t bl = bh + B_TILE * 4u;
 #pragma unroll
-                for (int kk = 0; kk < BK / 8; ++kk) {
-                    const uint32_t off = uint32_t(kk) * 32u;   // 8 tf32 = 32 bytes along K
-                    const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-                    mma_tf32(taddr, smem_desc_sw128(al + off), smem_desc_sw128(bh + off), acc);
-                    mma_tf32(taddr, smem_desc_sw128(ah + off), smem_desc_sw128(bl + off), 1u);
-                    mma_tf32(taddr, smem_desc_sw128(ah + off), smem_desc_sw128(bh + off), 1u);
+                    for (int kk = 0; kk < BK / 8; ++kk) {
+                        const uint32_t off = uint32_t(kk) * 32u;   // 8 tf32 = 32 bytes along K
+                        const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                        mma_tf32(d, smem_desc_sw128(al + off), smem_desc_sw128(bh + off), acc);
+                        mma_tf32(d, smem_desc_sw128(ah + off), smem_desc_sw128(bl + off), 1u);
+                        mma_tf32(d, smem_desc_sw128(ah + off), smem_desc_sw128(bh + off), 1u);
+                    }
+                    mma_commit(&empty[stage]);     // stage free once these MMAs have read it
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
-                mma_commit(&empty[stage]);     // stage free once these MMAs have read it
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+                if (ok) mma_commit(&acc_full[a]);  // this tile's accumulator is complete
             }
-            if (ok) {
-                mma_commit(acc_full);          // accumulator complete
-            } else {
+            if (!ok) {
                 // no MMA may still run when TMEM is freed
                 mma_commit(drain);
                 if (!mbar_wait(drain, 0u, p.timeout_ns)) atomicOr(&g_error_word, ERR_DRAIN_WAIT);
@@ -256,54 +283,56 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp >= 4) {
         // ================================================================ epilogue
         const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
-        bool ready = false;
-        if (!__any_sync(0xffffffffu, *abort_flag)) {
-            ready = mbar_wait(acc_full, 0u, p.timeout_ns);
+        float *buf = epi + quarter * (32 * 33);
+        const float alpha = p.alpha, beta = p.beta;
+        for (int j = 0; j < my_tiles; ++j) {
+            const int a = j & 1;
+            if (__any_sync(0xffffffffu, *abort_flag)) break;
+            bool ready = mbar_wait(&acc_full[a], uint32_t(j >> 1) & 1u, p.timeout_ns);
             ready = __all_sync(0xffffffffu, ready);
-            if (!ready && lane == 0) {
-                atomicOr(&g_error_word, ERR_FULL_WAIT);
-                *abort_flag = 1;
+            if (!ready) {
+                if (lane == 0) {
+                    atomicOr(&g_error_word, ERR_FULL_WAIT);
+                    *abort_flag = 1;
+                }
+                break;
             }
-        }
-        if (ready) {
             tc_fence_after();
-            const int row = tm * BM + quarter * 32 + lane;
-            const bool row_ok = row < p.M;
-            float *crow = p.C + (long long)row * p.ldc;
-            const float alpha = p.alpha, beta = p.beta;
+            int tm, tn;
+            tile_coords(blockIdx.x + j * gridDim.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            const int row0 = tm * BM + quarter * 32;
+            const uint32_t src = taddr + uint32_t(a) * ACC_COLS + (uint32_t(quarter * 32) << 16);
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 float v[32];
-                __syncwarp();   // tcgen05.ld is warp-collective
-                tmem_load32(taddr + (uint32_t(quarter * 32) << 16) + uint32_t(c * 32), v);
-                const int col0 = tn * BN + c * 32;
-                if (!row_ok || col0 >= p.N) continue;
-                if (p.c_vec4 && col0 + 31 < p.N) {
+                __syncwarp();   // tcgen05.ld is warp-collective; buf reuse
+                tmem_load32(src + uint32_t(c * 32), v);
+                if (c == BN / 32 - 1) {
+                    // all of this accumulator is in registers: hand it back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[a]);
+                }
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        float4 o;
-                        float4 *dst = reinterpret_cast<float4 *>(crow + col0) + q;
-                        if (beta != 0.0f) {
-                            const float4 cin = __ldcs(dst);
-                            o.x = fmaf(alpha, v[4 * q + 0], beta * cin.x);
-                            o.y = fmaf(alpha, v[4 * q + 1], beta * cin.y);
-                            o.z = fmaf(alpha, v[4 * q + 2], beta * cin.z);
-                            o.w = fmaf(alpha, v[4 * q + 3], beta * cin.w);
-                        } else {
-                            o.x = alpha * v[4 * q + 0];
-                            o.y = alpha * v[4 * q + 1];
-                            o.z = alpha * v[4 * q + 2];
-                            o.w = alpha * v[4 * q + 3];
-                        }
-                        __stcs(dst, o);
-                    }
-                } else {
+                for (int i = 0; i < 32; ++i) buf[lane * 33 + i] = v[i];
+                __syncwarp();
+                // row r of the block: lane = column; C rows read and written
+                // 128 contiguous bytes at a time, all 32 loads in flight first
+                const int col = tn * BN + c * 32 + lane;
+                const bool col_ok = col < p.N;
+                float cin[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int col = col0 + e;
-                        if (col < p.N) {
-                            const float cin = (beta != 0.0f) ? beta * crow[col] : 0.0f;
-                            crow[col] = (beta != 0.0f) ? fmaf(alpha, v[e], cin) : alpha * v[e];
+                for (int r = 0; r < 32; ++r)
+                    cin[r] = (beta != 0.0f && col_ok && row0 + r < p.M)
+                                 ? __ldcs(p.C + (long long)(row0 + r) * p.ldc + col)
+                                 : 0.0f;
+                if (col_ok) {
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) {
+                        if (row0 + r < p.M) {
+                            const float x = buf[r * 33 + lane];
+                            p.C[(long long)(row0 + r) * p.ldc + col] =
+                                (beta != 0.0f) ? fmaf(alpha, x, beta * cin[r]) : alpha * x;
                         }
                     }
                 }
@@ -321,17 +350,55 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // ------------------------------------------------------------------ split pre-pass
 // A (M x K, row pitch lda) -> Ah, Al (M x K, row pitch ldk): same layout, K-major.
+// Each thread keeps 16 floats in flight: 4 float4 when `vec4` (A 16-byte
+// aligned, lda and K multiples of 4), else 16 scalars; a block covers 4096
+// consecutive floats of a row per step.
 __global__ void __launch_bounds__(256)
     split_a_kernel(const float *__restrict__ A, long long lda, int M, int K, float *__restrict__ Ah,
-                   float *__restrict__ Al, long long ldk) {
+                   float *__restrict__ Al, long long ldk, int vec4) {
     for (long long m = blockIdx.y; m < M; m += gridDim.y) {
         const float *src = A + m * lda;
-        for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < K;
-             k += (long long)gridDim.x * blockDim.x) {
-            float hi, lo;
-            split(__ldcs(src + k), hi, lo);
-            Ah[m * ldk + k] = hi;
-            Al[m * ldk + k] = lo;
+        float *dh = Ah + m * ldk, *dl = Al + m * ldk;
+        for (long long c0 = (long long)blockIdx.x * 4096; c0 < K; c0 += (long long)gridDim.x * 4096) {
+            if (vec4) {
+                float4 v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const long long c = c0 + (j * 256 + threadIdx.x) * 4;
+                    v[j] = c < K ? __ldcs(reinterpret_cast<const float4 *>(src + c))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const long long c = c0 + (j * 256 + threadIdx.x) * 4;
+                    if (c < K) {
+                        float4 h, l;
+                        split(v[j].x, h.x, l.x);
+                        split(v[j].y, h.y, l.y);
+                        split(v[j].z, h.z, l.z);
+                        split(v[j].w, h.w, l.w);
+                        *reinterpret_cast<float4 *>(dh + c) = h;
+                        *reinterpret_cast<float4 *>(dl + c) = l;
+                    }
+                }
+            } else {
+                float v[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const long long c = c0 + j * 256 + threadIdx.x;
+                    v[j] = c < K ? __ldcs(src + c) : 0.0f;
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const long long c = c0 + j * 256 + threadIdx.x;
+                    if (c < K) {
+                        float h, l;
+                        split(v[j], h, l);
+                        dh[c] = h;
+                        dl[c] = l;
+                    }
+                }
+            }
         }
     }
 }
