@@ -37,6 +37,10 @@ METRIC = "SGEMM GFLOP/s (2MNK/t) at M=N=K=8192 FP32; % of GB300 FP32 FFMA peak"
 FFMA_PER_SM_PER_CLK = 128
 SM_MAX_MHZ_FALLBACK = 2070.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "traffic.json")
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+# nominal dense TF32 / BF16 tensor throughput of GB300 (1.1 / 2.25 PFLOP/s)
+TF32_PER_BF16 = 1.1 / 2.25
+BF16_FALLBACK_TFLOPS = 1900.0
 
 
 def parse_args():
@@ -48,6 +52,8 @@ def parse_args():
     ap.add_argument("--workload", default=None, help="workload name (default: the 8192^3 case)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-tf32x3", action="store_true",
+                    help="skip the 3xTF32 tensor-core measurement added to the default line")
     ap.add_argument("--path", choices=["ffma", "tf32x3"], default="ffma",
                     help="ffma: the FP32 FFMA kernel (the headline); tf32x3: the 3xTF32 "
                          "tensor-core entry point, same tolerance, its own roofline")
@@ -131,21 +137,26 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, windows=None):
+        """Clock summary over the samples inside `windows` (default: every
+        marked window); the sample file is read once and kept."""
         import datetime
-        rows = []
-        if self.path and os.path.exists(self.path):
-            for line in open(self.path):
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 10:
-                    continue
-                try:
-                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                    rows.append((ts, float(parts[2]), float(parts[3]), parts[4], parts[5:]))
-                except ValueError:
-                    continue
-            os.unlink(self.path)
-        inside = [r for r in rows if any(t0 - 0.15 <= r[0] <= t1 + 0.15 for t0, t1 in self.windows)]
+        if not hasattr(self, "_rows"):
+            self._rows = []
+            if self.path and os.path.exists(self.path):
+                for line in open(self.path):
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 10:
+                        continue
+                    try:
+                        ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                        self._rows.append((ts, float(parts[2]), float(parts[3]), parts[4], parts[5:]))
+                    except ValueError:
+                        continue
+                os.unlink(self.path)
+        rows = self._rows
+        windows = self.windows if windows is None else windows
+        inside = [r for r in rows if any(t0 - 0.15 <= r[0] <= t1 + 0.15 for t0, t1 in windows)]
         use = inside or rows
         if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
@@ -271,6 +282,101 @@ def kernel_revision():
     return h.hexdigest()[:16]
 
 
+def tensor_peak_tf32():
+    """(peak TFLOP/s of TF32 MMA, source text): the measured dense bf16 burst
+    peak times the nominal TF32/BF16 ratio."""
+    try:
+        with open(PEAKS_FILE) as f:
+            bf16 = float(json.load(f)["bf16_tflops"])
+        src = f"measured bf16 burst {bf16} TFLOP/s x nominal tf32/bf16 ratio 1.1/2.25"
+    except (OSError, ValueError, KeyError):
+        bf16 = BF16_FALLBACK_TFLOPS
+        src = f"fallback bf16 {bf16} TFLOP/s x nominal tf32/bf16 ratio 1.1/2.25"
+    return bf16 * TF32_PER_BF16, src
+
+
+def measure_tf32x3(args, w, binding, dA, dB, dC, C, stream, world, device):
+    """The 3xTF32 tensor-core entry point on the same workload: device-time
+    rate, the main kernel against the TF32 tensor roofline, and end to end
+    (pinned host buffers copied in and C copied out every step)."""
+    import numpy as np
+    import torch
+    C0 = torch.from_numpy(np.ascontiguousarray(C)).to(device) if C is not None else None
+
+    def reset():
+        if C0 is not None:
+            dC.copy_(C0)
+
+    def step():
+        binding.sgemm_3xtf32_into(dA, dB, dC, w.alpha, w.beta, stream=stream)
+
+    reset()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    binding.profile_collect()
+    binding.profile_enable(True)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, device)
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    stop.record(stream)
+    stop.synchronize()
+    binding.profile_enable(False)
+    prof = binding.profile_collect()
+    if binding.device_status(stream=stream) != 0:
+        raise RuntimeError("device error word set during the 3xTF32 timed region")
+    ms = max_over_ranks(world, start.elapsed_time(stop), device) / args.steps
+    main_ms = prof["main_ms"] / max(1, prof["main_launches"])
+    split_ms = prof["pack_ms"] / max(1, prof["pack_launches"]) if prof["pack_launches"] else 0.0
+    peak, src = tensor_peak_tf32()
+    mma_tflops = 3.0 * w.flops / (main_ms * 1e-3) / 1e12
+    out = {
+        "value": round(aggregate_gflops(w.flops, ms, world), 3), "unit": "GFLOP/s",
+        "ms_per_step": round(ms, 4), "entry_point": "sgemm_3xtf32",
+        "roofline": {"bound": "tensor", "kernel": "sgemm_3xtf32_kernel",
+                     "achieved": round(mma_tflops, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
+                     "frac": round(mma_tflops / peak, 4), "traffic": None, "peak_source": src,
+                     "algorithmic_flops_per_launch": 3.0 * w.flops,
+                     "note": "three TF32 MMAs per fp32 product: achieved counts MMA FLOPs",
+                     "main_kernel_ms": round(main_ms, 4), "split_kernels_ms": round(split_ms, 4)},
+    }
+    if not args.no_e2e:
+        hA = torch.from_numpy(np.ascontiguousarray(dA.cpu().numpy())).pin_memory()
+        hB = torch.from_numpy(np.ascontiguousarray(dB.cpu().numpy())).pin_memory()
+        hC = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+        if C0 is not None:
+            hC.copy_(C0.cpu())
+        hOut = torch.empty_like(hC).pin_memory()
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                dA.copy_(hA, non_blocking=True)
+                dB.copy_(hB, non_blocking=True)
+                if w.beta != 0:
+                    dC.copy_(hC, non_blocking=True)
+                step()
+                hOut.copy_(dC, non_blocking=True)
+            stream.synchronize()
+
+        e2e_step()
+        barrier(world, device)
+        t = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        e2e_s = max_over_ranks(world, time.perf_counter() - t, device)
+        out["e2e"] = {"value": round(w.flops * args.steps / e2e_s / 1e9 * world, 3),
+                      "unit": "GFLOP/s",
+                      "h2d_bytes_per_step": (hA.numel() + hB.numel()
+                                             + (hC.numel() if w.beta != 0 else 0)) * 4,
+                      "d2h_bytes_per_step": hOut.numel() * 4,
+                      "ms_per_step": round(e2e_s / args.steps * 1e3, 3)}
+    return out
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -360,8 +466,20 @@ def run_ours(args):
         e2e = {"value": round(w.flops * args.steps / e2e_s / 1e9 * world, 3), "unit": "GFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e2e_s / args.steps * 1e3, 3)}
+    main_windows = list(clocks.windows)
+    tf32x3 = None
+    if args.path == "ffma" and not args.no_tf32x3:
+        t0x = time.time()
+        tf32x3 = measure_tf32x3(args, w, binding, dA, dB, dC, C, stream, world, device)
+        tf_window = (t0x, time.time())
+        clocks.mark(*tf_window)
     clocks.stop()
-    clk = clocks.summary()
+    clk = clocks.summary(main_windows)
+    if tf32x3 is not None:
+        tclk = clocks.summary([tf_window])
+        tf32x3["clocks"] = {"sm_mhz": tclk.get("sm_mhz"), "sm_max_mhz": tclk.get("sm_max_mhz"),
+                            "reasons": tclk.get("reasons"), "samples": tclk.get("samples"),
+                            "power_w_median": tclk.get("power_w_median")}
 
     # ---- roofline of the main kernel (FP32 FFMA pipe)
     main_ms = prof["main_ms"] / max(1, prof["main_launches"])
@@ -405,6 +523,7 @@ def run_ours(args):
             "pct_of_ffma_peak": round(100.0 * gflops / world / (peak_tflops * 1e3), 2),
             "sm_count": sms,
             "roofline": roofline,
+            "tf32x3": tf32x3,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": int(launches),
