@@ -396,7 +396,7 @@ int sgemm_device_3xtf32(int M, int N, int K, float alpha, const float *A, int ld
         return cuda_fail(e);
     }
     CUtensorMap mAh, mAl, mBh, mBl;
-    const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    const auto sw = t3::ROW_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     if ((st = encode_2d(&mAh, Ah, K, M, ldk, t3::BK, t3::BM, sw)) != SGEMM_OK ||
         (st = encode_2d(&mAl, Al, K, M, ldk, t3::BK, t3::BM, sw)) != SGEMM_OK ||
         (st = encode_2d(&mBh, Bh, K, N, ldk, t3::BK, t3::BN, sw)) != SGEMM_OK ||

@@ -8,9 +8,9 @@
 //
 // Kernel layout (persistent: one CTA per SM walks 128 x 256 output tiles
 // b, b + gridDim.x, ...; 256 threads):
-//   warp 0    thread 0 issues TMA copies of A_hi, A_lo (128 x 32) and B_hi,
-//             B_lo (256 x 32, B transposed so both operands are K-major) into
-//             a 2-stage ring, 128-byte swizzled;
+//   warp 0    thread 0 issues TMA copies of A_hi, A_lo (128 x 16) and B_hi,
+//             B_lo (256 x 16, B transposed so both operands are K-major) into
+//             a 4-stage ring, 64-byte swizzled;
 //   warp 1    allocates all 512 TMEM columns (two 128 x 256 fp32
 //             accumulators); thread 32 issues tcgen05.mma (M 128, N 256, K 8)
 //             three times per 8-wide k step into the tile's accumulator and
@@ -32,7 +32,12 @@
 namespace sg {
 namespace t3 {
 
-constexpr int BM = 128, BN = 256, BK = 32, STAGES = 2;
+constexpr int BM = 128, BN = 256, BK = 16, STAGES = 4;
+// K-major operand rows of BK floats: 64 bytes, so the TMA box and the MMA
+// descriptor both use the 64-byte swizzle; 8-row groups are 8 x 64 bytes apart.
+constexpr int ROW_BYTES = BK * 4;
+static_assert(ROW_BYTES == 64 || ROW_BYTES == 128, "64- or 128-byte swizzle rows");
+constexpr uint32_t SWIZZLE_CODE = ROW_BYTES == 128 ? 2u : 4u;   // descriptor layout field
 constexpr int A_TILE = BM * BK;                       // floats, 16 KB
 constexpr int B_TILE = BN * BK;                       // floats, 32 KB
 constexpr int STAGE_FLOATS = 2 * A_TILE + 2 * B_TILE; // A_hi, A_lo, B_hi, B_lo
@@ -56,15 +61,15 @@ constexpr uint32_t IDESC = (1u << 4)                    // D format: f32
                            | (uint32_t(BN >> 3) << 17)  // N / 8
                            | (uint32_t(BM >> 4) << 24); // M / 16
 
-// Shared-memory matrix descriptor: K-major operand, rows of 128 bytes with the
-// 128-byte swizzle (the layout the TMA writes), 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+// Shared-memory matrix descriptor: K-major operand, rows of ROW_BYTES with the
+// matching swizzle (the layout the TMA writes), 8-row groups 8 rows apart.
+__device__ __forceinline__ uint64_t smem_desc_sw(uint32_t saddr) {
     uint64_t d = 0;
-    d |= uint64_t((saddr & 0x3FFFFu) >> 4);     // start address, 16-byte units
-    d |= uint64_t(1) << 16;                     // leading offset (unused for this layout)
-    d |= uint64_t(1024 >> 4) << 32;             // stride between 8-row groups
-    d |= uint64_t(1) << 46;                     // descriptor version
-    d |= uint64_t(2) << 61;                     // 128-byte swizzle
+    d |= uint64_t((saddr & 0x3FFFFu) >> 4);           // start address, 16-byte units
+    d |= uint64_t(1) << 16;                           // leading offset (unused: K fits one row)
+    d |= uint64_t((8 * ROW_BYTES) >> 4) << 32;        // stride between 8-row groups
+    d |= uint64_t(1) << 46;                           // descriptor version
+    d |= uint64_t(SWIZZLE_CODE) << 61;                // 64- or 128-byte swizzle
     return d;
 }
 
@@ -262,9 +267,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int kk = 0; kk < BK / 8; ++kk) {
                         const uint32_t off = uint32_t(kk) * 32u;   // 8 tf32 = 32 bytes along K
                         const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-                        mma_tf32(d, smem_desc_sw128(al + off), smem_desc_sw128(bh + off), acc);
-                        mma_tf32(d, smem_desc_sw128(ah + off), smem_desc_sw128(bl + off), 1u);
-                        mma_tf32(d, smem_desc_sw128(ah + off), smem_desc_sw128(bh + off), 1u);
+                        mma_tf32(d, smem_desc_sw(al + off), smem_desc_sw(bh + off), acc);
+                        mma_tf32(d, smem_desc_sw(ah + off), smem_desc_sw(bl + off), 1u);
+                        mma_tf32(d, smem_desc_sw(ah + off), smem_desc_sw(bh + off), 1u);
                     }
                     mma_commit(&empty[stage]);     // stage free once these MMAs have read it
                     if (++stage == STAGES) {
