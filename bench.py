@@ -339,7 +339,8 @@ def measure_tf32x3(args, w, binding, dA, dB, dC, C, stream, world, device):
         "ms_per_step": round(ms, 4), "entry_point": "sgemm_3xtf32",
         "roofline": {"bound": "tensor", "kernel": "sgemm_3xtf32_kernel",
                      "achieved": round(mma_tflops, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
-                     "frac": round(mma_tflops / peak, 4), "traffic": None, "peak_source": src,
+                     "frac": round(mma_tflops / peak, 4), "traffic": load_traffic(w.name + ":tf32x3"),
+                     "peak_source": src,
                      "algorithmic_flops_per_launch": 3.0 * w.flops,
                      "note": "three TF32 MMAs per fp32 product: achieved counts MMA FLOPs",
                      "main_kernel_ms": round(main_ms, 4), "split_kernels_ms": round(split_ms, 4)},
@@ -481,25 +482,40 @@ def run_ours(args):
                             "reasons": tclk.get("reasons"), "samples": tclk.get("samples"),
                             "power_w_median": tclk.get("power_w_median")}
 
-    # ---- roofline of the main kernel (FP32 FFMA pipe)
+    # ---- roofline of the main kernel
     main_ms = prof["main_ms"] / max(1, prof["main_launches"])
     pack_ms = prof["pack_ms"] / max(1, prof["pack_launches"]) if prof["pack_launches"] else 0.0
-    achieved_tflops = w.flops / (main_ms * 1e-3) / 1e12 if main_ms > 0 else None
     peak_tflops = sms * FFMA_PER_SM_PER_CLK * 2 * SM_MAX_MHZ_FALLBACK * 1e6 / 1e12
-    f_meas = clk.get("sm_mhz")
-    peak_meas = sms * FFMA_PER_SM_PER_CLK * 2 * f_meas * 1e6 / 1e12 if f_meas else None
-    roofline = {
-        "bound": "alu", "kernel": "sgemm_tma_ffma_kernel",
-        "achieved": round(achieved_tflops, 3) if achieved_tflops else None,
-        "peak": round(peak_tflops, 3), "unit": "TFLOP/s",
-        "frac": round(achieved_tflops / peak_tflops, 4) if achieved_tflops else None,
-        "traffic": load_traffic(w.name),
-        "peak_source": f"derived: {sms} SMs x 128 FFMA/clk x 2 FLOP x 2070 MHz max SM clock",
-        "frac_at_measured_clock": (round(achieved_tflops / peak_meas, 4)
-                                   if (achieved_tflops and peak_meas) else None),
-        "main_kernel_ms": round(main_ms, 4), "pack_kernels_ms": round(pack_ms, 4),
-        "algorithmic_flops_per_launch": w.flops,
-    }
+    if args.path == "ffma":
+        # FP32 FFMA pipe
+        achieved_tflops = w.flops / (main_ms * 1e-3) / 1e12 if main_ms > 0 else None
+        f_meas = clk.get("sm_mhz")
+        peak_meas = sms * FFMA_PER_SM_PER_CLK * 2 * f_meas * 1e6 / 1e12 if f_meas else None
+        roofline = {
+            "bound": "alu", "kernel": "sgemm_tma_ffma_kernel",
+            "achieved": round(achieved_tflops, 3) if achieved_tflops else None,
+            "peak": round(peak_tflops, 3), "unit": "TFLOP/s",
+            "frac": round(achieved_tflops / peak_tflops, 4) if achieved_tflops else None,
+            "traffic": load_traffic(w.name),
+            "peak_source": f"derived: {sms} SMs x 128 FFMA/clk x 2 FLOP x 2070 MHz max SM clock",
+            "frac_at_measured_clock": (round(achieved_tflops / peak_meas, 4)
+                                       if (achieved_tflops and peak_meas) else None),
+            "main_kernel_ms": round(main_ms, 4), "pack_kernels_ms": round(pack_ms, 4),
+            "algorithmic_flops_per_launch": w.flops,
+        }
+    else:
+        # TF32 tensor pipe: three MMAs per fp32 product
+        tpeak, tsrc = tensor_peak_tf32()
+        mma_tflops = 3.0 * w.flops / (main_ms * 1e-3) / 1e12 if main_ms > 0 else None
+        roofline = {
+            "bound": "tensor", "kernel": "sgemm_3xtf32_kernel",
+            "achieved": round(mma_tflops, 3) if mma_tflops else None,
+            "peak": round(tpeak, 3), "unit": "TFLOP/s",
+            "frac": round(mma_tflops / tpeak, 4) if mma_tflops else None,
+            "traffic": load_traffic(w.name + ":tf32x3"), "peak_source": tsrc,
+            "main_kernel_ms": round(main_ms, 4), "split_kernels_ms": round(pack_ms, 4),
+            "algorithmic_flops_per_launch": 3.0 * w.flops,
+        }
 
     # ---- CPU oracle baseline (rank 0 only, N = 1 only)
     cpu = None
@@ -519,7 +535,9 @@ def run_ours(args):
                        "beta": w.beta, "seed": w.seed,
                        "l2": "inputs larger than L2 (A, B, C 805 MB vs 129 MB), no flush",
                        "parallelism": "replicas" if world > 1 else "single_gpu",
-                       "kernel": binding.config_string(w.M, w.N, w.K)},
+                       "kernel": (binding.config_string(w.M, w.N, w.K) if args.path == "ffma"
+                                  else "3xtf32 tcgen05 tile=128x256x16 stages=4 persistent "
+                                       "tmem_accumulators=2 (sgemm_3xtf32)")},
             "pct_of_ffma_peak": round(100.0 * gflops / world / (peak_tflops * 1e3), 2),
             "sm_count": sms,
             "roofline": roofline,
