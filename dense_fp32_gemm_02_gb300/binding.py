@@ -33,6 +33,8 @@ lib.sgemm_noalloc.argtypes = [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]
 lib.sgemm_noalloc.restype = _i
 lib.sgemm_3xtf32.argtypes = [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]
 lib.sgemm_3xtf32.restype = _i
+lib.sgemm_host_3xtf32.argtypes = [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]
+lib.sgemm_host_3xtf32.restype = _i
 lib.sgemm_status_string.argtypes = [_i]
 lib.sgemm_status_string.restype = ctypes.c_char_p
 lib.sgemm_version.argtypes = []
@@ -189,9 +191,12 @@ def sgemm(A, B, C=None, alpha: float = 1.0, beta: float = 0.0, stream=None):
     return sgemm_into(A, B, C, alpha, beta, stream)
 
 
-def sgemm_host(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None, device=None):
+def sgemm_host(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None, device=None,
+               tensor_cores: bool = False):
     """The host-buffer entry point: A, B, C are CPU float32 tensors (pinned for
-    speed).  C is overwritten with alpha*A@B + beta*C; synchronous."""
+    speed).  C is overwritten with alpha*A@B + beta*C; synchronous.  Copies and
+    compute are pipelined over row blocks.  tensor_cores=True uses the 3xTF32
+    path (sgemm_host_3xtf32)."""
     import torch
     for name, t in (("A", A), ("B", B), ("C", C)):
         if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.is_cuda:
@@ -199,10 +204,10 @@ def sgemm_host(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None, devi
     M, N, K = _shapes(A, B, C)
     device = torch.device(device) if device is not None else \
         torch.device("cuda", torch.cuda.current_device())
+    fn = lib.sgemm_host_3xtf32 if tensor_cores else lib.sgemm_host
     with torch.cuda.device(device):
-        st = lib.sgemm_host(M, N, K, float(alpha), A.data_ptr(), _ld(A, K), B.data_ptr(),
-                            _ld(B, N), float(beta), C.data_ptr(), _ld(C, N),
-                            _stream_handle(stream, device))
+        st = fn(M, N, K, float(alpha), A.data_ptr(), _ld(A, K), B.data_ptr(), _ld(B, N),
+                float(beta), C.data_ptr(), _ld(C, N), _stream_handle(stream, device))
     check(st)
     return C
 

@@ -357,53 +357,42 @@ int sgemm_device(int M, int N, int K, float alpha, const float *A, int lda, cons
     return SGEMM_OK;
 }
 
-// The 3xTF32 tensor-core path: split A and B into tf32 hi/lo parts (B
-// transposed), then one CTA per 128 x 256 tile runs three TF32 MMAs per k step.
-int sgemm_device_3xtf32(int M, int N, int K, float alpha, const float *A, int lda,
-                        const float *B, int ldb, float beta, float *C, int ldc,
-                        cudaStream_t stream) {
-    int st = checked_args(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta);
-    if (st != SGEMM_OK || M == 0 || N == 0) return st;
-    DeviceState *dev = nullptr;
-    if ((st = device_state(&dev)) != SGEMM_OK) return st;
-    if (K == 0 || alpha == 0.0f) return launch_scale(stream, C, ldc, M, N, beta, dev->sm_count);
+// ------------------------------------------------------------------ 3xTF32 path
+// Split A and B into tf32 hi/lo parts (B transposed, both K-major), then one
+// persistent CTA per SM runs three TF32 MMAs per k step (tf32x3.cuh).
 
+// Bh, Bl (N x ldk each): B split and transposed.
+int t3_split_b(int N, int K, const float *B, int ldb, float *Bh, float *Bl, long long ldk,
+               cudaStream_t stream) {
+    dim3 gb(unsigned(std::min<long long>((N + 63) / 64, 1LL << 20)),
+            unsigned(std::min<long long>((K + 63) / 64, 65535)));
+    sg::t3::split_bt_kernel<<<gb, 256, 0, stream>>>(B, ldb, K, N, Bh, Bl, ldk);
+    g_launches.fetch_add(1);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SGEMM_OK : cuda_fail(e);
+}
+
+// C = alpha*A*B + beta*C with B already split (Bh, Bl); Ah, Al: M x ldk scratch.
+int t3_run(int M, int N, int K, float alpha, const float *A, int lda, const float *Bh,
+           const float *Bl, long long ldk, float beta, float *C, int ldc, float *Ah, float *Al,
+           int sm_count, cudaStream_t stream) {
     namespace t3 = sg::t3;
-    const long long ldk = round_up(K, 4);
-    const size_t a_bytes = round_up((long long)M * ldk * 4, 256);
-    const size_t b_bytes = round_up((long long)N * ldk * 4, 256);
-    void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, 2 * a_bytes + 2 * b_bytes, dev->pool, stream);
-    if (e != cudaSuccess) return cuda_fail(e);
-    char *w = static_cast<char *>(ws);
-    float *Ah = reinterpret_cast<float *>(w);
-    float *Al = reinterpret_cast<float *>(w + a_bytes);
-    float *Bh = reinterpret_cast<float *>(w + 2 * a_bytes);
-    float *Bl = reinterpret_cast<float *>(w + 2 * a_bytes + b_bytes);
+    int st;
     {
-        ProfScope prof(stream, false);
         const int vec4 = (aligned16(A) && lda % 4 == 0 && K % 4 == 0) ? 1 : 0;
         dim3 ga(unsigned(std::min<long long>((K + 4095) / 4096, 64)), unsigned(std::min(M, 65535)));
         t3::split_a_kernel<<<ga, 256, 0, stream>>>(A, lda, M, K, Ah, Al, ldk, vec4);
-        dim3 gb(unsigned(std::min<long long>((N + 63) / 64, 1LL << 20)),
-                unsigned(std::min<long long>((K + 63) / 64, 65535)));
-        t3::split_bt_kernel<<<gb, 256, 0, stream>>>(B, ldb, K, N, Bh, Bl, ldk);
-        g_launches.fetch_add(2);
+        g_launches.fetch_add(1);
     }
-    e = cudaGetLastError();
-    if (e != cudaSuccess) {
-        cudaFreeAsync(ws, stream);
-        return cuda_fail(e);
-    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
     CUtensorMap mAh, mAl, mBh, mBl;
     const auto sw = t3::ROW_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     if ((st = encode_2d(&mAh, Ah, K, M, ldk, t3::BK, t3::BM, sw)) != SGEMM_OK ||
         (st = encode_2d(&mAl, Al, K, M, ldk, t3::BK, t3::BM, sw)) != SGEMM_OK ||
         (st = encode_2d(&mBh, Bh, K, N, ldk, t3::BK, t3::BN, sw)) != SGEMM_OK ||
-        (st = encode_2d(&mBl, Bl, K, N, ldk, t3::BK, t3::BN, sw)) != SGEMM_OK) {
-        cudaFreeAsync(ws, stream);
+        (st = encode_2d(&mBl, Bl, K, N, ldk, t3::BK, t3::BN, sw)) != SGEMM_OK)
         return st;
-    }
     t3::Params p;
     p.C = C;
     p.ldc = ldc;
@@ -417,11 +406,8 @@ int sgemm_device_3xtf32(int M, int N, int K, float alpha, const float *A, int ld
     p.group_m = 8;
     p.timeout_ns = g_timeout_ns.load();
     const long long tiles = (long long)p.tiles_m * p.tiles_n;
-    if (tiles > 0x7fffffffLL) {
-        cudaFreeAsync(ws, stream);
-        return SGEMM_ERR_INVALID_ARG;
-    }
-    const unsigned grid = unsigned(std::min<long long>(tiles, dev->sm_count));
+    if (tiles > 0x7fffffffLL) return SGEMM_ERR_INVALID_ARG;
+    const unsigned grid = unsigned(std::min<long long>(tiles, sm_count));
     {
         ProfScope prof(stream, true);
         t3::sgemm_3xtf32_kernel<<<grid, t3::THREADS, t3::SMEM_BYTES, stream>>>(mAh, mAl, mBh,
@@ -429,10 +415,188 @@ int sgemm_device_3xtf32(int M, int N, int K, float alpha, const float *A, int ld
         g_launches.fetch_add(1);
     }
     e = cudaGetLastError();
-    cudaError_t ef = cudaFreeAsync(ws, stream);
+    return e == cudaSuccess ? SGEMM_OK : cuda_fail(e);
+}
+
+int sgemm_device_3xtf32(int M, int N, int K, float alpha, const float *A, int lda,
+                        const float *B, int ldb, float beta, float *C, int ldc,
+                        cudaStream_t stream) {
+    int st = checked_args(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta);
+    if (st != SGEMM_OK || M == 0 || N == 0) return st;
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != SGEMM_OK) return st;
+    if (K == 0 || alpha == 0.0f) return launch_scale(stream, C, ldc, M, N, beta, dev->sm_count);
+
+    const long long ldk = round_up(K, 4);
+    const size_t a_bytes = round_up((long long)M * ldk * 4, 256);
+    const size_t b_bytes = round_up((long long)N * ldk * 4, 256);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, 2 * a_bytes + 2 * b_bytes, dev->pool, stream);
     if (e != cudaSuccess) return cuda_fail(e);
+    char *w = static_cast<char *>(ws);
+    float *Ah = reinterpret_cast<float *>(w);
+    float *Al = reinterpret_cast<float *>(w + a_bytes);
+    float *Bh = reinterpret_cast<float *>(w + 2 * a_bytes);
+    float *Bl = reinterpret_cast<float *>(w + 2 * a_bytes + b_bytes);
+    {
+        ProfScope prof(stream, false);
+        st = t3_split_b(N, K, B, ldb, Bh, Bl, ldk, stream);
+    }
+    if (st == SGEMM_OK)
+        st = t3_run(M, N, K, alpha, A, lda, Bh, Bl, ldk, beta, C, ldc, Ah, Al, dev->sm_count,
+                    stream);
+    cudaError_t ef = cudaFreeAsync(ws, stream);
+    if (st != SGEMM_OK) return st;
     if (ef != cudaSuccess) return cuda_fail(ef);
     return SGEMM_OK;
+}
+
+// ------------------------------------------------------------------ host buffers
+// Copy streams of a device, created on first use: one for host->device copies,
+// one for device->host copies, so both directions of the host link and the
+// GEMM on the caller's stream run at the same time.
+struct CopyStreams {
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+};
+CopyStreams g_copy_streams[kMaxDevices];
+
+int copy_streams(CopyStreams **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    CopyStreams &c = g_copy_streams[dev];
+    if (!c.h2d) {
+        if ((e = cudaStreamCreateWithFlags(&c.h2d, cudaStreamNonBlocking)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaStreamCreateWithFlags(&c.d2h, cudaStreamNonBlocking)) != cudaSuccess)
+            return cuda_fail(e);
+    }
+    *out = &c;
+    return SGEMM_OK;
+}
+
+struct EventSet {
+    std::vector<cudaEvent_t> ev;
+    cudaEvent_t make() {
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+        ev.push_back(e);
+        return e;
+    }
+    ~EventSet() {
+        for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    }
+};
+
+// The host-buffer GEMM, pipelined over row blocks of A and C: B goes in first;
+// then block i of A (and of C when beta != 0) is copied in on the h2d stream,
+// multiplied on the caller's stream while block i+1 is copied in, and copied
+// back on the d2h stream while block i+1 is multiplied.  `tensor` selects the
+// 3xTF32 path (B is split once, each block of A is split with its GEMM).
+int host_gemm(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
+              float beta, float *C, int ldc, cudaStream_t stream, bool tensor) {
+    int st = checked_args(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta);
+    if (st != SGEMM_OK || M == 0 || N == 0) return st;
+    DeviceState *dev = nullptr;
+    if ((st = device_state(&dev)) != SGEMM_OK) return st;
+    CopyStreams *cs = nullptr;
+    if ((st = copy_streams(&cs)) != SGEMM_OK) return st;
+
+    const bool need_ab = (K > 0 && alpha != 0.0f);
+    const bool need_c_in = (beta != 0.0f);
+    const long long ldk = round_up(std::max(K, 1), 4);
+    // row blocks: about 1024 rows or more, at most 8 blocks
+    const int nblk = need_ab ? std::max(1, std::min(8, M / 1024)) : 1;
+    const int rows_per_blk = (M + nblk - 1) / nblk;
+
+    const size_t a_bytes = need_ab ? round_up((long long)M * K * 4, 256) : 0;
+    const size_t b_bytes = need_ab ? round_up((long long)K * N * 4, 256) : 0;
+    const size_t c_bytes = round_up((long long)M * N * 4, 256);
+    // 3xTF32: split parts of B (2 x N x ldk) and of the largest block of A
+    const size_t bs_bytes = (need_ab && tensor) ? round_up((long long)N * ldk * 4, 256) : 0;
+    const size_t as_bytes = (need_ab && tensor) ? round_up((long long)rows_per_blk * ldk * 4, 256) : 0;
+    const size_t total = a_bytes + b_bytes + c_bytes + 2 * bs_bytes + 2 * as_bytes;
+    void *buf = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&buf, total, dev->pool, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    char *base = static_cast<char *>(buf);
+    float *dA = reinterpret_cast<float *>(base);
+    float *dB = reinterpret_cast<float *>(base + a_bytes);
+    float *dC = reinterpret_cast<float *>(base + a_bytes + b_bytes);
+    float *Bh = reinterpret_cast<float *>(base + a_bytes + b_bytes + c_bytes);
+    float *Bl = Bh + bs_bytes / 4;
+    float *Ah = reinterpret_cast<float *>(base + a_bytes + b_bytes + c_bytes + 2 * bs_bytes);
+    float *Al = Ah + as_bytes / 4;
+
+    EventSet evs;
+    auto fail = [&](int code) {
+        cudaStreamSynchronize(cs->h2d);
+        cudaStreamSynchronize(cs->d2h);
+        cudaFreeAsync(buf, stream);
+        cudaStreamSynchronize(stream);
+        return code;
+    };
+    cudaEvent_t allocated = evs.make(), b_ready = evs.make(), done = evs.make();
+    if (!allocated || !b_ready || !done) return fail(SGEMM_ERR_CUDA);
+    // the copy streams may touch the buffer only after its allocation on `stream`
+    if ((e = cudaEventRecord(allocated, stream)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(cs->h2d, allocated, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(cs->d2h, allocated, 0)) != cudaSuccess)
+        return fail(cuda_fail(e));
+    if (need_ab) {
+        e = cudaMemcpy2DAsync(dB, size_t(N) * 4, B, size_t(ldb) * 4, size_t(N) * 4, size_t(K),
+                              cudaMemcpyHostToDevice, cs->h2d);
+        if (e == cudaSuccess) e = cudaEventRecord(b_ready, cs->h2d);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, b_ready, 0);
+        if (e != cudaSuccess) return fail(cuda_fail(e));
+        if (tensor && (st = t3_split_b(N, K, dB, N, Bh, Bl, ldk, stream)) != SGEMM_OK)
+            return fail(st);
+    }
+    for (int blk = 0; blk < nblk; ++blk) {
+        const int r0 = blk * rows_per_blk;
+        const int rows = std::min(rows_per_blk, M - r0);
+        if (rows <= 0) break;
+        cudaEvent_t in = evs.make(), out = evs.make();
+        if (!in || !out) return fail(SGEMM_ERR_CUDA);
+        e = cudaSuccess;
+        if (need_ab)
+            e = cudaMemcpy2DAsync(dA + (size_t)r0 * K, size_t(K) * 4, A + (size_t)r0 * lda,
+                                  size_t(lda) * 4, size_t(K) * 4, size_t(rows),
+                                  cudaMemcpyHostToDevice, cs->h2d);
+        if (e == cudaSuccess && need_c_in)
+            e = cudaMemcpy2DAsync(dC + (size_t)r0 * N, size_t(N) * 4, C + (size_t)r0 * ldc,
+                                  size_t(ldc) * 4, size_t(N) * 4, size_t(rows),
+                                  cudaMemcpyHostToDevice, cs->h2d);
+        if (e == cudaSuccess) e = cudaEventRecord(in, cs->h2d);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, in, 0);
+        if (e != cudaSuccess) return fail(cuda_fail(e));
+        const float *a_blk = need_ab ? dA + (size_t)r0 * K : nullptr;
+        float *c_blk = dC + (size_t)r0 * N;
+        if (!need_ab)
+            st = sgemm_device(rows, N, K, alpha, nullptr, std::max(1, K), nullptr, std::max(1, N),
+                              beta, c_blk, N, stream);
+        else if (tensor)
+            st = t3_run(rows, N, K, alpha, a_blk, K, Bh, Bl, ldk, beta, c_blk, N, Ah, Al,
+                        dev->sm_count, stream);
+        else
+            st = sgemm_device(rows, N, K, alpha, a_blk, K, dB, N, beta, c_blk, N, stream);
+        if (st != SGEMM_OK) return fail(st);
+        e = cudaEventRecord(out, stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(cs->d2h, out, 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(C + (size_t)r0 * ldc, size_t(ldc) * 4, c_blk, size_t(N) * 4,
+                                  size_t(N) * 4, size_t(rows), cudaMemcpyDeviceToHost, cs->d2h);
+        if (e != cudaSuccess) return fail(cuda_fail(e));
+    }
+    // the buffer is freed only after the last copy back
+    if ((e = cudaEventRecord(done, cs->d2h)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(stream, done, 0)) != cudaSuccess)
+        return fail(cuda_fail(e));
+    cudaFreeAsync(buf, stream);
+    e = cudaStreamSynchronize(stream);
+    return e == cudaSuccess ? SGEMM_OK : cuda_fail(e);
 }
 
 int read_and_clear_error_word(cudaStream_t stream) {
@@ -580,55 +744,16 @@ SGEMM_API int sgemm(int M, int N, int K, float alpha, const float *A, int lda, c
 
 SGEMM_API int sgemm_host(int M, int N, int K, float alpha, const float *A, int lda,
                          const float *B, int ldb, float beta, float *C, int ldc,
-                         sgemm_stream_t stream_) {
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    int st = checked_args(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta);
-    if (st != SGEMM_OK || M == 0 || N == 0) return st;
-    DeviceState *dev = nullptr;
-    if ((st = device_state(&dev)) != SGEMM_OK) return st;
+                         sgemm_stream_t stream) {
+    return host_gemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                     reinterpret_cast<cudaStream_t>(stream), false);
+}
 
-    const bool need_ab = (K > 0 && alpha != 0.0f);
-    const bool need_c_in = (beta != 0.0f);
-    const size_t a_bytes = need_ab ? size_t(M) * K * sizeof(float) : 0;
-    const size_t b_bytes = need_ab ? size_t(K) * N * sizeof(float) : 0;
-    const size_t c_bytes = size_t(M) * N * sizeof(float);
-    const size_t off_b = size_t(round_up((long long)a_bytes, 256));
-    const size_t off_c = off_b + size_t(round_up((long long)b_bytes, 256));
-    void *buf = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&buf, off_c + c_bytes, dev->pool, stream);
-    if (e != cudaSuccess) return cuda_fail(e);
-    char *base = static_cast<char *>(buf);
-    float *dA = reinterpret_cast<float *>(base);
-    float *dB = reinterpret_cast<float *>(base + off_b);
-    float *dC = reinterpret_cast<float *>(base + off_c);
-
-    if (need_ab) {
-        e = cudaMemcpy2DAsync(dA, size_t(K) * sizeof(float), A, size_t(lda) * sizeof(float),
-                              size_t(K) * sizeof(float), size_t(M), cudaMemcpyHostToDevice, stream);
-        if (e == cudaSuccess)
-            e = cudaMemcpy2DAsync(dB, size_t(N) * sizeof(float), B, size_t(ldb) * sizeof(float),
-                                  size_t(N) * sizeof(float), size_t(K), cudaMemcpyHostToDevice,
-                                  stream);
-    }
-    if (e == cudaSuccess && need_c_in)
-        e = cudaMemcpy2DAsync(dC, size_t(N) * sizeof(float), C, size_t(ldc) * sizeof(float),
-                              size_t(N) * sizeof(float), size_t(M), cudaMemcpyHostToDevice, stream);
-    if (e != cudaSuccess) {
-        cudaFreeAsync(buf, stream);
-        cudaStreamSynchronize(stream);
-        return cuda_fail(e);
-    }
-    st = sgemm_device(M, N, K, alpha, need_ab ? dA : nullptr, std::max(1, K),
-                      need_ab ? dB : nullptr, std::max(1, N), beta, dC, N, stream);
-    if (st == SGEMM_OK) {
-        e = cudaMemcpy2DAsync(C, size_t(ldc) * sizeof(float), dC, size_t(N) * sizeof(float),
-                              size_t(N) * sizeof(float), size_t(M), cudaMemcpyDeviceToHost, stream);
-        if (e != cudaSuccess) st = cuda_fail(e);
-    }
-    cudaFreeAsync(buf, stream);
-    e = cudaStreamSynchronize(stream);
-    if (st == SGEMM_OK && e != cudaSuccess) st = cuda_fail(e);
-    return st;
+SGEMM_API int sgemm_host_3xtf32(int M, int N, int K, float alpha, const float *A, int lda,
+                                const float *B, int ldb, float beta, float *C, int ldc,
+                                sgemm_stream_t stream) {
+    return host_gemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                     reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 SGEMM_API const char *sgemm_status_string(int status) {

@@ -75,10 +75,16 @@ int sgemm(int M, int N, int K, float alpha,
  * sgemm_host -- the same GEMM on HOST buffers; synchronous.
  *
  * A, B, C are host pointers (page-locked memory gives the fastest copies, but
- * pageable memory is accepted).  The call copies A and B (and C when beta != 0)
- * to device buffers taken from the library pool, runs sgemm() on `stream`,
- * copies the M x N result back into C (respecting ldc) and synchronises
- * `stream` before returning, so C holds the result on return.
+ * pageable memory is accepted).  The call copies B to the device, then works
+ * through row blocks of A and C (up to 8 blocks of at least 1024 rows): block
+ * i is copied in on a host-to-device copy stream, multiplied on `stream` while
+ * block i+1 is copied in, and copied back into C (respecting ldc) on a
+ * device-to-host copy stream while block i+1 is multiplied.  Device buffers
+ * come from the library pool; the two copy streams are the library's own (one
+ * pair per device).  `stream` is synchronised before returning, so C holds
+ * the result on return.  Results meet the same tolerance as sgemm(); when the
+ * rows are split into blocks they need not be bitwise equal to one sgemm() call
+ * on the whole matrix (the k split of leftover tiles depends on the shape).
  */
 int sgemm_host(int M, int N, int K, float alpha,
                const float *A, int lda,
@@ -104,6 +110,18 @@ int sgemm_3xtf32(int M, int N, int K, float alpha,
                  const float *B, int ldb,
                  float beta, float *C, int ldc,
                  sgemm_stream_t stream);
+
+/*
+ * sgemm_host_3xtf32 -- sgemm_host() through the 3xTF32 tensor-core path: B is
+ * split once on the device, each row block of A is split and multiplied as
+ * in sgemm_3xtf32().  Same arguments, pipelining and synchronisation as
+ * sgemm_host(); same tolerance as sgemm_3xtf32().
+ */
+int sgemm_host_3xtf32(int M, int N, int K, float alpha,
+                      const float *A, int lda,
+                      const float *B, int ldb,
+                      float beta, float *C, int ldc,
+                      sgemm_stream_t stream);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char *sgemm_status_string(int status);
