@@ -418,8 +418,11 @@ def run_ours(args):
     torch.cuda.synchronize()
     t0 = time.time()
     start.record(stream)
-    for _ in range(args.steps):
+    # one event after every step as well: per-call median and minimum
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
         step()
+        marks[i].record(stream)
     stop.record(stream)
     stop.synchronize()
     torch.cuda.synchronize()
@@ -436,6 +439,10 @@ def run_ours(args):
 
     ms_per_step = ms / args.steps
     gflops = aggregate_gflops(w.flops, ms_per_step, world)
+    per_call = [start.elapsed_time(marks[0])] + \
+        [marks[i - 1].elapsed_time(marks[i]) for i in range(1, args.steps)]
+    per_call_median = statistics.median(per_call)
+    per_call_min = min(per_call)
 
     # ---- end to end through the host-buffer entry point
     e2e = None
@@ -479,6 +486,8 @@ def run_ours(args):
     main_ms = prof["main_ms"] / max(1, prof["main_launches"])
     pack_ms = prof["pack_ms"] / max(1, prof["pack_launches"]) if prof["pack_launches"] else 0.0
     peak_tflops = sms * FFMA_PER_SM_PER_CLK * 2 * SM_MAX_MHZ_FALLBACK * 1e6 / 1e12
+    peak_meas_clk = (sms * FFMA_PER_SM_PER_CLK * 2 * clk["sm_mhz"] * 1e6 / 1e12
+                     if clk.get("sm_mhz") else None)
     if args.path == "ffma":
         # FP32 FFMA pipe
         achieved_tflops = w.flops / (main_ms * 1e-3) / 1e12 if main_ms > 0 else None
@@ -532,6 +541,12 @@ def run_ours(args):
                                   else "3xtf32 tcgen05 tile=128x256x16 stages=4 persistent "
                                        "tmem_accumulators=2 (sgemm_3xtf32)")},
             "pct_of_ffma_peak": round(100.0 * gflops / world / (peak_tflops * 1e3), 2),
+            "pct_of_ffma_peak_at_measured_clock": (
+                round(100.0 * gflops / world / (peak_meas_clk * 1e3), 2) if peak_meas_clk else None),
+            "per_call": {"median_ms": round(per_call_median, 4), "min_ms": round(per_call_min, 4),
+                         "gflops_at_median": round(w.flops / (per_call_median * 1e-3) / 1e9, 3),
+                         "gflops_at_min": round(w.flops / (per_call_min * 1e-3) / 1e9, 3),
+                         "calls": len(per_call)},
             "sm_count": sms,
             "roofline": roofline,
             "tf32x3": tf32x3,

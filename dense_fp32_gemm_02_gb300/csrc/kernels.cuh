@@ -51,12 +51,19 @@ enum Micro : int {
                        //   (c[i][j], c[i+1][j]) += (a[i], a[i+1]) * (b[j], b[j])
 };
 
+// Who issues the TMA copies of the k-slabs.
+enum Issue : int {
+    ISSUE_THREAD0 = 0,       // consumer thread 0, at the start of each of its slabs
+    ISSUE_PRODUCER_WG = 1,   // a producer warpgroup in front of the consumer warps
+    ISSUE_LAST_WARP = 2,     // the consumer warp that releases a stage last refills it
+};
+
 // Lanes of a warp form a LANES_M x LANES_N = 4 x 8 grid.  A thread owns a
 // TM x TN tile made of (TM/4) x (TN/4) sub-tiles of 4x4 spaced 16 rows and 32
 // columns apart, so a warp covers (4*TM) x (8*TN) outputs and every fragment
 // load is one 128-bit shared load of four consecutive floats.
 template <int BM_, int BN_, int BK_, int STAGES_, int WARPS_M_, int WARPS_N_, int TM_, int TN_,
-          int MICRO_, bool WS_>
+          int MICRO_, int ISSUE_>
 struct TileConfig {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_;
@@ -66,9 +73,8 @@ struct TileConfig {
     static constexpr int WM = TM * LANES_M, WN = TN * LANES_N;
     static constexpr int CONSUMER_WARPS = WARPS_M * WARPS_N;
     static constexpr int CONSUMER_THREADS = CONSUMER_WARPS * 32;
-    // WS: a producer warpgroup in front of the consumer warps issues the TMA
-    // copies; otherwise consumer thread 0 issues them between its own slabs.
-    static constexpr bool WS = WS_;
+    static constexpr int ISSUE = ISSUE_;
+    static constexpr bool WS = ISSUE_ == ISSUE_PRODUCER_WG;
     static constexpr int PRODUCER_THREADS = WS ? 128 : 0;
     static constexpr int THREADS = PRODUCER_THREADS + CONSUMER_THREADS;
     // Register split (setmaxnreg, WS only): the launch gives every thread
@@ -409,11 +415,23 @@ __device__ __forceinline__ void sum_pieces_row(float (&row)[Cfg::TN], const floa
 }
 
 // ------------------------------------------------------------------ main kernel
-// Shared-memory ring and flags of one CTA.
+// Shared-memory ring and flags of one CTA, addressed by 32-bit shared-window
+// addresses that all derive from one base register:
+//   [ A stages | B stages | full barriers | empty barriers | abort flag ].
+template <class Cfg>
 struct Ring {
-    float *sA, *sB;
-    uint64_t *full, *empty;
-    volatile int *abort_flag;
+    uint32_t base;
+    static constexpr uint32_t B_OFF = uint32_t(Cfg::STAGES * Cfg::A_STAGE) * 4u;
+    static constexpr uint32_t BAR_OFF = B_OFF + uint32_t(Cfg::STAGES * Cfg::B_STAGE) * 4u;
+    static constexpr uint32_t BYTES = BAR_OFF + 16u * Cfg::STAGES + 16u;
+
+    __device__ uint32_t a(int s) const { return base + uint32_t(s * Cfg::A_STAGE) * 4u; }
+    __device__ uint32_t b(int s) const { return base + B_OFF + uint32_t(s * Cfg::B_STAGE) * 4u; }
+    __device__ uint32_t full(int s) const { return base + BAR_OFF + 8u * s; }
+    __device__ uint32_t empty(int s) const { return base + BAR_OFF + 8u * (Cfg::STAGES + s); }
+    __device__ uint32_t abort_flag() const { return base + BAR_OFF + 16u * Cfg::STAGES; }
+    __device__ bool aborted() const { return ld_shared_flag(abort_flag()) != 0; }
+    __device__ void set_abort() const { st_shared_flag(abort_flag(), 1); }
 };
 
 // State of the TMA issuer: the next slab to copy is slab `slab` of segment
@@ -438,10 +456,10 @@ struct IssueState {
 // Issue the copies of the next slab.  Returns false when there is none left or
 // the wait for the stage to be released expired (abort).
 template <class Cfg>
-__device__ __forceinline__ bool issue_one(IssueState &st, const Ring &ring,
+__device__ __forceinline__ bool issue_one(IssueState &st, const Ring<Cfg> &ring,
                                           const CUtensorMap *tmA, const CUtensorMap *tmB,
                                           const MainParams &p, int k_tiles) {
-    if (*ring.abort_flag) return false;
+    if (ring.aborted()) return false;
     if (!st.have) {
         Segment sg;
         if (!st.iter.next(p, k_tiles, sg)) return false;
@@ -456,14 +474,14 @@ __device__ __forceinline__ bool issue_one(IssueState &st, const Ring &ring,
     const int s = st.stage;
     // first use of a stage: parity 1 refers to the phase before the barrier's
     // first one and counts as complete
-    if (!mbar_wait(&ring.empty[s], st.phase ^ 1u, p.timeout_ns)) {
+    if (!mbar_wait_at(ring.empty(s), st.phase ^ 1u, p.timeout_ns)) {
         atomicOr(&g_error_word, ERR_EMPTY_WAIT);
-        *ring.abort_flag = 1;
+        ring.set_abort();
         return false;
     }
-    mbar_arrive_expect_tx(&ring.full[s], Cfg::STAGE_BYTES);
-    tma_load_2d(ring.sA + s * Cfg::A_STAGE, tmA, &ring.full[s], st.tm * Cfg::BM, st.slab * Cfg::BK);
-    tma_load_2d(ring.sB + s * Cfg::B_STAGE, tmB, &ring.full[s], st.tn * Cfg::BN, st.slab * Cfg::BK);
+    mbar_arrive_expect_tx_at(ring.full(s), Cfg::STAGE_BYTES);
+    tma_load_2d_at(ring.a(s), tmA, ring.full(s), st.tm * Cfg::BM, st.slab * Cfg::BK);
+    tma_load_2d_at(ring.b(s), tmB, ring.full(s), st.tn * Cfg::BN, st.slab * Cfg::BK);
     st.issued = st.issued + 1;
     if (s + 1 == Cfg::STAGES) {
         st.stage = 0;
@@ -478,11 +496,12 @@ __device__ __forceinline__ bool issue_one(IssueState &st, const Ring &ring,
 // After an abort: wait (bounded) for the last copies issued, so none is still
 // writing shared memory when the CTA exits.
 template <class Cfg>
-__device__ __forceinline__ void drain_copies(const Ring &ring, long long issued, const MainParams &p) {
+__device__ __forceinline__ void drain_copies(const Ring<Cfg> &ring, long long issued,
+                                             const MainParams &p) {
     const long long first = issued > Cfg::STAGES ? issued - Cfg::STAGES : 0;
     for (long long q = first; q < issued; ++q) {
         const int s = int(q % Cfg::STAGES);
-        if (!mbar_wait(&ring.full[s], uint32_t((q / Cfg::STAGES) & 1), p.timeout_ns)) {
+        if (!mbar_wait_at(ring.full(s), uint32_t((q / Cfg::STAGES) & 1), p.timeout_ns)) {
             atomicOr(&g_error_word, ERR_DRAIN_WAIT);
             break;
         }
@@ -502,45 +521,55 @@ struct FixInfo {
 };
 
 // The consumer warps: FFMA micro-tiles over the ring, stream-K fixup and the
-// epilogue.  `before_slab` runs at the start of every slab (the issuer hook of
-// the non-warp-specialised kernel).
-template <class Cfg, class Hook>
-__device__ __forceinline__ void consumer_loop(const Ring &ring, const MainParams &p, int k_tiles,
-                                              int cw, int ctid, FixInfo &fix, Hook &&before_slab) {
+// epilogue.  `before_slab` runs before the wait for every slab (the issuer
+// hook of ISSUE_THREAD0); `after_release(s)` runs on lane 0 of every warp
+// right after the warp released stage s (the issuer hook of ISSUE_LAST_WARP).
+//
+// Register budget: the accumulators and two fragment buffers take TM*TN +
+// 2*(TM+TN) registers for the whole main loop, so little else stays live
+// across it: the ring is one base address, and the segment's tile, slot and
+// stream-K constants are fetched again after the loop instead of being kept.
+template <class Cfg, class Hook, class Release>
+__device__ __forceinline__ void consumer_loop(const Ring<Cfg> &ring, const MainParams &p,
+                                              int k_tiles, int cw, int ctid, FixInfo &fix,
+                                              Hook &&before_slab, Release &&after_release) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int TM = Cfg::TM, TN = Cfg::TN;
     constexpr int BAR_CONSUMERS = 1;
     const int lane = threadIdx.x & 31;
-    const int wm0 = (cw % Cfg::WARPS_M) * Cfg::WM;
-    const int wn0 = (cw / Cfg::WARPS_M) * Cfg::WN;
     // zig-zag lane map: lane bits {1,4} -> row group, bits {0,2,3} -> column group
-    const int lm = ((lane >> 1) & 1) | ((lane >> 3) & 2);
-    const int ln = (lane & 1) | ((lane >> 1) & 6);
-    const int a_off = wm0 + lm * 4;
-    const int b_off = wn0 + ln * 4;
-    // sk_start(b + 1) = sk_start(b) + sk_q + carry, carry from sk_r: additions only
-    const long long sk_q = p.sk_slabs / gridDim.x;
-    const int sk_r = int(p.sk_slabs % gridDim.x);
-    const uint32_t sA_addr = smem_addr(ring.sA), sB_addr = smem_addr(ring.sB);
+    auto a_off = [&] {
+        return (cw % Cfg::WARPS_M) * Cfg::WM + (((lane >> 1) & 1) | ((lane >> 3) & 2)) * 4;
+    };
+    auto b_off = [&] {
+        return (cw / Cfg::WARPS_M) * Cfg::WN + ((lane & 1) | ((lane >> 1) & 6)) * 4;
+    };
+    // this thread's fragment addresses in stage 0; stage s adds s times the stage size
+    const uint32_t a_base = ring.a(0) + uint32_t(a_off()) * 4u;
+    const uint32_t b_base = ring.b(0) + uint32_t(b_off()) * 4u;
 
     int stage = 0;          // stage of the next slab to consume
     uint32_t phase = 0;     // parity of that stage's full barrier
     for (int si = 0;; ++si) {
-        Segment seg;
-        if (!segment_at(p, k_tiles, si, seg)) break;
-        int tm, tn;
-        tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-        if (seg.slot >= 0 && ctid == 0) {
-            const long long rel = seg.tile - p.dp_tiles;
-            fix.tile_start = rel * k_tiles;
-            fix.b_lo = sk_owner(fix.tile_start, p.sk_slabs, gridDim.x);
-            fix.b_hi = sk_owner(fix.tile_start + k_tiles - 1, p.sk_slabs, gridDim.x);
-            fix.q0 = sk_start(fix.b_lo, p.sk_slabs, gridDim.x);
-            fix.r0 = int(((long long)fix.b_lo * p.sk_slabs) % gridDim.x);
-            int pieces = 0;
-            for (int b = fix.b_lo; b <= fix.b_hi; ++b)
-                pieces += sk_start(b, p.sk_slabs, gridDim.x) < sk_start(b + 1, p.sk_slabs, gridDim.x);
-            fix.pieces = pieces;
+        int nslabs, slot;
+        {
+            Segment seg;
+            if (!segment_at(p, k_tiles, si, seg)) break;
+            nslabs = seg.ke - seg.kb;
+            slot = seg.slot;
+            if (slot >= 0 && ctid == 0) {
+                const long long rel = seg.tile - p.dp_tiles;
+                fix.tile_start = rel * k_tiles;
+                fix.b_lo = sk_owner(fix.tile_start, p.sk_slabs, gridDim.x);
+                fix.b_hi = sk_owner(fix.tile_start + k_tiles - 1, p.sk_slabs, gridDim.x);
+                fix.q0 = sk_start(fix.b_lo, p.sk_slabs, gridDim.x);
+                fix.r0 = int(((long long)fix.b_lo * p.sk_slabs) % gridDim.x);
+                int pieces = 0;
+                for (int b = fix.b_lo; b <= fix.b_hi; ++b)
+                    pieces +=
+                        sk_start(b, p.sk_slabs, gridDim.x) < sk_start(b + 1, p.sk_slabs, gridDim.x);
+                fix.pieces = pieces;
+            }
         }
 
         float acc[TM][TN];
@@ -549,25 +578,23 @@ __device__ __forceinline__ void consumer_loop(const Ring &ring, const MainParams
 #pragma unroll
             for (int jj = 0; jj < TN; ++jj) acc[i][jj] = 0.0f;
 
-        const int slot = seg.slot;
-        const int rel_tile = seg.tile - p.dp_tiles;
-        for (int n = seg.ke - seg.kb; n > 0; --n) {
+        for (int n = nslabs; n > 0; --n) {
             before_slab();
             const int s = stage;
             // Fast path: one try_wait that finds the slab already copied.  Only
             // if some lane misses it does the warp take a warp-uniform look at
             // the abort flag and enter the bounded wait.
-            if (!__all_sync(0xffffffffu, mbar_try_wait(&ring.full[s], phase)) &&
-                !__any_sync(0xffffffffu, *ring.abort_flag)) {
-                bool ok = mbar_wait(&ring.full[s], phase, p.timeout_ns);
+            if (!__all_sync(0xffffffffu, mbar_try_wait_at(ring.full(s), phase)) &&
+                !__any_sync(0xffffffffu, ring.aborted())) {
+                bool ok = mbar_wait_at(ring.full(s), phase, p.timeout_ns);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) {
                     if (lane == 0) atomicOr(&g_error_word, ERR_FULL_WAIT);
-                    *ring.abort_flag = 1;
+                    ring.set_abort();
                 }
             }
-            const uint32_t a_s = sA_addr + uint32_t(s * Cfg::A_STAGE + a_off) * 4u;
-            const uint32_t b_s = sB_addr + uint32_t(s * Cfg::B_STAGE + b_off) * 4u;
+            const uint32_t a_s = a_base + uint32_t(s * Cfg::A_STAGE) * 4u;
+            const uint32_t b_s = b_base + uint32_t(s * Cfg::B_STAGE) * 4u;
             // register double buffering of the fragments: the loads for k+1
             // are issued before the FMAs of k
             float fa[2][TM], fb[2][TN];
@@ -580,7 +607,10 @@ __device__ __forceinline__ void consumer_loop(const Ring &ring, const MainParams
                 outer_product<Cfg>(acc, fa[kk & 1], fb[kk & 1]);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ring.empty[s]);
+            if (lane == 0) {
+                mbar_arrive_at(ring.empty(s));
+                after_release(s);
+            }
             if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1u;
@@ -595,6 +625,7 @@ __device__ __forceinline__ void consumer_loop(const Ring &ring, const MainParams
             __threadfence();
             named_barrier(BAR_CONSUMERS, Cfg::CONSUMER_THREADS);
             if (ctid == 0) {
+                const int rel_tile = int(fix.tile_start / k_tiles);
                 const int before = atomicAdd(&p.counters[rel_tile], 1);
                 fix.last = (before == fix.pieces - 1);
             }
@@ -606,6 +637,10 @@ __device__ __forceinline__ void consumer_loop(const Ring &ring, const MainParams
             named_barrier(BAR_CONSUMERS, Cfg::CONSUMER_THREADS);
             if (finish) {
                 __threadfence();
+                // sk_start(b + 1) = sk_start(b) + sk_q + carry, carry from sk_r:
+                // additions only
+                const long long sk_q = p.sk_slabs / gridDim.x;
+                const int sk_r = int(p.sk_slabs % gridDim.x);
                 // this CTA's own piece is read back too, so the sum order is the
                 // k order whichever piece arrived last
 #pragma unroll
@@ -614,7 +649,13 @@ __device__ __forceinline__ void consumer_loop(const Ring &ring, const MainParams
                                         tile_start);
             }
         }
-        if (finish && !*ring.abort_flag) store_tile<Cfg>(acc, p, tm, tn, a_off, b_off);
+        if (finish && !ring.aborted()) {
+            Segment seg;
+            segment_at(p, k_tiles, si, seg);
+            int tm, tn;
+            tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            store_tile<Cfg>(acc, p, tm, tn, a_off(), b_off());
+        }
     }
 }
 
@@ -624,11 +665,12 @@ __device__ __forceinline__ void consumer_loop(const Ring &ring, const MainParams
 // warp has released the stage's previous contents (empty barrier); consumer
 // warps wait on the full barrier of a stage (TMA byte count) before reading it.
 //
-// WS (warp-specialised): warpgroup 0 is the producer; it gives back registers
+// ISSUE_PRODUCER_WG: warpgroup 0 is the producer; it gives back registers
 // (setmaxnreg.dec) and one of its threads issues all copies, STAGES ahead.  The
-// 8 consumer warps take the registers (setmaxnreg.inc).  Otherwise the CTA is
-// the 8 consumer warps alone (two per SM sub-partition, up to 255 registers a
-// thread) and consumer thread 0 issues slab q + STAGES - 1 when starting slab q.
+// consumer warps take the registers (setmaxnreg.inc).  Otherwise the CTA is
+// the consumer warps alone: with ISSUE_THREAD0 consumer thread 0 issues slab
+// q + STAGES - 1 when starting slab q; with ISSUE_LAST_WARP the warp that
+// releases slab q last issues slab q + STAGES.
 //
 // A stream-K piece that is not a whole tile writes its partial sums to its
 // slot and increments the tile's counter; the piece that brings the counter to
@@ -647,25 +689,29 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     constexpr int STAGES = Cfg::STAGES;
     constexpr int BAR_END = 2;
 
+    static_assert(Ring<Cfg>::BYTES + 1024 <= Cfg::SMEM_BYTES, "ring fits the dynamic shared memory");
     extern __shared__ unsigned char smem_raw[];
-    const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
-    Ring ring;
-    ring.sA = reinterpret_cast<float *>(base);
-    ring.sB = ring.sA + STAGES * Cfg::A_STAGE;
-    ring.full = reinterpret_cast<uint64_t *>(ring.sB + STAGES * Cfg::B_STAGE);
-    ring.empty = ring.full + STAGES;
-    ring.abort_flag = reinterpret_cast<volatile int *>(ring.empty + STAGES);
+    // stages 1024-byte aligned
+    const Ring<Cfg> ring{(smem_addr(smem_raw) + 1023u) & ~1023u};
     __shared__ FixInfo fix;
+    // issuer state in shared memory (ISSUE_THREAD0, ISSUE_LAST_WARP): keeping
+    // it out of registers leaves them to the accumulators
+    __shared__ IssueState ist;
+    __shared__ int released[STAGES];   // ISSUE_LAST_WARP: warps done with a stage
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
+        uint64_t *bars = reinterpret_cast<uint64_t *>(
+            smem_raw + (ring.full(0) - smem_addr(smem_raw)));
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&ring.full[s], 1);
-            mbar_init(&ring.empty[s], Cfg::CONSUMER_WARPS);
+            mbar_init(&bars[s], 1);
+            mbar_init(&bars[STAGES + s], Cfg::CONSUMER_WARPS);
+            released[s] = 0;
         }
-        *ring.abort_flag = 0;
+        st_shared_flag(ring.abort_flag(), 0);
+        ist.init(p);
         fence_barrier_init();
     }
     __syncthreads();
@@ -689,28 +735,49 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // wait until every consumer is done, then (after an abort) make
             // sure no copy is still writing shared memory when the CTA exits
             named_barrier(BAR_END, 32 + Cfg::CONSUMER_THREADS);
-            if (lane == 0 && *ring.abort_flag) drain_copies<Cfg>(ring, st.issued, p);
+            if (lane == 0 && ring.aborted()) drain_copies<Cfg>(ring, st.issued, p);
             return;
         }
         // ============================================================ consumers
         regs_increase<Cfg::CONSUMER_REGS>();
         consumer_loop<Cfg>(ring, p, k_tiles, warp - Cfg::PRODUCER_THREADS / 32,
-                           threadIdx.x - Cfg::PRODUCER_THREADS, fix, [] {});
+                           threadIdx.x - Cfg::PRODUCER_THREADS, fix, [] {}, [](int) {});
         named_barrier(BAR_END, 32 + Cfg::CONSUMER_THREADS);
-    } else {
-        // issue state in shared memory: only thread 0 touches it, and keeping
-        // it out of registers leaves them to the accumulators
-        __shared__ IssueState ist;
+    } else if constexpr (Cfg::ISSUE == ISSUE_THREAD0) {
         if (threadIdx.x == 0) {
-            ist.init(p);
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
             for (int i = 0; i < STAGES - 1; ++i) issue_one<Cfg>(ist, ring, &tmA, &tmB, p, k_tiles);
         }
-        consumer_loop<Cfg>(ring, p, k_tiles, warp, threadIdx.x, fix, [&] {
-            if (threadIdx.x == 0) issue_one<Cfg>(ist, ring, &tmA, &tmB, p, k_tiles);
+        consumer_loop<Cfg>(
+            ring, p, k_tiles, warp, threadIdx.x, fix,
+            [&] {
+                if (threadIdx.x == 0) issue_one<Cfg>(ist, ring, &tmA, &tmB, p, k_tiles);
+            },
+            [](int) {});
+        if (threadIdx.x == 0 && ring.aborted()) drain_copies<Cfg>(ring, ist.issued, p);
+    } else {
+        // ISSUE_LAST_WARP: thread 0 fills every stage once; afterwards the warp
+        // whose release completes a stage's count copies the next slab into it
+        // at once, so no warp waits for the others.  Slab q + STAGES goes into
+        // the stage of slab q, and the releases of slab q all precede those of
+        // q + 1, so the elected warps use `ist` one at a time, in slab order.
+        if (threadIdx.x == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            for (int i = 0; i < STAGES; ++i) issue_one<Cfg>(ist, ring, &tmA, &tmB, p, k_tiles);
+        }
+        consumer_loop<Cfg>(ring, p, k_tiles, warp, threadIdx.x, fix, [] {}, [&](int s) {
+            __threadfence_block();
+            if (atomicAdd(&released[s], 1) == Cfg::CONSUMER_WARPS - 1) {
+                released[s] = 0;
+                __threadfence_block();
+                issue_one<Cfg>(ist, ring, &tmA, &tmB, p, k_tiles);
+            }
         });
-        if (threadIdx.x == 0 && *ring.abort_flag) drain_copies<Cfg>(ring, ist.issued, p);
+        // every warp is past its last issue before the copies are counted
+        __syncthreads();
+        if (threadIdx.x == 0 && ring.aborted()) drain_copies<Cfg>(ring, ist.issued, p);
     }
 }
 

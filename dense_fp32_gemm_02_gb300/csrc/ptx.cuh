@@ -29,41 +29,63 @@ __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+// The barrier operations take the barrier either as a pointer or as its
+// 32-bit shared-window address (`_at` forms), which keeps a kernel's barrier
+// addresses in one 32-bit register each.
+__device__ __forceinline__ void mbar_arrive_at(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) { mbar_arrive_at(smem_addr(bar)); }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-                 "r"(bytes)
+__device__ __forceinline__ void mbar_arrive_expect_tx_at(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    mbar_arrive_expect_tx_at(smem_addr(bar), bytes);
 }
 
 // true once the phase with the given parity has completed
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait_at(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(bar), "r"(parity)
         : "memory");
     return done != 0;
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    return mbar_try_wait_at(smem_addr(bar), parity);
 }
 
 // Bounded wait: spins on try_wait and gives up after `timeout_ns` of global time.
 // Returns false on expiry.  The clock is read only after a failed try, so the
 // fast path costs one try_wait.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t timeout_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+__device__ __forceinline__ bool mbar_wait_at(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+    if (mbar_try_wait_at(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (mbar_try_wait_at(bar, parity)) return true;
         if (global_timer_ns() - t0 > timeout_ns) return false;
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t timeout_ns) {
+    return mbar_wait_at(smem_addr(bar), parity, timeout_ns);
+}
+
+// Volatile 32-bit shared-memory flag access by shared-window address.
+__device__ __forceinline__ int ld_shared_flag(uint32_t addr) {
+    int v;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_shared_flag(uint32_t addr, int v) {
+    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // ---------------------------------------------------------------- TMA
@@ -73,13 +95,17 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
 
 // 2-D tiled bulk tensor load global -> shared, completion counted in bytes on `bar`.
 // x is the innermost (contiguous) coordinate; it must be a multiple of 4 floats.
-__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
-                                            int x, int y) {
+__device__ __forceinline__ void tma_load_2d_at(uint32_t smem_dst, const CUtensorMap *map,
+                                               uint32_t bar, int x, int y) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y)
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
         : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y) {
+    tma_load_2d_at(smem_addr(smem_dst), map, smem_addr(bar), x, y);
 }
 
 // ---------------------------------------------------------------- FP32x2

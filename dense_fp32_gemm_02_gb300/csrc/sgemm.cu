@@ -68,33 +68,42 @@ constexpr Variant make_variant(const char *name, bool stream_k, int group_m = 8)
 
 using sg::MICRO_FFMA;
 using sg::MICRO_FFMA2;
+using sg::ISSUE_THREAD0;
+using sg::ISSUE_PRODUCER_WG;
+using sg::ISSUE_LAST_WARP;
 // Variant 0 is the default for every shape: it was the fastest or within 1%
 // of the fastest on every measured workload.  Its 16 consumer warps (four per
 // scheduler) hide the shared-memory latency of the fragment loads better than
-// 12 warps plus a producer warpgroup; a producer warpgroup does not fit beside
-// 16 consumer warps at 128 registers each.  The others stay for sweeps and as
-// evidence for the design choices (tile shape, stream-K, warp specialisation,
-// packed FP32x2 FMA, thread-tile size, k depth of a stage).
+// 12 warps plus a producer warpgroup (16 consumer warps at 128 registers fill
+// the register file, so the two do not fit together), and the warp that
+// releases a stage last refills it, so no warp waits for the others.  The
+// others stay for sweeps and as evidence for the design choices (issuer,
+// tile shape, stream-K, warp specialisation, packed FP32x2 FMA, thread-tile
+// size, k depth of a stage).
 const Variant kVariants[] = {
-    make_variant<sg::TileConfig<256, 128, 64, 2, 8, 2, 8, 8, MICRO_FFMA2, false>>(
+    make_variant<sg::TileConfig<256, 128, 64, 2, 8, 2, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>>(
+        "ffma2 tile=256x128x64 stages=2 warps=16 issuer=last_warp thread=8x8 stream_k", true),
+    make_variant<sg::TileConfig<128, 256, 64, 2, 4, 4, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>>(
+        "ffma2 tile=128x256x64 stages=2 warps=16 issuer=last_warp thread=8x8 stream_k", true),
+    make_variant<sg::TileConfig<256, 128, 64, 2, 8, 2, 8, 8, MICRO_FFMA2, ISSUE_THREAD0>>(
         "ffma2 tile=256x128x64 stages=2 warps=16 issuer=thread0 thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<128, 256, 64, 2, 4, 4, 8, 8, MICRO_FFMA2, false>>(
-        "ffma2 tile=128x256x64 stages=2 warps=16 issuer=thread0 thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<256, 128, 64, 2, 8, 2, 8, 8, MICRO_FFMA2, false>>(
-        "ffma2 tile=256x128x64 stages=2 warps=16 issuer=thread0 thread=8x8 no_stream_k", false),
-    make_variant<sg::TileConfig<256, 128, 48, 3, 8, 2, 8, 8, MICRO_FFMA2, false>>(
-        "ffma2 tile=256x128x48 stages=3 warps=16 issuer=thread0 thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<128, 192, 64, 2, 4, 3, 8, 8, MICRO_FFMA2, true>>(
+    make_variant<sg::TileConfig<256, 128, 64, 2, 8, 2, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>>(
+        "ffma2 tile=256x128x64 stages=2 warps=16 issuer=last_warp thread=8x8 no_stream_k", false),
+    make_variant<sg::TileConfig<256, 128, 48, 3, 8, 2, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>>(
+        "ffma2 tile=256x128x48 stages=3 warps=16 issuer=last_warp thread=8x8 stream_k", true),
+    make_variant<sg::TileConfig<128, 192, 64, 2, 4, 3, 8, 8, MICRO_FFMA2, ISSUE_PRODUCER_WG>>(
         "ffma2 tile=128x192x64 stages=2 warps=12+producer_wg thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<128, 192, 64, 2, 4, 3, 8, 8, MICRO_FFMA2, false>>(
+    make_variant<sg::TileConfig<128, 192, 64, 2, 4, 3, 8, 8, MICRO_FFMA2, ISSUE_THREAD0>>(
         "ffma2 tile=128x192x64 stages=2 warps=12 issuer=thread0 thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<192, 128, 64, 2, 6, 2, 8, 8, MICRO_FFMA2, true>>(
+    make_variant<sg::TileConfig<128, 192, 64, 2, 4, 3, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>>(
+        "ffma2 tile=128x192x64 stages=2 warps=12 issuer=last_warp thread=8x8 stream_k", true),
+    make_variant<sg::TileConfig<192, 128, 64, 2, 6, 2, 8, 8, MICRO_FFMA2, ISSUE_PRODUCER_WG>>(
         "ffma2 tile=192x128x64 stages=2 warps=12+producer_wg thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<128, 128, 48, 4, 4, 2, 8, 8, MICRO_FFMA2, true>>(
+    make_variant<sg::TileConfig<128, 128, 48, 4, 4, 2, 8, 8, MICRO_FFMA2, ISSUE_PRODUCER_WG>>(
         "ffma2 tile=128x128x48 stages=4 warps=8+producer_wg thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<128, 128, 48, 4, 4, 2, 8, 8, MICRO_FFMA, true>>(
+    make_variant<sg::TileConfig<128, 128, 48, 4, 4, 2, 8, 8, MICRO_FFMA, ISSUE_PRODUCER_WG>>(
         "ffma tile=128x128x48 stages=4 warps=8+producer_wg thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<256, 128, 32, 4, 4, 2, 16, 8, MICRO_FFMA2, true>>(
+    make_variant<sg::TileConfig<256, 128, 32, 4, 4, 2, 16, 8, MICRO_FFMA2, ISSUE_PRODUCER_WG>>(
         "ffma2 tile=256x128x32 stages=4 warps=8+producer_wg thread=16x8 stream_k", true),
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
