@@ -29,7 +29,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle_sgemm.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, f"liboracle_sgemm_{platform.machine()}.so")
-_ABI_VERSION = 1
+_ABI_VERSION = 2
 
 # -ffp-contract=off: no fused multiply-add contraction; no -ffast-math; no -march:
 # the same source gives the same bits on x86-64 and aarch64.
@@ -71,6 +71,9 @@ def load_library(path: str):
     lib.oracle_sgemm_cols.argtypes = [ll, ll, ll, f32, p, ll, p, ll, f32, p, ll,
                                       p, ll, ll, ll, p, p]
     lib.oracle_sgemm_cols.restype = ctypes.c_int
+    lib.oracle_sgemm_ex_rows.argtypes = [ll, ll, ll, f32, p, ll, p, ll, f32, p, ll,
+                                         p, ctypes.c_int, p, ll, p, p]
+    lib.oracle_sgemm_ex_rows.restype = ctypes.c_int
     return lib
 
 
@@ -183,3 +186,59 @@ def sgemm(A, B, C_in, alpha, beta, threads=None, with_bound=True, lib=None):
     M = A.shape[0]
     return sgemm_rows(A, B, C_in, alpha, beta, np.arange(M, dtype=np.int64),
                       threads=threads, with_bound=with_bound, lib=lib)
+
+
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2}
+
+
+def sgemm_ex_rows(A, B, C_in, alpha, beta, bias=None, act="none", rows=None, threads=None,
+                  with_bound=True, lib=None):
+    """Rows ``rows`` (all when None) of act(alpha*A@B + beta*C_in + bias) for one
+    batch; ``bias`` is a float32 vector of length N or None.  Returns (out, bound)."""
+    A, lda, B, ldb, C_in, ldc, M, N, K = _dims(A, B, C_in, beta)
+    if bias is not None:
+        if not isinstance(bias, np.ndarray) or bias.dtype != np.float32 or bias.shape != (N,):
+            raise TypeError(f"bias must be a float32 vector of length {N}")
+        bias = np.ascontiguousarray(bias)
+    code = ACTIVATIONS[act]
+    rows = np.arange(M, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    nrows = rows.shape[0]
+    out = np.empty((nrows, N), dtype=np.float32)
+    bound = np.empty((nrows, N), dtype=np.float64) if with_bound else None
+    lib = lib or _load()
+    nt = min(_threads(threads), max(1, nrows))
+    chunks = np.array_split(np.arange(nrows), nt)
+
+    def run(idx):
+        if idx.size == 0:
+            return 0
+        r0, r1 = int(idx[0]), int(idx[-1]) + 1
+        o = out[r0:r1]
+        b = bound[r0:r1] if bound is not None else None
+        return lib.oracle_sgemm_ex_rows(M, N, K, float(alpha), _ptr(A), lda, _ptr(B), ldb,
+                                        float(beta), _ptr(C_in), ldc, _ptr(bias), code,
+                                        rows[r0:r1].ctypes.data, r1 - r0, _ptr(o), _ptr(b))
+
+    with ThreadPoolExecutor(max_workers=nt) as ex:
+        codes = list(ex.map(run, chunks))
+    if any(codes):
+        raise RuntimeError(f"oracle_sgemm_ex_rows failed with codes {set(codes)}")
+    return out, bound
+
+
+def sgemm_batched(As, Bs, Cs, alpha, beta, biases=None, act="none", rows=None, threads=None,
+                  with_bound=True, lib=None):
+    """One fused GEMM per batch: As, Bs, Cs are sequences of 2-D float32 arrays (Cs
+    entries may be None when beta == 0), biases a sequence of vectors or None.
+    Returns (out [batch, len(rows), N], bound of the same shape)."""
+    batch = len(As)
+    if len(Bs) != batch or (Cs is not None and len(Cs) != batch):
+        raise ValueError("As, Bs and Cs must have one entry per batch")
+    outs, bounds = [], []
+    for b in range(batch):
+        o, bd = sgemm_ex_rows(As[b], Bs[b], None if Cs is None else Cs[b], alpha, beta,
+                              None if biases is None else biases[b], act, rows, threads,
+                              with_bound, lib)
+        outs.append(o)
+        bounds.append(bd)
+    return np.stack(outs), (np.stack(bounds) if with_bound else None)

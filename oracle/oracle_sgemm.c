@@ -194,5 +194,103 @@ int oracle_sgemm_cols(long long M, long long N, long long K, float alpha,
     return ORACLE_OK;
 }
 
+/*
+ * Fused epilogue: the GEMM of one batch followed by a bias and an activation,
+ * the layer form in which neural networks use matrix multiplication (the
+ * article "How to implement matrix multiplication efficiently? An introduction
+ * from a CUDA beginner's view" motivates GEMM optimisation by neural-network
+ * workloads and names operator fusion with the GEMM as the next step; it fixes
+ * no bias or activation, so the forms below are this oracle's reading):
+ *
+ *   Z[i][j]     = alpha * sum_k A[i][k]*B[k][j]  +  beta * C_in[i][j]  +  bias[j]
+ *   C_out[i][j] = (float) act(Z[i][j])
+ *
+ * in double with one final rounding; bias == NULL means no bias (the bias is
+ * per output column, broadcast over the rows); act 0 = identity, 1 = ReLU
+ * max(Z, 0), 2 = GELU in its erf form Z * Phi(Z) = 0.5 * Z * (1 + erf(Z / sqrt 2)).
+ * A batched GEMM is one call per batch on that batch's own matrices.
+ *
+ * Bound: the plain bound plus 1e-6 * |bias[j]| for Z; identity and ReLU
+ * (1-Lipschitz) keep it; GELU takes 1.129 * bound_Z + 1e-6 * |Z|, where 1.129
+ * is the largest slope of Z * Phi(Z) (at Z = sqrt 2: Phi(sqrt 2) + sqrt 2 *
+ * phi(sqrt 2)) and the second term covers a single-precision erf.
+ */
+#define ORACLE_ACT_NONE 0
+#define ORACLE_ACT_RELU 1
+#define ORACLE_ACT_GELU 2
+
+static double activation(int act, double z)
+{
+    if (act == ORACLE_ACT_RELU)
+        return z > 0.0 ? z : 0.0;
+    if (act == ORACLE_ACT_GELU)
+        return 0.5 * z * (1.0 + erf(z / sqrt(2.0)));
+    return z;
+}
+
+int oracle_sgemm_ex_rows(long long M, long long N, long long K, float alpha,
+                         const float *A, long long lda, const float *B, long long ldb,
+                         float beta, const float *C_in, long long ldc,
+                         const float *bias, int act,
+                         const long long *rows, long long nrows,
+                         float *out, double *bound)
+{
+    if (act < ORACLE_ACT_NONE || act > ORACLE_ACT_GELU)
+        return ORACLE_ERR_ARG;
+    if (M < 0 || N < 0 || K < 0 || nrows < 0 || !rows || (!out && nrows * N > 0))
+        return ORACLE_ERR_ARG;
+    if (beta != 0.0f && !C_in && nrows * N > 0)
+        return ORACLE_ERR_ARG;
+    if (N == 0 || nrows == 0)
+        return ORACLE_OK;
+
+    double *acc = (double *)malloc(sizeof(double) * (size_t)N);
+    double *abs_acc = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!acc || !abs_acc) {
+        free(acc);
+        free(abs_acc);
+        return ORACLE_ERR_ALLOC;
+    }
+    for (long long r = 0; r < nrows; ++r) {
+        long long i = rows[r];
+        if (i < 0 || i >= M) {
+            free(acc);
+            free(abs_acc);
+            return ORACLE_ERR_ARG;
+        }
+        memset(acc, 0, sizeof(double) * (size_t)N);
+        memset(abs_acc, 0, sizeof(double) * (size_t)N);
+        if (alpha != 0.0f) {
+            for (long long k = 0; k < K; ++k) {
+                double a = (double)A[i * lda + k];
+                const float *brow = B + k * ldb;
+                for (long long j = 0; j < N; ++j) {
+                    acc[j] += a * (double)brow[j];
+                    abs_acc[j] += fabs(a) * fabs((double)brow[j]);
+                }
+            }
+        }
+        for (long long j = 0; j < N; ++j) {
+            double z = (alpha == 0.0f) ? 0.0 : (double)alpha * acc[j];
+            double bz = 1e-6 * (double)K * fabs((double)alpha) * abs_acc[j];
+            if (beta != 0.0f) {
+                double cterm = (double)beta * (double)C_in[i * ldc + j];
+                z += cterm;
+                bz += 1e-6 * fabs(cterm);
+            }
+            if (bias) {
+                z += (double)bias[j];
+                bz += 1e-6 * fabs((double)bias[j]);
+            }
+            out[r * N + j] = (float)activation(act, z);
+            if (bound)
+                bound[r * N + j] = (act == ORACLE_ACT_GELU) ? 1.129 * bz + 1e-6 * fabs(z) : bz;
+        }
+    }
+    free(acc);
+    free(abs_acc);
+    return ORACLE_OK;
+}
+
 /* Version tag so the loader can refuse a stale build. */
-int oracle_abi_version(void) { return 1; }
+int oracle_abi_version(void) { return 2; }
