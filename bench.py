@@ -181,12 +181,36 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------- CPU oracle timing
+def l2_note(w):
+    """How the timed steps avoid a warm L2: the bytes of A, B and C per step."""
+    lda, ldb, ldc = w.lds()
+    mb = 4.0 * w.batch * (w.M * lda + w.K * ldb + w.M * ldc) / 1e6
+    if mb > 129.0:
+        return f"inputs larger than L2 (A, B, C {mb:.0f} MB vs 129 MB), no flush"
+    return f"A, B, C {mb:.0f} MB, not larger than the 129 MB L2: no flush, L2 partly warm"
+
+
+def oracle_rows_fn(w, A, B, C):
+    """f(idx): the oracle as it stands on full rows idx of the workload (batch 0
+    of a batched one, with its bias and activation)."""
+    import oracle
+    from dense_fp32_gemm_02_gb300.workloads import workload_bias
+    if w.extended:
+        bias = workload_bias(w)
+        A0, B0 = (A[0], B[0]) if w.batch > 1 else (A, B)
+        C0 = None if (C is None or w.beta == 0) else (C[0] if w.batch > 1 else C)
+        b0 = None if bias is None else bias[0]
+        return lambda idx: oracle.sgemm_ex_rows(A0, B0, C0, w.alpha, w.beta, b0, w.act, idx,
+                                                with_bound=False)
+    c_in = C if w.beta != 0 else None
+    return lambda idx: oracle.sgemm_rows(A, B, c_in, w.alpha, w.beta, idx, with_bound=False)
+
+
 def time_oracle_rows(w, A, B, C, row_budget_s=12.0, first=16, max_rows=None):
     """The oracle as it stands on full rows of the workload; grows the sample
     until about `row_budget_s` seconds of CPU work.  Returns (gflops, rows, secs)."""
     import numpy as np
-    import oracle
-    c_in = C if w.beta != 0 else None
+    rows_fn = oracle_rows_fn(w, A, B, C)
     rows_done, secs, r0 = 0, 0.0, 0
     n = first
     max_rows = max_rows or w.M
@@ -194,7 +218,7 @@ def time_oracle_rows(w, A, B, C, row_budget_s=12.0, first=16, max_rows=None):
         n = min(n, max_rows - rows_done)
         idx = np.arange(r0, r0 + n, dtype=np.int64)
         t = time.perf_counter()
-        oracle.sgemm_rows(A, B, c_in, w.alpha, w.beta, idx, with_bound=False)
+        rows_fn(idx)
         secs += time.perf_counter() - t
         rows_done += n
         r0 += n
@@ -221,15 +245,14 @@ def run_reference(args):
     from dense_fp32_gemm_02_gb300.workloads import BENCH_WORKLOAD, WORKLOADS, workload_inputs
     w = WORKLOADS[args.workload or BENCH_WORKLOAD]
     A, B, C = workload_inputs(w)
-    import oracle
     # enough full rows per step for every host core to get two
     rows_per_step = max(16, 2 * host_cores())
-    c_in = C if w.beta != 0 else None
+    rows_fn = oracle_rows_fn(w, A, B, C)
 
     def step(i):
         r0 = (i * rows_per_step) % w.M
         idx = np.arange(r0, min(r0 + rows_per_step, w.M), dtype=np.int64)
-        oracle.sgemm_rows(A, B, c_in, w.alpha, w.beta, idx, with_bound=False)
+        rows_fn(idx)
         return len(idx)
 
     for i in range(args.warmup):
@@ -381,10 +404,14 @@ def run_ours(args):
     dist_init(world, "nccl")
 
     from dense_fp32_gemm_02_gb300 import binding
-    from dense_fp32_gemm_02_gb300.workloads import BENCH_WORKLOAD, WORKLOADS, workload_inputs
+    from dense_fp32_gemm_02_gb300.workloads import (BENCH_WORKLOAD, WORKLOADS, workload_bias,
+                                                    workload_inputs)
     w = WORKLOADS[args.workload or BENCH_WORKLOAD]
     binding.set_variant(args.variant)
     A, B, C = workload_inputs(w)
+    bias = workload_bias(w)
+    if w.extended and args.path != "ffma":
+        raise SystemExit("batched and fused-epilogue workloads run on the FFMA path (sgemm_ex)")
     props = torch.cuda.get_device_properties(device)
     sms = props.multi_processor_count
     stream = torch.cuda.Stream(device)
@@ -392,13 +419,18 @@ def run_ours(args):
     dA = torch.from_numpy(np.ascontiguousarray(A)).to(device)
     dB = torch.from_numpy(np.ascontiguousarray(B)).to(device)
     dC = torch.from_numpy(np.ascontiguousarray(C)).to(device) if C is not None else \
-        torch.zeros((w.M, w.N), device=device)
+        torch.zeros(((w.batch,) if w.batch > 1 else ()) + (w.M, w.N), device=device)
+    dbias = torch.from_numpy(bias).to(device) if bias is not None else None
     torch.cuda.synchronize()
 
     gemm = binding.sgemm_into if args.path == "ffma" else binding.sgemm_3xtf32_into
 
     def step():
-        gemm(dA, dB, dC, w.alpha, w.beta, stream=stream)
+        if w.extended:
+            binding.sgemm_ex_into(dA, dB, dC, w.alpha, w.beta, bias=dbias, act=w.act,
+                                  stream=stream)
+        else:
+            gemm(dA, dB, dC, w.alpha, w.beta, stream=stream)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -446,7 +478,7 @@ def run_ours(args):
 
     # ---- end to end through the host-buffer entry point
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not w.extended:
         hA = torch.from_numpy(np.ascontiguousarray(A)).pin_memory()
         hB = torch.from_numpy(np.ascontiguousarray(B)).pin_memory()
         hC0 = torch.from_numpy(np.ascontiguousarray(C)) if C is not None else None
@@ -469,7 +501,7 @@ def run_ours(args):
                "ms_per_step": round(e2e_s / args.steps * 1e3, 3)}
     main_windows = list(clocks.windows)
     tf32x3 = None
-    if args.path == "ffma" and not args.no_tf32x3:
+    if args.path == "ffma" and not args.no_tf32x3 and not w.extended:
         t0x = time.time()
         tf32x3 = measure_tf32x3(args, w, binding, dA, dB, dC, C, stream, world, device)
         tf_window = (t0x, time.time())
@@ -535,7 +567,8 @@ def run_ours(args):
             "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
                        "beta": w.beta, "seed": w.seed,
-                       "l2": "inputs larger than L2 (A, B, C 805 MB vs 129 MB), no flush",
+                       "l2": l2_note(w),
+                       "batch": w.batch, "bias": w.bias, "act": w.act,
                        "parallelism": "replicas" if world > 1 else "single_gpu",
                        "kernel": (binding.config_string(w.M, w.N, w.K) if args.path == "ffma"
                                   else "3xtf32 tcgen05 tile=128x256x16 stages=4 persistent "

@@ -29,6 +29,9 @@ lib.sgemm.argtypes = [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]
 lib.sgemm.restype = _i
 lib.sgemm_host.argtypes = [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]
 lib.sgemm_host.restype = _i
+lib.sgemm_ex.argtypes = [_i, _i, _i, _f, _p, _i, _ll, _p, _i, _ll, _f, _p, _i, _ll, _i, _p, _ll,
+                         _i, _p]
+lib.sgemm_ex.restype = _i
 lib.sgemm_noalloc.argtypes = [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]
 lib.sgemm_noalloc.restype = _i
 lib.sgemm_3xtf32.argtypes = [_i, _i, _i, _f, _p, _i, _p, _i, _f, _p, _i, _p]
@@ -136,6 +139,57 @@ def sgemm_into(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
     with torch.cuda.device(C.device):
         st = lib.sgemm(M, N, K, float(alpha), A.data_ptr(), _ld(A, K), B.data_ptr(), _ld(B, N),
                        float(beta), C.data_ptr(), _ld(C, N), _stream_handle(stream, C.device))
+    check(st)
+    return C
+
+
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2}
+
+
+def _batched(t, name):
+    """(2-D view of batch 0, batch count, batch stride in elements) of a 2-D or
+    3-D tensor; a 2-D tensor is one matrix used by every batch (stride 0)."""
+    if t.dim() == 2:
+        return t, 1, 0
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be 2-D or 3-D")
+    return t[0], t.size(0), (t.stride(0) if t.size(0) > 1 else 0)
+
+
+def sgemm_ex_into(A, B, C, alpha: float = 1.0, beta: float = 0.0, bias=None, act: str = "none",
+                  stream=None):
+    """C[b] <- act(alpha*A[b]@B[b] + beta*C[b] + bias[b]) on CUDA float32 tensors.
+    C is 3-D (batch, M, N) or 2-D (one batch); A and B are 3-D with the same
+    batch or 2-D (shared by all batches); bias is None, a length-N vector
+    (shared) or (batch, N).  Asynchronous on `stream`."""
+    import torch
+    for name, t in (("A", A), ("B", B), ("C", C)) + ((("bias", bias),) if bias is not None else ()):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA float32 tensor")
+        if t.device != C.device:
+            raise ValueError(f"{name} must be on C's device")
+    C0, batch, sc = _batched(C, "C")
+    A0, ba, sa = _batched(A, "A")
+    B0, bb, sb = _batched(B, "B")
+    for name, t, n in (("A", A, ba), ("B", B, bb)):
+        if t.dim() == 3 and n != batch:
+            raise ValueError(f"{name} has {n} batches, C has {batch}")
+    M, N, K = _shapes(A0, B0, C0)
+    bias_ptr, sbias = None, 0
+    if bias is not None:
+        if bias.dim() == 1 and bias.size(0) == N:
+            sbias = 0
+        elif bias.dim() == 2 and tuple(bias.shape) == (batch, N):
+            sbias = bias.stride(0) if batch > 1 else 0
+        else:
+            raise ValueError(f"bias must be ({N},) or ({batch}, {N})")
+        if bias.size(-1) > 1 and bias.stride(-1) != 1:
+            raise ValueError("bias rows must be contiguous")
+        bias_ptr = bias.data_ptr()
+    with torch.cuda.device(C.device):
+        st = lib.sgemm_ex(M, N, K, float(alpha), A0.data_ptr(), _ld(A0, K), sa, B0.data_ptr(),
+                          _ld(B0, N), sb, float(beta), C0.data_ptr(), _ld(C0, N), sc, batch,
+                          bias_ptr, sbias, ACTIVATIONS[act], _stream_handle(stream, C.device))
     check(st)
     return C
 

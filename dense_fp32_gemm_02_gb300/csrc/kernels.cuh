@@ -25,6 +25,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -91,6 +92,10 @@ struct TileConfig {
     static constexpr size_t SMEM_BYTES =
         size_t(STAGES) * STAGE_BYTES + 2 * STAGES * sizeof(uint64_t) + 16 + 1024;
     static constexpr int TILE_FLOATS = BM * BN;
+    // EX: the kernel serves batched calls and the fused bias/activation
+    // epilogue (see ExConfig); the plain kernel leaves that code out, which
+    // keeps its main loop under the register cap.
+    static constexpr bool EX = false;
 
     static_assert(WM * WARPS_M == BM && WN * WARPS_N == BN, "warp grid must cover the tile");
     static_assert(TM % 4 == 0 && TN % 4 == 0, "thread tile is made of 4x4 sub-tiles");
@@ -103,13 +108,22 @@ struct TileConfig {
                   "register split exceeds the launch allocation");
 };
 
+// Activation of the fused epilogue.
+enum Act : int { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU = 2 };
+
+// The same tile configuration for the batched / fused-epilogue kernel.
+template <class Base>
+struct ExConfig : Base {
+    static constexpr bool EX = true;
+};
+
 struct MainParams {
     float *C;
     long long ldc;
     int M, N, K;
     float alpha, beta;
     int tiles_m, tiles_n, group_m;
-    int c_vec4;              // C base 16-byte aligned and ldc % 4 == 0
+    int c_vec4;              // C base 16-byte aligned and ldc % 4 == 0 (and stride_c % 4 == 0)
     unsigned long long timeout_ns;
     // Work split.  Tiles [0, dp_tiles) are whole-tile work, CTA b taking tiles
     // b, b + gridDim.x, ...  The k-slabs of the remaining tiles, in tile-major
@@ -119,6 +133,23 @@ struct MainParams {
     long long sk_slabs;
     float *partials;         // 2 * gridDim.x slots of BM*BN floats (sk_slabs > 0)
     int *counters;           // one per stream-K tile, zero at launch (sk_slabs > 0)
+};
+
+// Parameters only the batched / fused-epilogue kernel (EX) reads; a separate
+// kernel argument, so the plain kernel's parameters stay as they are.
+struct ExParams {
+    // Batches: tile t belongs to batch t / (tiles_m * tiles_n).  Batch b's C
+    // starts at C + b * stride_c; its A and B are plane b of the 3-D tensor
+    // maps (plane 0 for every batch when a_planes / b_planes is 1).
+    int batch;
+    long long stride_c;
+    int a_planes, b_planes;
+    // Fused epilogue: C = act(alpha*acc + beta*C + bias[col]); bias may be null
+    // (batch b's bias at bias + b * stride_bias).
+    const float *bias;
+    long long stride_bias;
+    int bias_vec4;           // bias base 16-byte aligned and stride_bias % 4 == 0
+    int act;
 };
 
 // Grouped raster: tiles are visited in groups of `group_m` tile-rows, column
@@ -134,6 +165,14 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
     const int local = tile - g * per_group;
     tm = first_m + local % gm;
     tn = local / gm;
+}
+
+// Batch and tile coordinates of tile number `tile`.
+__device__ __forceinline__ void decode_tile(const struct MainParams &p, int tile, int &tb, int &tm,
+                                            int &tn) {
+    const int per_batch = p.tiles_m * p.tiles_n;
+    tb = tile / per_batch;
+    tile_coords(tile - tb * per_batch, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
 }
 
 // 128-bit shared-memory load from a 32-bit shared-window address.  Explicit
@@ -301,6 +340,13 @@ __device__ __forceinline__ bool segment_at(const MainParams &p, int k_tiles, int
 }
 
 // ------------------------------------------------------------------ epilogue
+// Activation of the fused epilogue (ACT_GELU: the erf form v * Phi(v)).
+__device__ __forceinline__ float activate(float v, int act) {
+    if (act == ACT_RELU) return fmaxf(v, 0.0f);
+    if (act == ACT_GELU) return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+    return v;
+}
+
 // C = alpha * acc + beta * C for this thread's outputs of tile (tm, tn);
 // C is not read when beta == 0.  Rows >= M and columns >= N are not written.
 template <class Cfg>
@@ -341,6 +387,81 @@ __device__ __forceinline__ void store_tile(const float (&acc)[Cfg::TM][Cfg::TN],
                         if (col + e < p.N) {
                             const float c = (beta != 0.0f) ? beta * crow[col + e] : 0.0f;
                             crow[col + e] = (beta != 0.0f) ? fmaf(alpha, v[e], c) : alpha * v[e];
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+// The epilogue of the batched / fused kernel: C = act(alpha * acc + beta * C +
+// bias) for this thread's outputs of tile (tm, tn) of batch tb; C is not read
+// when beta == 0, and without a bias or an activation the plain alpha/beta
+// update is all that runs.  Rows >= M and columns >= N are not written.
+template <class Cfg>
+__device__ __forceinline__ void store_tile_ex(const float (&acc)[Cfg::TM][Cfg::TN],
+                                              const MainParams &p, const ExParams &x, int tb,
+                                              int tm, int tn, int a_off, int b_off) {
+    const int row0 = tm * Cfg::BM + a_off;
+    const int col0 = tn * Cfg::BN + b_off;
+    const float alpha = p.alpha, beta = p.beta;
+    float *const Cb = p.C + (long long)tb * x.stride_c;
+    const float *const bias = x.bias ? x.bias + (long long)tb * x.stride_bias : nullptr;
+    const bool fused = bias != nullptr || x.act != ACT_NONE;
+    // the bias of four columns (read where it is used: an L1 hit after the
+    // first row, and four live registers instead of TN)
+    auto bias4 = [&](int col) {
+        if (bias && x.bias_vec4 && col + 3 < p.N)
+            return __ldg(reinterpret_cast<const float4 *>(bias + col));
+        float4 q;
+        q.x = (bias && col < p.N) ? bias[col] : 0.0f;
+        q.y = (bias && col + 1 < p.N) ? bias[col + 1] : 0.0f;
+        q.z = (bias && col + 2 < p.N) ? bias[col + 2] : 0.0f;
+        q.w = (bias && col + 3 < p.N) ? bias[col + 3] : 0.0f;
+        return q;
+    };
+#pragma unroll
+    for (int s4 = 0; s4 < Cfg::TM / 4; ++s4) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int row = row0 + s4 * 16 + r;
+            if (row >= p.M) continue;
+            float *crow = Cb + (long long)row * p.ldc;
+#pragma unroll
+            for (int t = 0; t < Cfg::TN / 4; ++t) {
+                const int col = col0 + t * 32;
+                const float *v = &acc[4 * s4 + r][4 * t];
+                if (p.c_vec4 && col + 3 < p.N) {
+                    float4 o;
+                    if (beta != 0.0f) {
+                        const float4 c = __ldcs(reinterpret_cast<const float4 *>(crow + col));
+                        o.x = fmaf(alpha, v[0], beta * c.x);
+                        o.y = fmaf(alpha, v[1], beta * c.y);
+                        o.z = fmaf(alpha, v[2], beta * c.z);
+                        o.w = fmaf(alpha, v[3], beta * c.w);
+                    } else {
+                        o.x = alpha * v[0];
+                        o.y = alpha * v[1];
+                        o.z = alpha * v[2];
+                        o.w = alpha * v[3];
+                    }
+                    if (fused) {
+                        const float4 bq = bias4(col);
+                        o.x = activate(bias ? o.x + bq.x : o.x, x.act);
+                        o.y = activate(bias ? o.y + bq.y : o.y, x.act);
+                        o.z = activate(bias ? o.z + bq.z : o.z, x.act);
+                        o.w = activate(bias ? o.w + bq.w : o.w, x.act);
+                    }
+                    __stcs(reinterpret_cast<float4 *>(crow + col), o);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (col + e < p.N) {
+                            const float c = (beta != 0.0f) ? beta * crow[col + e] : 0.0f;
+                            float o = (beta != 0.0f) ? fmaf(alpha, v[e], c) : alpha * v[e];
+                            if (fused) o = activate(bias ? o + bias[col + e] : o, x.act);
+                            crow[col + e] = o;
                         }
                     }
                 }
@@ -453,12 +574,17 @@ struct IssueState {
     }
 };
 
+// The issuer state of the batched kernel: also the batch of the current tile.
+struct IssueStateEx : IssueState {
+    int tb;
+};
+
 // Issue the copies of the next slab.  Returns false when there is none left or
 // the wait for the stage to be released expired (abort).
-template <class Cfg>
-__device__ __forceinline__ bool issue_one(IssueState &st, const Ring<Cfg> &ring,
+template <class Cfg, class State>
+__device__ __forceinline__ bool issue_one(State &st, const Ring<Cfg> &ring,
                                           const CUtensorMap *tmA, const CUtensorMap *tmB,
-                                          const MainParams &p, int k_tiles) {
+                                          const MainParams &p, const ExParams &x, int k_tiles) {
     if (ring.aborted()) return false;
     if (!st.have) {
         Segment sg;
@@ -467,7 +593,13 @@ __device__ __forceinline__ bool issue_one(IssueState &st, const Ring<Cfg> &ring,
         st.have = 1;
         st.slab = sg.kb;
         int tm, tn;
-        tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        if constexpr (Cfg::EX) {
+            int tb;
+            decode_tile(p, sg.tile, tb, tm, tn);
+            st.tb = tb;
+        } else {
+            tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        }
         st.tm = tm;
         st.tn = tn;
     }
@@ -480,8 +612,15 @@ __device__ __forceinline__ bool issue_one(IssueState &st, const Ring<Cfg> &ring,
         return false;
     }
     mbar_arrive_expect_tx_at(ring.full(s), Cfg::STAGE_BYTES);
-    tma_load_2d_at(ring.a(s), tmA, ring.full(s), st.tm * Cfg::BM, st.slab * Cfg::BK);
-    tma_load_2d_at(ring.b(s), tmB, ring.full(s), st.tn * Cfg::BN, st.slab * Cfg::BK);
+    if constexpr (Cfg::EX) {
+        tma_load_3d_at(ring.a(s), tmA, ring.full(s), st.tm * Cfg::BM, st.slab * Cfg::BK,
+                       x.a_planes > 1 ? st.tb : 0);
+        tma_load_3d_at(ring.b(s), tmB, ring.full(s), st.tn * Cfg::BN, st.slab * Cfg::BK,
+                       x.b_planes > 1 ? st.tb : 0);
+    } else {
+        tma_load_2d_at(ring.a(s), tmA, ring.full(s), st.tm * Cfg::BM, st.slab * Cfg::BK);
+        tma_load_2d_at(ring.b(s), tmB, ring.full(s), st.tn * Cfg::BN, st.slab * Cfg::BK);
+    }
     st.issued = st.issued + 1;
     if (s + 1 == Cfg::STAGES) {
         st.stage = 0;
@@ -531,7 +670,8 @@ struct FixInfo {
 // stream-K constants are fetched again after the loop instead of being kept.
 template <class Cfg, class Hook, class Release>
 __device__ __forceinline__ void consumer_loop(const Ring<Cfg> &ring, const MainParams &p,
-                                              int k_tiles, int cw, int ctid, FixInfo &fix,
+                                              const ExParams &x, int k_tiles, int cw, int ctid,
+                                              FixInfo &fix,
                                               Hook &&before_slab, Release &&after_release) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     constexpr int TM = Cfg::TM, TN = Cfg::TN;
@@ -653,8 +793,14 @@ __device__ __forceinline__ void consumer_loop(const Ring<Cfg> &ring, const MainP
             Segment seg;
             segment_at(p, k_tiles, si, seg);
             int tm, tn;
-            tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-            store_tile<Cfg>(acc, p, tm, tn, a_off(), b_off());
+            if constexpr (Cfg::EX) {
+                int tb;
+                decode_tile(p, seg.tile, tb, tm, tn);
+                store_tile_ex<Cfg>(acc, p, x, tb, tm, tn, a_off(), b_off());
+            } else {
+                tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                store_tile<Cfg>(acc, p, tm, tn, a_off(), b_off());
+            }
         }
     }
 }
@@ -685,7 +831,8 @@ __device__ __forceinline__ void consumer_loop(const Ring<Cfg> &ring, const MainP
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     sgemm_tma_ffma_kernel(const __grid_constant__ CUtensorMap tmA,
-                          const __grid_constant__ CUtensorMap tmB, const MainParams p) {
+                          const __grid_constant__ CUtensorMap tmB, const MainParams p,
+                          const ExParams x) {
     constexpr int STAGES = Cfg::STAGES;
     constexpr int BAR_END = 2;
 
@@ -696,7 +843,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     __shared__ FixInfo fix;
     // issuer state in shared memory (ISSUE_THREAD0, ISSUE_LAST_WARP): keeping
     // it out of registers leaves them to the accumulators
-    __shared__ IssueState ist;
+    __shared__ typename std::conditional<Cfg::EX, IssueStateEx, IssueState>::type ist;
     __shared__ int released[STAGES];   // ISSUE_LAST_WARP: warps done with a stage
 
     const int warp = threadIdx.x >> 5;
@@ -723,12 +870,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // ======================================================== producer
             regs_decrease<Cfg::PRODUCER_REGS>();
             if (warp != 0) return;
-            IssueState st;
+            typename std::conditional<Cfg::EX, IssueStateEx, IssueState>::type st;
             st.init(p);
             if (lane == 0) {
                 tma_prefetch_desc(&tmA);
                 tma_prefetch_desc(&tmB);
-                while (issue_one<Cfg>(st, ring, &tmA, &tmB, p, k_tiles)) {
+                while (issue_one<Cfg>(st, ring, &tmA, &tmB, p, x, k_tiles)) {
                 }
             }
             __syncwarp();
@@ -740,19 +887,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         // ============================================================ consumers
         regs_increase<Cfg::CONSUMER_REGS>();
-        consumer_loop<Cfg>(ring, p, k_tiles, warp - Cfg::PRODUCER_THREADS / 32,
+        consumer_loop<Cfg>(ring, p, x, k_tiles, warp - Cfg::PRODUCER_THREADS / 32,
                            threadIdx.x - Cfg::PRODUCER_THREADS, fix, [] {}, [](int) {});
         named_barrier(BAR_END, 32 + Cfg::CONSUMER_THREADS);
     } else if constexpr (Cfg::ISSUE == ISSUE_THREAD0) {
         if (threadIdx.x == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
-            for (int i = 0; i < STAGES - 1; ++i) issue_one<Cfg>(ist, ring, &tmA, &tmB, p, k_tiles);
+            for (int i = 0; i < STAGES - 1; ++i) issue_one<Cfg>(ist, ring, &tmA, &tmB, p, x, k_tiles);
         }
         consumer_loop<Cfg>(
-            ring, p, k_tiles, warp, threadIdx.x, fix,
+            ring, p, x, k_tiles, warp, threadIdx.x, fix,
             [&] {
-                if (threadIdx.x == 0) issue_one<Cfg>(ist, ring, &tmA, &tmB, p, k_tiles);
+                if (threadIdx.x == 0) issue_one<Cfg>(ist, ring, &tmA, &tmB, p, x, k_tiles);
             },
             [](int) {});
         if (threadIdx.x == 0 && ring.aborted()) drain_copies<Cfg>(ring, ist.issued, p);
@@ -765,14 +912,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (threadIdx.x == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
-            for (int i = 0; i < STAGES; ++i) issue_one<Cfg>(ist, ring, &tmA, &tmB, p, k_tiles);
+            for (int i = 0; i < STAGES; ++i) issue_one<Cfg>(ist, ring, &tmA, &tmB, p, x, k_tiles);
         }
-        consumer_loop<Cfg>(ring, p, k_tiles, warp, threadIdx.x, fix, [] {}, [&](int s) {
+        consumer_loop<Cfg>(ring, p, x, k_tiles, warp, threadIdx.x, fix, [] {}, [&](int s) {
             __threadfence_block();
             if (atomicAdd(&released[s], 1) == Cfg::CONSUMER_WARPS - 1) {
                 released[s] = 0;
                 __threadfence_block();
-                issue_one<Cfg>(ist, ring, &tmA, &tmB, p, k_tiles);
+                issue_one<Cfg>(ist, ring, &tmA, &tmB, p, x, k_tiles);
             }
         });
         // every warp is past its last issue before the copies are counted
@@ -782,17 +929,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 }
 
 // ------------------------------------------------------------------ pre-pass
-// At[k][m] = A[m][k].  64x64 tiles through shared memory, 256 threads: each
-// thread has 16 independent loads in flight (coalesced along k) and then 16
-// stores (coalesced along m).  Block (0,0) also zeroes `zero_count` ints at
-// `zero` (the stream-K tile counters of the GEMM that follows on the stream).
-__global__ void __launch_bounds__(256)
-    pack_a_transpose_kernel(const float *__restrict__ A, long long lda, int M, int K,
-                            float *__restrict__ At, long long ldat, int *zero, int zero_count) {
+// At[k][m] = A[m][k] for one plane.  64x64 tiles through shared memory, 256
+// threads: each thread has 16 independent loads in flight (coalesced along k)
+// and then 16 stores (coalesced along m).
+__device__ __forceinline__ void transpose_plane(const float *__restrict__ A, long long lda, int M,
+                                                int K, float *__restrict__ At, long long ldat) {
     __shared__ float tile[64][65];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;   // 8 warps
-    if (blockIdx.x == 0 && blockIdx.y == 0)
-        for (int i = threadIdx.x; i < zero_count; i += blockDim.x) zero[i] = 0;
     for (long long m0 = (long long)blockIdx.y * 64; m0 < M; m0 += (long long)gridDim.y * 64) {
         for (long long k0 = (long long)blockIdx.x * 64; k0 < K; k0 += (long long)gridDim.x * 64) {
             float v[16];
@@ -824,30 +967,61 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// Bp[k][n] = B[k][n] with a 16-byte row pitch (ldbp % 4 == 0) for the TMA.
+// The pre-pass of a single GEMM.  Block (0,0) also zeroes `zero_count` ints at
+// `zero` (the stream-K tile counters of the GEMM that follows on the stream).
+__global__ void __launch_bounds__(256)
+    pack_a_transpose_kernel(const float *__restrict__ A, long long lda, int M, int K,
+                            float *__restrict__ At, long long ldat, int *zero, int zero_count) {
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        for (int i = threadIdx.x; i < zero_count; i += blockDim.x) zero[i] = 0;
+    transpose_plane(A, lda, M, K, At, ldat);
+}
+
+// The batched pre-pass: plane z = blockIdx.z transposes A + z * stride_a into
+// At + z * at_plane (the host launches at most 65535 planes per call).  Held to
+// 64 registers (four blocks per SM).
+__global__ void __launch_bounds__(256, 4)
+    pack_a_transpose_batched_kernel(const float *__restrict__ A, long long lda, long long stride_a,
+                                    int M, int K, float *__restrict__ At, long long ldat,
+                                    long long at_plane, int *zero, int zero_count) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+        for (int i = threadIdx.x; i < zero_count; i += blockDim.x) zero[i] = 0;
+    transpose_plane(A + (long long)blockIdx.z * stride_a, lda, M, K,
+                    At + (long long)blockIdx.z * at_plane, ldat);
+}
+
+// Bp[k][n] = B[k][n] with a 16-byte row pitch (ldbp % 4 == 0) and a 16-byte
+// plane pitch for the TMA, plane by plane (batch z of B at B + z * stride_b).
 // One block row per k (grid-stride), threads along n.
 __global__ void __launch_bounds__(256)
-    pack_b_copy_kernel(const float *__restrict__ B, long long ldb, int K, int N,
-                       float *__restrict__ Bp, long long ldbp) {
-    for (long long k = blockIdx.y; k < K; k += gridDim.y) {
-        const float *src = B + k * ldb;
-        float *dst = Bp + k * ldbp;
-        for (long long n = (long long)blockIdx.x * blockDim.x + threadIdx.x; n < N;
-             n += (long long)gridDim.x * blockDim.x)
-            dst[n] = __ldcs(src + n);
+    pack_b_copy_kernel(const float *__restrict__ B, long long ldb, long long stride_b, int K,
+                       int N, float *__restrict__ Bp, long long ldbp, long long bp_plane,
+                       int planes) {
+    for (int z = blockIdx.z; z < planes; z += gridDim.z) {
+        for (long long k = blockIdx.y; k < K; k += gridDim.y) {
+            const float *src = B + (long long)z * stride_b + k * ldb;
+            float *dst = Bp + (long long)z * bp_plane + k * ldbp;
+            for (long long n = (long long)blockIdx.x * blockDim.x + threadIdx.x; n < N;
+                 n += (long long)gridDim.x * blockDim.x)
+                dst[n] = __ldcs(src + n);
+        }
     }
 }
 
-// C = beta * C on the M x N block (C not read when beta == 0): the alpha == 0 /
-// K == 0 case, where A and B are not read.
+// C = act(beta * C + bias) on each batch's M x N block (C not read when
+// beta == 0): the alpha == 0 / K == 0 case, where A and B are not read.
 __global__ void __launch_bounds__(256)
-    scale_c_kernel(float *C, long long ldc, int M, int N, float beta) {
-    const long long total = (long long)M * N;
+    scale_c_kernel(float *C, long long ldc, long long stride_c, int M, int N, int batch,
+                   float beta, const float *bias, long long stride_bias, int act) {
+    const long long per = (long long)M * N, total = per * batch;
     for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
-        const long long i = idx / N, j = idx - i * N;
-        float *c = C + i * ldc + j;
-        *c = (beta == 0.0f) ? 0.0f : beta * *c;
+        const long long b = idx / per, rem = idx - b * per;
+        const long long i = rem / N, j = rem - i * N;
+        float *c = C + b * stride_c + i * ldc + j;
+        float v = (beta == 0.0f) ? 0.0f : beta * *c;
+        if (bias) v += bias[b * stride_bias + j];
+        *c = activate(v, act);
     }
 }
 

@@ -103,6 +103,15 @@ __device__ __forceinline__ void tma_load_2d_at(uint32_t smem_dst, const CUtensor
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
         : "memory");
 }
+// 3-D form: (x, y) as above and z the batch.
+__device__ __forceinline__ void tma_load_3d_at(uint32_t smem_dst, const CUtensorMap *map,
+                                               uint32_t bar, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
                                             int x, int y) {
     tma_load_2d_at(smem_addr(smem_dst), map, smem_addr(bar), x, y);

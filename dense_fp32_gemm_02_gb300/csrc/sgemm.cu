@@ -3,7 +3,7 @@
 // descriptor encoding, kernel selection and launch, and benchmark timing hooks.
 //
 // Path of one sgemm() call (all on the caller's stream, no host sync):
-//   1. pack_a_transpose_kernel: A (M x K, any lda) -> At (K x M, paired: K x 2M)
+//   1. pack_a_transpose_kernel: A (M x K, any lda) -> At (K x roundup(M, 4))
 //   2. pack_b_copy_kernel, only when B's address or row pitch is not 16-byte
 //      aligned as the TMA requires
 //   3. sgemm_tma_ffma_kernel: persistent CTAs, TMA ring, FFMA micro-tiles,
@@ -45,7 +45,7 @@ struct Variant {
     int group_m;
     cudaError_t (*set_attr)();
     void (*launch)(int grid, cudaStream_t s, const CUtensorMap &a, const CUtensorMap &b,
-                   const sg::MainParams &p);
+                   const sg::MainParams &p, const sg::ExParams &x);
 };
 
 template <class Cfg>
@@ -56,8 +56,8 @@ cudaError_t set_attr_t() {
 
 template <class Cfg>
 void launch_t(int grid, cudaStream_t s, const CUtensorMap &a, const CUtensorMap &b,
-              const sg::MainParams &p) {
-    sg::sgemm_tma_ffma_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(a, b, p);
+              const sg::MainParams &p, const sg::ExParams &x) {
+    sg::sgemm_tma_ffma_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(a, b, p, x);
 }
 
 template <class Cfg>
@@ -107,6 +107,13 @@ const Variant kVariants[] = {
         "ffma2 tile=256x128x32 stages=4 warps=8+producer_wg thread=16x8 stream_k", true),
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
+
+// Batched calls and calls with a bias or an activation run the default
+// configuration compiled with the batch and fused-epilogue code.
+const Variant kExVariant =
+    make_variant<sg::ExConfig<sg::TileConfig<256, 128, 64, 2, 8, 2, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>>>(
+        "ffma2 tile=256x128x64 stages=2 warps=16 issuer=last_warp thread=8x8 stream_k batched+epilogue",
+        true);
 std::atomic<int> g_forced_variant{-1};
 
 int pick_variant(int M, int N, int K) {
@@ -233,6 +240,7 @@ int device_state(DeviceState **out) {
             cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
             for (const Variant &v : kVariants)
                 if ((e = v.set_attr()) != cudaSuccess) return cuda_fail(e);
+            if ((e = kExVariant.set_attr()) != cudaSuccess) return cuda_fail(e);
             e = cudaFuncSetAttribute(sg::t3::sgemm_3xtf32_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      int(sg::t3::SMEM_BYTES));
@@ -263,45 +271,137 @@ int encode_2d(CUtensorMap *map, const float *ptr, uint64_t inner, uint64_t outer
     return SGEMM_OK;
 }
 
-int launch_scale(cudaStream_t stream, float *C, int ldc, int M, int N, float beta, int sms) {
-    const long long total = (long long)M * N;
+// 3-D tensor map over `planes` row-major matrices of outer x inner floats,
+// rows row_pitch floats apart and planes plane_pitch floats apart; box
+// box_inner x box_outer x 1.
+int encode_3d(CUtensorMap *map, const float *ptr, uint64_t inner, uint64_t outer, uint64_t planes,
+              uint64_t row_pitch_elems, uint64_t plane_pitch_elems, uint32_t box_inner,
+              uint32_t box_outer) {
+    cuuint64_t dims[3] = {inner, outer, planes};
+    cuuint64_t strides[2] = {row_pitch_elems * sizeof(float), plane_pitch_elems * sizeof(float)};
+    cuuint32_t box[3] = {box_inner, box_outer, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(ptr),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        t_last_cuda_error = int(r);
+        return SGEMM_ERR_CUDA;
+    }
+    return SGEMM_OK;
+}
+
+long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
+
+// One call of the FFMA path: `batch` GEMMs with strided operands and the
+// fused epilogue.  sgemm() is batch 1 without bias or activation.
+struct GemmCall {
+    int M, N, K;
+    float alpha;
+    const float *A;
+    int lda;
+    long long stride_a;
+    const float *B;
+    int ldb;
+    long long stride_b;
+    float beta;
+    float *C;
+    int ldc;
+    long long stride_c;
+    int batch;
+    const float *bias;
+    long long stride_bias;
+    int act;
+};
+
+GemmCall plain_call(int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+                    int ldb, float beta, float *C, int ldc) {
+    return GemmCall{M, N, K, alpha, A, lda, 0, B, ldb, 0, beta, C, ldc, 0, 1, nullptr, 0,
+                    sg::ACT_NONE};
+}
+
+// Argument checks of a batched call (the single-GEMM checks plus batch,
+// strides, bias and activation).  Batches of C must not overlap.
+int checked_call(const GemmCall &g) {
+    if (g.batch < 0 || g.stride_a < 0 || g.stride_b < 0 || g.stride_c < 0 || g.stride_bias < 0)
+        return SGEMM_ERR_INVALID_ARG;
+    if (g.act < sg::ACT_NONE || g.act > sg::ACT_GELU) return SGEMM_ERR_INVALID_ARG;
+    // an empty batch, like an empty matrix, reads and writes nothing
+    const bool empty = g.batch == 0;
+    int st = checked_args(g.M, empty ? 0 : g.N, g.K, g.A, g.lda, g.B, g.ldb, g.C,
+                          std::max(g.ldc, empty ? 1 : g.ldc), g.alpha, g.beta);
+    if (st != SGEMM_OK) return st;
+    if (g.M == 0 || g.N == 0 || empty) return SGEMM_OK;
+    if (g.bias && !aligned4(g.bias)) return SGEMM_ERR_INVALID_ARG;
+    if (g.batch > 1 && g.stride_c < (long long)(g.M - 1) * g.ldc + g.N) return SGEMM_ERR_INVALID_ARG;
+    return SGEMM_OK;
+}
+
+int launch_scale(cudaStream_t stream, const GemmCall &g, int sms) {
+    const long long total = (long long)g.M * g.N * g.batch;
     const int blocks = int(std::min<long long>((total + 255) / 256, (long long)sms * 8));
-    sg::scale_c_kernel<<<blocks, 256, 0, stream>>>(C, ldc, M, N, beta);
+    sg::scale_c_kernel<<<blocks, 256, 0, stream>>>(g.C, g.ldc, g.stride_c, g.M, g.N, g.batch,
+                                                   g.beta, g.bias, g.stride_bias, g.act);
     g_launches.fetch_add(1);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? SGEMM_OK : cuda_fail(e);
 }
 
-long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
+// Epilogue and batch parameters of the batched / fused kernel.
+sg::ExParams ex_params(const GemmCall &g, int a_planes, int b_planes) {
+    sg::ExParams x;
+    x.batch = g.batch;
+    x.stride_c = g.stride_c;
+    x.a_planes = a_planes;
+    x.b_planes = b_planes;
+    x.bias = g.bias;
+    x.stride_bias = g.stride_bias;
+    x.bias_vec4 = (g.bias && aligned16(g.bias) && g.stride_bias % 4 == 0) ? 1 : 0;
+    x.act = g.act;
+    return x;
+}
 
-int sgemm_device(int M, int N, int K, float alpha, const float *A, int lda, const float *B,
-                 int ldb, float beta, float *C, int ldc, cudaStream_t stream) {
-    int st = checked_args(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta);
-    if (st != SGEMM_OK || M == 0 || N == 0) return st;
+int gemm_device(const GemmCall &g, cudaStream_t stream) {
+    int st = checked_call(g);
+    if (st != SGEMM_OK || g.M == 0 || g.N == 0 || g.batch == 0) return st;
     DeviceState *dev = nullptr;
     if ((st = device_state(&dev)) != SGEMM_OK) return st;
 
-    if (K == 0 || alpha == 0.0f) return launch_scale(stream, C, ldc, M, N, beta, dev->sm_count);
+    if (g.K == 0 || g.alpha == 0.0f) return launch_scale(stream, g, dev->sm_count);
 
-    const Variant &var = kVariants[pick_variant(M, N, K)];
+    const int M = g.M, N = g.N, K = g.K;
+    const bool extended = g.batch > 1 || g.bias != nullptr || g.act != sg::ACT_NONE;
+    const Variant &var = extended ? kExVariant : kVariants[pick_variant(M, N, K)];
+    // A and B enter as one plane per batch, or one plane for all batches when
+    // their stride is 0
+    const int a_planes = (g.batch > 1 && g.stride_a != 0) ? g.batch : 1;
+    const int b_planes = (g.batch > 1 && g.stride_b != 0) ? g.batch : 1;
     // ---- work split: whole-tile waves, then the leftover tiles' k-slabs spread
     // evenly over all CTAs (stream-K) so the last wave is not partly idle
     const long long tiles_m = (M + var.bm - 1) / var.bm, tiles_n = (N + var.bn - 1) / var.bn;
-    const long long tiles = tiles_m * tiles_n;
+    const long long tiles = tiles_m * tiles_n * g.batch;
     const long long k_tiles = (K + var.bk - 1) / var.bk;
     const int grid = var.stream_k ? int(std::min<long long>(dev->sm_count, tiles * k_tiles))
                                   : int(std::min<long long>(dev->sm_count, tiles));
     const long long dp_tiles = var.stream_k ? (tiles / grid) * grid : tiles;
     const long long sk_tiles = tiles - dp_tiles;
     const long long sk_slabs = sk_tiles * k_tiles;
+    if (tiles > (1LL << 30)) return SGEMM_ERR_TOO_LARGE;
 
     // ---- workspace: transposed A, a re-pitched B if needed, stream-K partial
     // sums and tile counters
     const long long ldat = round_up(M, 4);
-    const bool b_direct = aligned16(B) && (ldb % 4 == 0);
-    const long long ldbp = b_direct ? ldb : round_up(N, 4);
-    const size_t at_bytes = round_up((long long)K * ldat * 4, 256);
-    const size_t bp_bytes = b_direct ? 0 : round_up((long long)K * ldbp * 4, 256);
+    const long long at_plane = round_up((long long)K * ldat, 64);   // 256-byte aligned planes
+    // B is read in place when the TMA can address it: 16-byte base and row
+    // pitch, and (several planes) a 16-byte plane pitch that is at least a
+    // whole matrix
+    const bool b_direct = aligned16(g.B) && (g.ldb % 4 == 0) &&
+                          (b_planes == 1 || (g.stride_b % 4 == 0 && g.stride_b >= (long long)K * g.ldb));
+    const long long ldbp = b_direct ? g.ldb : round_up(N, 4);
+    const long long bp_plane = b_direct ? g.stride_b : round_up((long long)K * ldbp, 64);
+    const size_t at_bytes = size_t(at_plane) * a_planes * 4;
+    const size_t bp_bytes = b_direct ? 0 : size_t(bp_plane) * b_planes * 4;
     const size_t part_bytes = sk_slabs ? size_t(2) * grid * var.bm * var.bn * 4 : 0;
     const size_t cnt_bytes = size_t(sk_tiles) * 4;
     const size_t ws_bytes = at_bytes + bp_bytes + part_bytes + cnt_bytes;
@@ -311,21 +411,35 @@ int sgemm_device(int M, int N, int K, float alpha, const float *A, int lda, cons
     if (e != cudaSuccess) return cuda_fail(e);
     char *wsb = static_cast<char *>(ws);
     float *At = reinterpret_cast<float *>(wsb);
-    float *Bp = b_direct ? const_cast<float *>(B) : reinterpret_cast<float *>(wsb + at_bytes);
+    float *Bp = b_direct ? const_cast<float *>(g.B) : reinterpret_cast<float *>(wsb + at_bytes);
     float *partials = sk_slabs ? reinterpret_cast<float *>(wsb + at_bytes + bp_bytes) : nullptr;
     int *counters = sk_slabs ? reinterpret_cast<int *>(wsb + at_bytes + bp_bytes + part_bytes) : nullptr;
 
     {
         ProfScope prof(stream, false);
-        dim3 pgrid(unsigned(std::min<long long>((K + 63) / 64, 1LL << 20)),
-                   unsigned(std::min<long long>((M + 63) / 64, 65535)));
-        sg::pack_a_transpose_kernel<<<pgrid, 256, 0, stream>>>(A, lda, M, K, At, ldat, counters,
-                                                               int(sk_tiles));
-        g_launches.fetch_add(1);
+        if (a_planes == 1) {
+            dim3 pgrid(unsigned(std::min<long long>((K + 63) / 64, 1LL << 20)),
+                       unsigned(std::min<long long>((M + 63) / 64, 65535)));
+            sg::pack_a_transpose_kernel<<<pgrid, 256, 0, stream>>>(g.A, g.lda, M, K, At, ldat,
+                                                                   counters, int(sk_tiles));
+            g_launches.fetch_add(1);
+        }
+        for (int z0 = 0; a_planes > 1 && z0 < a_planes; z0 += 65535) {
+            const int nz = std::min(a_planes - z0, 65535);
+            dim3 pgrid(unsigned(std::min<long long>((K + 63) / 64, 1LL << 20)),
+                       unsigned(std::min<long long>((M + 63) / 64, 65535)), unsigned(nz));
+            sg::pack_a_transpose_batched_kernel<<<pgrid, 256, 0, stream>>>(
+                g.A + (long long)z0 * g.stride_a, g.lda, g.stride_a, M, K,
+                At + (long long)z0 * at_plane, ldat, at_plane, z0 == 0 ? counters : nullptr,
+                z0 == 0 ? int(sk_tiles) : 0);
+            g_launches.fetch_add(1);
+        }
         if (!b_direct) {
             dim3 bgrid(unsigned(std::min<long long>((N + 255) / 256, 64)),
-                       unsigned(std::min<long long>(K, 65535)));
-            sg::pack_b_copy_kernel<<<bgrid, 256, 0, stream>>>(B, ldb, K, N, Bp, ldbp);
+                       unsigned(std::min<long long>(K, 65535)),
+                       unsigned(std::min(b_planes, 65535)));
+            sg::pack_b_copy_kernel<<<bgrid, 256, 0, stream>>>(g.B, g.ldb, g.stride_b, K, N, Bp,
+                                                              ldbp, bp_plane, b_planes);
             g_launches.fetch_add(1);
         }
     }
@@ -335,33 +449,42 @@ int sgemm_device(int M, int N, int K, float alpha, const float *A, int lda, cons
         return cuda_fail(e);
     }
 
+    // the plain kernel takes 2-D tensor maps, the batched one 3-D maps
     CUtensorMap tmA, tmB;
-    if ((st = encode_2d(&tmA, At, M, K, ldat, var.bm, var.bk)) != SGEMM_OK ||
-        (st = encode_2d(&tmB, Bp, N, K, ldbp, var.bn, var.bk)) != SGEMM_OK) {
+    if (extended) {
+        if ((st = encode_3d(&tmA, At, M, K, a_planes, ldat, at_plane, var.bm, var.bk)) == SGEMM_OK)
+            st = encode_3d(&tmB, Bp, N, K, b_planes, ldbp, b_planes > 1 ? bp_plane : K * ldbp,
+                           var.bn, var.bk);
+    } else {
+        if ((st = encode_2d(&tmA, At, M, K, ldat, var.bm, var.bk)) == SGEMM_OK)
+            st = encode_2d(&tmB, Bp, N, K, ldbp, var.bn, var.bk);
+    }
+    if (st != SGEMM_OK) {
         cudaFreeAsync(ws, stream);
         return st;
     }
 
     sg::MainParams p;
-    p.C = C;
-    p.ldc = ldc;
+    p.C = g.C;
+    p.ldc = g.ldc;
     p.M = M;
     p.N = N;
     p.K = K;
-    p.alpha = alpha;
-    p.beta = beta;
+    p.alpha = g.alpha;
+    p.beta = g.beta;
     p.tiles_m = int(tiles_m);
     p.tiles_n = int(tiles_n);
     p.group_m = var.group_m;
-    p.c_vec4 = (aligned16(C) && ldc % 4 == 0) ? 1 : 0;
+    p.c_vec4 = (aligned16(g.C) && g.ldc % 4 == 0 && (g.batch == 1 || g.stride_c % 4 == 0)) ? 1 : 0;
     p.timeout_ns = g_timeout_ns.load();
     p.dp_tiles = int(dp_tiles);
     p.sk_slabs = sk_slabs;
     p.partials = partials;
     p.counters = counters;
+    const sg::ExParams x = ex_params(g, a_planes, b_planes);
     {
         ProfScope prof(stream, true);
-        var.launch(grid, stream, tmA, tmB, p);
+        var.launch(grid, stream, tmA, tmB, p, x);
         g_launches.fetch_add(1);
     }
     e = cudaGetLastError();
@@ -369,6 +492,11 @@ int sgemm_device(int M, int N, int K, float alpha, const float *A, int lda, cons
     if (e != cudaSuccess) return cuda_fail(e);
     if (ef != cudaSuccess) return cuda_fail(ef);
     return SGEMM_OK;
+}
+
+int sgemm_device(int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+                 int ldb, float beta, float *C, int ldc, cudaStream_t stream) {
+    return gemm_device(plain_call(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc), stream);
 }
 
 // ------------------------------------------------------------------ 3xTF32 path
@@ -439,7 +567,8 @@ int sgemm_device_3xtf32(int M, int N, int K, float alpha, const float *A, int ld
     if (st != SGEMM_OK || M == 0 || N == 0) return st;
     DeviceState *dev = nullptr;
     if ((st = device_state(&dev)) != SGEMM_OK) return st;
-    if (K == 0 || alpha == 0.0f) return launch_scale(stream, C, ldc, M, N, beta, dev->sm_count);
+    if (K == 0 || alpha == 0.0f) return launch_scale(stream, plain_call(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc),
+                            dev->sm_count);
 
     const long long ldk = round_up(K, 4);
     const size_t a_bytes = round_up((long long)M * ldk * 4, 256);
@@ -669,6 +798,7 @@ int noalloc_state(NoAllocState **out) {
             }
             for (const Variant &v : kVariants)
                 if ((e = v.set_attr()) != cudaSuccess) return cuda_fail(e);
+            if ((e = kExVariant.set_attr()) != cudaSuccess) return cuda_fail(e);
             // In host code the array's name is only a host-side stand-in: the
             // kernels must be given its device address.
             void *ptr = nullptr;
@@ -691,7 +821,8 @@ int sgemm_device_noalloc(int M, int N, int K, float alpha, const float *A, int l
     NoAllocState *dev = nullptr;
     if ((st = noalloc_state(&dev)) != SGEMM_OK) return st;
 
-    if (K == 0 || alpha == 0.0f) return launch_scale(stream, C, ldc, M, N, beta, dev->sm_count);
+    if (K == 0 || alpha == 0.0f) return launch_scale(stream, plain_call(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc),
+                            dev->sm_count);
 
     const Variant &var = kVariants[pick_variant(M, N, K)];
     const long long ldat = round_up(M, 4);
@@ -711,7 +842,7 @@ int sgemm_device_noalloc(int M, int N, int K, float alpha, const float *A, int l
     if (!b_direct) {
         dim3 bgrid(unsigned(std::min<long long>((N + 255) / 256, 64)),
                    unsigned(std::min<long long>(K, 65535)));
-        sg::pack_b_copy_kernel<<<bgrid, 256, 0, stream>>>(B, ldb, K, N, Bp, ldbp);
+        sg::pack_b_copy_kernel<<<bgrid, 256, 0, stream>>>(B, ldb, 0, K, N, Bp, ldbp, 0, 1);
         g_launches.fetch_add(1);
     }
     cudaError_t e = cudaGetLastError();
@@ -741,7 +872,8 @@ int sgemm_device_noalloc(int M, int N, int K, float alpha, const float *A, int l
     p.sk_slabs = 0;
     p.partials = nullptr;
     p.counters = nullptr;
-    var.launch(grid_main, stream, tmA, tmB, p);
+    var.launch(grid_main, stream, tmA, tmB, p,
+               ex_params(plain_call(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc), 1, 1));
     g_launches.fetch_add(1);
     e = cudaGetLastError();
     return e == cudaSuccess ? SGEMM_OK : cuda_fail(e);
@@ -754,6 +886,15 @@ SGEMM_API int sgemm(int M, int N, int K, float alpha, const float *A, int lda, c
                     int ldb, float beta, float *C, int ldc, sgemm_stream_t stream) {
     return sgemm_device(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+SGEMM_API int sgemm_ex(int M, int N, int K, float alpha, const float *A, int lda,
+                       long long stride_a, const float *B, int ldb, long long stride_b, float beta,
+                       float *C, int ldc, long long stride_c, int batch, const float *bias,
+                       long long stride_bias, int act, sgemm_stream_t stream) {
+    const GemmCall g{M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b, beta, C, ldc, stride_c,
+                     batch, bias, stride_bias, act};
+    return gemm_device(g, reinterpret_cast<cudaStream_t>(stream));
 }
 
 SGEMM_API int sgemm_host(int M, int N, int K, float alpha, const float *A, int lda,

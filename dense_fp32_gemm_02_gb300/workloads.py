@@ -37,10 +37,18 @@ class Workload:
     check: str = "full"         # full | rows:<n> | rows:<n>+cols:<n>
     note: str = ""
     extra: dict = field(default_factory=dict)
+    batch: int = 1              # independent GEMMs of this shape (sgemm_ex)
+    bias: bool = False          # a per-column bias vector per batch (sgemm_ex)
+    act: str = "none"           # none | relu | gelu (sgemm_ex)
 
     @property
     def flops(self) -> float:
-        return 2.0 * self.M * self.N * self.K
+        return 2.0 * self.M * self.N * self.K * self.batch
+
+    @property
+    def extended(self) -> bool:
+        """True when the workload needs sgemm_ex (batches, bias or activation)."""
+        return self.batch > 1 or self.bias or self.act != "none"
 
     def lds(self):
         return (self.lda or self.K, self.ldb or self.N, self.ldc or self.N)
@@ -60,6 +68,15 @@ WORKLOADS = {
     "sgemm_16384x16384x512": Workload("sgemm_16384x16384x512", 16384, 16384, 512, 1.0, 0.0,
                                       "normal", "normal", None, 1005, check="rows:128",
                                       note="short K, epilogue heavy"),
+    # the adjacent uses of the same main loop: many independent GEMMs in one
+    # call, and the GEMM of a neural-network layer with its bias and activation
+    "sgemm_batched_64x1024": Workload("sgemm_batched_64x1024", 1024, 1024, 1024, 1.0, 0.0,
+                                      "upm1", "upm1", None, 1006, check="rows:16", batch=64,
+                                      note="64 independent 1024^3 GEMMs in one call"),
+    "sgemm_8192_bias_gelu": Workload("sgemm_8192_bias_gelu", 8192, 8192, 8192, 1.0, 0.0,
+                                     "upm1", "upm1", None, 1007, check="rows:64",
+                                     bias=True, act="gelu",
+                                     note="layer form: bias per output column, then GELU"),
 }
 
 # The timed workload of the benchmark.
@@ -112,8 +129,26 @@ def make_inputs(M, N, K, dist_a="upm1", dist_b="upm1", dist_c=None, seed=0,
 
 
 def workload_inputs(w: Workload):
+    """(A, B, C_in) of a workload; for batch > 1, arrays (batch, rows, cols) with
+    batch b drawn from seed + 7919 * b (compact leading dimensions)."""
     lda, ldb, ldc = w.lds()
-    return make_inputs(w.M, w.N, w.K, w.dist_a, w.dist_b, w.dist_c, w.seed, lda, ldb, ldc)
+    if w.batch == 1:
+        return make_inputs(w.M, w.N, w.K, w.dist_a, w.dist_b, w.dist_c, w.seed, lda, ldb, ldc)
+    parts = [make_inputs(w.M, w.N, w.K, w.dist_a, w.dist_b, w.dist_c, w.seed + 7919 * b)
+             for b in range(w.batch)]
+    A = np.stack([p[0] for p in parts])
+    B = np.stack([p[1] for p in parts])
+    C = np.stack([p[2] for p in parts]) if w.dist_c is not None else None
+    return A, B, C
+
+
+def workload_bias(w: Workload):
+    """The bias of a workload: float32 (batch, N) drawn N(0, 1) from seed + 17,
+    or None."""
+    if not w.bias:
+        return None
+    rng = np.random.default_rng(w.seed + 17)
+    return rng.standard_normal((w.batch, w.N), dtype=np.float32)
 
 
 def sample_indices(w: Workload):

@@ -54,8 +54,8 @@ typedef enum {
  * A, B, C: device pointers owned by the caller; the library keeps no reference
  * after the call returns.  The work is enqueued on `stream` and the call returns
  * without synchronising.  A, B and C must stay valid until that work completes.
- * The library may use a device workspace for a transposed copy of A (K x M
- * floats, twice that for the packed-FP32x2 micro-kernel) and, when B's row
+ * The library may use a device workspace for a transposed copy of A (K rows of
+ * M floats, M rounded up to a multiple of 4) and, when B's row
  * pitch or address does not meet the 16-byte rule of the tensor-memory
  * accelerator, a padded copy of B.  The workspace comes from a stream-ordered
  * memory pool owned by the library (one per device) and is returned to it on
@@ -70,6 +70,49 @@ int sgemm(int M, int N, int K, float alpha,
           const float *B, int ldb,
           float beta, float *C, int ldc,
           sgemm_stream_t stream);
+
+/* Activation of the fused epilogue of sgemm_ex. */
+typedef enum {
+    SGEMM_ACT_NONE = 0, /* identity */
+    SGEMM_ACT_RELU = 1, /* max(z, 0) */
+    SGEMM_ACT_GELU = 2  /* z * Phi(z) = 0.5 z (1 + erf(z / sqrt 2)) */
+} sgemm_act;
+
+/*
+ * sgemm_ex -- strided batched GEMM with a fused bias and activation, on device
+ * memory, asynchronous on `stream`.
+ *
+ * For b = 0 .. batch-1, with X_b = X + b * stride_x (strides in elements):
+ *
+ *   C_b[i][j] = act( alpha * sum_k A_b[i][k] * B_b[k][j] + beta * C_b[i][j] + bias_b[j] )
+ *
+ * Row-major like sgemm, with the same leading-dimension rules.  The article
+ * "How to implement matrix multiplication efficiently? An introduction from a
+ * CUDA beginner's view" (introduction) motivates the GEMM by neural-network
+ * layers and names operator fusion with it as the next step; it fixes neither
+ * a bias nor an activation, so this entry point takes the layer form: a bias
+ * per output column (broadcast over the rows; bias == NULL for none) and an
+ * element-wise activation `act` (sgemm_act).  batch == 1, bias == NULL and
+ * SGEMM_ACT_NONE is exactly sgemm().
+ *
+ * stride_a or stride_b 0 means every batch uses the same A or B.  Batches of C
+ * must not overlap: batch > 1 requires stride_c >= (M - 1) * ldc + N.  C is not
+ * read when beta == 0; when K == 0 or alpha == 0, A and B are not read and
+ * C_b = act(beta * C_b + bias_b).  Ownership, workspace and asynchrony are as
+ * for sgemm(); the workspace holds one transposed A per batch (one when
+ * stride_a == 0).
+ *
+ * Errors: SGEMM_ERR_INVALID_ARG for a negative size, batch or stride, an
+ * unknown `act`, a bias pointer not 4-byte aligned, overlapping batches of C,
+ * or any condition sgemm() rejects; batch == 0 (like M == 0 or N == 0) is a
+ * successful no-op.  The other codes are those of sgemm().
+ */
+int sgemm_ex(int M, int N, int K, float alpha,
+             const float *A, int lda, long long stride_a,
+             const float *B, int ldb, long long stride_b,
+             float beta, float *C, int ldc, long long stride_c,
+             int batch, const float *bias, long long stride_bias, int act,
+             sgemm_stream_t stream);
 
 /*
  * sgemm_host -- the same GEMM on HOST buffers; synchronous.

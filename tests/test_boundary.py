@@ -136,3 +136,43 @@ def test_binding_loads_and_reports_config():
     with pytest.raises(binding.SgemmError) as e:
         binding.check(1)
     assert "INVALID_ARG" in str(e.value)
+
+
+def _call_ex(lib, M=4, N=4, K=4, batch=2, stride_a=16, stride_b=16, stride_c=16, bias=None,
+             stride_bias=0, act=0, C=3):
+    f = lib.sgemm_ex
+    ll = ctypes.c_longlong
+    f.argtypes = [ctypes.c_int] * 3 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_int, ll,
+                                       ctypes.c_void_p, ctypes.c_int, ll, ctypes.c_float,
+                                       ctypes.c_void_p, ctypes.c_int, ll, ctypes.c_int,
+                                       ctypes.c_void_p, ll, ctypes.c_int, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    # fake, never-dereferenced, 16-byte aligned addresses (validation comes first)
+    ptr = lambda v: None if v is None else 0x100000 * v
+    return f(M, N, K, 1.0, ptr(1), max(1, K), stride_a, ptr(2), max(1, N), stride_b, 0.0,
+             ptr(C), max(1, N), stride_c, batch, bias, stride_bias, act, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(batch=-1), dict(stride_a=-1), dict(stride_b=-4), dict(stride_c=-16),
+    dict(stride_bias=-1, bias=0x400000), dict(act=3), dict(act=-1),
+    dict(bias=0x400001),                       # bias not 4-byte aligned
+    dict(stride_c=15),                         # batches of C overlap: (M-1)*ldc + N = 16
+    dict(M=-1), dict(C=None),
+])
+def test_ex_invalid_arguments_rejected_without_gpu(lib, kw):
+    assert _call_ex(lib, **kw) == 1  # SGEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(batch=0), dict(M=0), dict(N=0, stride_c=0),
+                                dict(batch=0, C=None, stride_c=0)])
+def test_ex_empty_is_a_no_op_without_gpu(lib, kw):
+    assert _call_ex(lib, **kw) == 0
+
+
+def test_ex_single_batch_needs_no_c_stride(lib):
+    # batch 1: stride_c is irrelevant, so 0 is accepted (rejected only if it were
+    # needed); validation happens before any CUDA call, so on a machine without a
+    # GPU the call gets as far as the device check
+    st = _call_ex(lib, batch=1, stride_c=0, stride_a=0, stride_b=0)
+    assert st != 1
