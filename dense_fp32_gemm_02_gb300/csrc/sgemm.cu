@@ -528,12 +528,14 @@ int t3_run(int M, int N, int K, float alpha, const float *A, int lda, const floa
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
-    CUtensorMap mAh, mAl, mBh, mBl;
+    CUtensorMap mAh, mAl, mBh, mBl, mBh2, mBl2;   // *2: boxes of BN/2 rows (half-width tiles)
     const auto sw = t3::ROW_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     if ((st = encode_2d(&mAh, Ah, K, M, ldk, t3::BK, t3::BM, sw)) != SGEMM_OK ||
         (st = encode_2d(&mAl, Al, K, M, ldk, t3::BK, t3::BM, sw)) != SGEMM_OK ||
         (st = encode_2d(&mBh, Bh, K, N, ldk, t3::BK, t3::BN, sw)) != SGEMM_OK ||
-        (st = encode_2d(&mBl, Bl, K, N, ldk, t3::BK, t3::BN, sw)) != SGEMM_OK)
+        (st = encode_2d(&mBl, Bl, K, N, ldk, t3::BK, t3::BN, sw)) != SGEMM_OK ||
+        (st = encode_2d(&mBh2, Bh, K, N, ldk, t3::BK, t3::BN / 2, sw)) != SGEMM_OK ||
+        (st = encode_2d(&mBl2, Bl, K, N, ldk, t3::BK, t3::BN / 2, sw)) != SGEMM_OK)
         return st;
     t3::Params p;
     p.C = C;
@@ -553,7 +555,7 @@ int t3_run(int M, int N, int K, float alpha, const float *A, int lda, const floa
     {
         ProfScope prof(stream, true);
         t3::sgemm_3xtf32_kernel<<<grid, t3::THREADS, t3::SMEM_BYTES, stream>>>(mAh, mAl, mBh,
-                                                                               mBl, p);
+                                                                               mBl, mBh2, mBl2, p);
         g_launches.fetch_add(1);
     }
     e = cudaGetLastError();

@@ -7,7 +7,8 @@
 // 3 * 2^-22, inside the FP32 tolerance 1e-6*K*|alpha|*sum|A||B| for every K.
 //
 // Kernel layout (persistent: one CTA per SM walks 128 x 256 output tiles
-// b, b + gridDim.x, ...; 256 threads):
+// b, b + gridDim.x, ...; a last wave of at most half the SMs is cut into
+// 128 x 128 tiles, one per SM; 256 threads):
 //   warp 0    thread 0 issues TMA copies of A_hi, A_lo (128 x 16) and B_hi,
 //             B_lo (256 x 16, B transposed so both operands are K-major) into
 //             a 4-stage ring, 64-byte swizzled;
@@ -42,6 +43,7 @@ constexpr int A_TILE = BM * BK;                       // floats, 16 KB
 constexpr int B_TILE = BN * BK;                       // floats, 32 KB
 constexpr int STAGE_FLOATS = 2 * A_TILE + 2 * B_TILE; // A_hi, A_lo, B_hi, B_lo
 constexpr uint32_t STAGE_BYTES = STAGE_FLOATS * 4u;   // 96 KB
+constexpr uint32_t STAGE_BYTES_HALF = STAGE_BYTES - uint32_t(B_TILE) * 4u;   // B boxes of BN/2 rows
 constexpr int THREADS = 256;
 constexpr int EPI_WARPS = 4;                          // warps 4..7
 constexpr uint32_t ACC_COLS = 256;                    // 128 lanes x 256 fp32 columns
@@ -60,6 +62,8 @@ constexpr uint32_t IDESC = (1u << 4)                    // D format: f32
                            | (2u << 10)                 // B format: tf32
                            | (uint32_t(BN >> 3) << 17)  // N / 8
                            | (uint32_t(BM >> 4) << 24); // M / 16
+// The same with N = 128, for the half-width tiles of the last wave.
+constexpr uint32_t IDESC_HALF = (IDESC & ~(0x3Fu << 17)) | (uint32_t((BN / 2) >> 3) << 17);
 
 // Shared-memory matrix descriptor: K-major operand, rows of ROW_BYTES with the
 // matching swizzle (the layout the TMA writes), 8-row groups 8 rows apart.
@@ -88,11 +92,11 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 
 // D (tmem) = A * B (+ D when accumulate != 0)
 __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t accumulate) {
+                                         uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(IDESC), "r"(accumulate)
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -150,9 +154,47 @@ struct Params {
     unsigned long long timeout_ns;
 };
 
+// Work of CTA b: its whole tiles t = b, b + G, ... below `full`, then, when
+// the last partial wave holds at most G/2 tiles, that wave cut into
+// half-width tiles (BM x BN/2) h = b, b + G, ... below 2 * (tiles - full), so
+// the last wave takes half as long.  Item j of the CTA: tile coordinates, the
+// first output column and the width (BN or BN/2).
+struct WorkPlan {
+    int full;      // whole tiles
+    int halves;    // half-width tiles after them
+    int mine_full, mine;
+
+    __device__ void init(const Params &p) {
+        const int G = gridDim.x, b = blockIdx.x;
+        const int tiles = p.tiles_m * p.tiles_n;
+        const int tail = tiles % G;
+        full = (tail != 0 && 2 * tail <= G) ? tiles - tail : tiles;
+        halves = 2 * (tiles - full);
+        mine_full = b < full ? (full - 1 - b) / G + 1 : 0;
+        const int mine_half = b < halves ? (halves - 1 - b) / G + 1 : 0;
+        mine = mine_full + mine_half;
+    }
+
+    __device__ void item(const Params &p, int j, int &tm, int &col0, int &ncols) const {
+        int tn;
+        if (j < mine_full) {
+            tile_coords(blockIdx.x + j * gridDim.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            col0 = tn * BN;
+            ncols = BN;
+        } else {
+            const int h = blockIdx.x + (j - mine_full) * gridDim.x;
+            tile_coords(full + h / 2, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            col0 = tn * BN + (h & 1) * (BN / 2);
+            ncols = BN / 2;
+        }
+    }
+};
+
 __global__ void __launch_bounds__(THREADS, 1)
     sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
                         const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl,
+                        const __grid_constant__ CUtensorMap tmBh2,
+                        const __grid_constant__ CUtensorMap tmBl2,
                         const Params p) {
     extern __shared__ unsigned char smem_raw[];
     const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
@@ -186,8 +228,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t taddr = *tmem_base;
 
-    const int num_tiles = p.tiles_m * p.tiles_n;
-    const int my_tiles = blockIdx.x < num_tiles ? (num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    WorkPlan plan;
+    plan.init(p);
+    const int my_tiles = plan.mine;
     const int k_tiles = (p.K + BK - 1) / BK;
 
     if (warp == 0) {
@@ -197,12 +240,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_prefetch_desc(&tmAl);
             tma_prefetch_desc(&tmBh);
             tma_prefetch_desc(&tmBl);
+            tma_prefetch_desc(&tmBh2);
+            tma_prefetch_desc(&tmBl2);
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
             for (int j = 0; j < my_tiles && !*abort_flag; ++j) {
-                int tm, tn;
-                tile_coords(blockIdx.x + j * gridDim.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                int tm, col0, ncols;
+                plan.item(p, j, tm, col0, ncols);
                 for (int kb = 0; kb < k_tiles; ++kb) {
                     if (*abort_flag) break;
                     // first use of a stage: parity 1 counts as complete
@@ -212,11 +257,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     float *st = ring + stage * STAGE_FLOATS;
-                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                    mbar_arrive_expect_tx(&full[stage], ncols == BN ? STAGE_BYTES : STAGE_BYTES_HALF);
                     tma_load_2d(st, &tmAh, &full[stage], kb * BK, tm * BM);
                     tma_load_2d(st + A_TILE, &tmAl, &full[stage], kb * BK, tm * BM);
-                    tma_load_2d(st + 2 * A_TILE, &tmBh, &full[stage], kb * BK, tn * BN);
-                    tma_load_2d(st + 2 * A_TILE + B_TILE, &tmBl, &full[stage], kb * BK, tn * BN);
+                    // a half-width tile copies BN/2-row boxes of B (tmBh2, tmBl2) into
+                    // the first half of each B region
+                    const bool half = ncols != BN;
+                    tma_load_2d(st + 2 * A_TILE, half ? &tmBh2 : &tmBh, &full[stage], kb * BK, col0);
+                    tma_load_2d(st + 2 * A_TILE + B_TILE, half ? &tmBl2 : &tmBl, &full[stage],
+                                kb * BK, col0);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -251,6 +300,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d = taddr + uint32_t(a) * ACC_COLS;
+                int tm_unused, col_unused, ncols;
+                plan.item(p, j, tm_unused, col_unused, ncols);
+                const uint32_t idesc = ncols == BN ? IDESC : IDESC_HALF;
                 for (int kb = 0; kb < k_tiles; ++kb) {
                     if (*abort_flag || !mbar_wait(&full[stage], phase, p.timeout_ns)) {
                         if (!*abort_flag) atomicOr(&g_error_word, ERR_FULL_WAIT);
@@ -267,9 +319,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int kk = 0; kk < BK / 8; ++kk) {
                         const uint32_t off = uint32_t(kk) * 32u;   // 8 tf32 = 32 bytes along K
                         const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-                        mma_tf32(d, smem_desc_sw(al + off), smem_desc_sw(bh + off), acc);
-                        mma_tf32(d, smem_desc_sw(ah + off), smem_desc_sw(bl + off), 1u);
-                        mma_tf32(d, smem_desc_sw(ah + off), smem_desc_sw(bh + off), 1u);
+                        mma_tf32(d, smem_desc_sw(al + off), smem_desc_sw(bh + off), idesc, acc);
+                        mma_tf32(d, smem_desc_sw(ah + off), smem_desc_sw(bl + off), idesc, 1u);
+                        mma_tf32(d, smem_desc_sw(ah + off), smem_desc_sw(bh + off), idesc, 1u);
                     }
                     mma_commit(&empty[stage]);     // stage free once these MMAs have read it
                     if (++stage == STAGES) {
@@ -303,16 +355,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
             }
             tc_fence_after();
-            int tm, tn;
-            tile_coords(blockIdx.x + j * gridDim.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            int tm, col0, ncols;
+            plan.item(p, j, tm, col0, ncols);
             const int row0 = tm * BM + quarter * 32;
             const uint32_t src = taddr + uint32_t(a) * ACC_COLS + (uint32_t(quarter * 32) << 16);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < ncols / 32; ++c) {
                 float v[32];
                 __syncwarp();   // tcgen05.ld is warp-collective; buf reuse
                 tmem_load32(src + uint32_t(c * 32), v);
-                if (c == BN / 32 - 1) {
+                if (c == ncols / 32 - 1) {
                     // all of this accumulator is in registers: hand it back
                     tc_fence_before();
                     __syncwarp();
@@ -323,7 +375,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __syncwarp();
                 // row r of the block: lane = column; C rows read and written
                 // 128 contiguous bytes at a time, all 32 loads in flight first
-                const int col = tn * BN + c * 32 + lane;
+                const int col = col0 + c * 32 + lane;
                 const bool col_ok = col < p.N;
                 float cin[32];
 #pragma unroll
