@@ -354,7 +354,8 @@ def measure_tf32x3(args, w, binding, dA, dB, dC, C, stream, world, device):
         raise RuntimeError("device error word set during the 3xTF32 timed region")
     ms = max_over_ranks(world, start.elapsed_time(stop), device) / args.steps
     main_ms = prof["main_ms"] / max(1, prof["main_launches"])
-    split_ms = prof["pack_ms"] / max(1, prof["pack_launches"]) if prof["pack_launches"] else 0.0
+    # all pre-pass launches of a step (split of A and split+transpose of B)
+    split_ms = prof["pack_ms"] / args.steps
     peak, src = tensor_peak_tf32()
     mma_tflops = 3.0 * w.flops / (main_ms * 1e-3) / 1e12
     out = {
@@ -516,7 +517,8 @@ def run_ours(args):
 
     # ---- roofline of the main kernel
     main_ms = prof["main_ms"] / max(1, prof["main_launches"])
-    pack_ms = prof["pack_ms"] / max(1, prof["pack_launches"]) if prof["pack_launches"] else 0.0
+    # all pre-pass launches of a step (transposes, re-pitching copies, splits)
+    pack_ms = prof["pack_ms"] / args.steps
     peak_tflops = sms * FFMA_PER_SM_PER_CLK * 2 * SM_MAX_MHZ_FALLBACK * 1e6 / 1e12
     peak_meas_clk = (sms * FFMA_PER_SM_PER_CLK * 2 * clk["sm_mhz"] * 1e6 / 1e12
                      if clk.get("sm_mhz") else None)

@@ -523,6 +523,7 @@ int t3_run(int M, int N, int K, float alpha, const float *A, int lda, const floa
     {
         const int vec4 = (aligned16(A) && lda % 4 == 0 && K % 4 == 0) ? 1 : 0;
         dim3 ga(unsigned(std::min<long long>((K + 4095) / 4096, 64)), unsigned(std::min(M, 65535)));
+        ProfScope prof(stream, false);
         t3::split_a_kernel<<<ga, 256, 0, stream>>>(A, lda, M, K, Ah, Al, ldk, vec4);
         g_launches.fetch_add(1);
     }
