@@ -190,6 +190,28 @@ def l2_note(w):
     return f"A, B, C {mb:.0f} MB, not larger than the 129 MB L2: no flush, L2 partly warm"
 
 
+def time_e2e(step, w, steps, world, device, entry_point, h2d_bytes, d2h_bytes):
+    """End-to-end timing of a host-buffer call: two untimed calls, then `steps`
+    calls timed one by one on the host clock (each call returns with C on the
+    host).  The value is taken at the median call (host-side copies make single
+    calls noisy); the mean and the minimum are reported beside it."""
+    for _ in range(2):
+        step()
+    barrier(world, device)
+    times = []
+    for _ in range(steps):
+        t = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t)
+    med = max_over_ranks(world, statistics.median(times), device)
+    mean = max_over_ranks(world, sum(times) / len(times), device)
+    return {"value": round(w.flops / med / 1e9 * world, 3), "unit": "GFLOP/s",
+            "entry_point": entry_point, "h2d_bytes_per_step": h2d_bytes,
+            "d2h_bytes_per_step": d2h_bytes, "ms_per_step": round(med * 1e3, 3),
+            "ms_mean": round(mean * 1e3, 3), "ms_min": round(min(times) * 1e3, 3),
+            "statistic": "median of the timed calls"}
+
+
 def oracle_rows_fn(w, A, B, C):
     """f(idx): the oracle as it stands on full rows idx of the workload (batch 0
     of a batched one, with its bias and activation)."""
@@ -380,18 +402,9 @@ def measure_tf32x3(args, w, binding, dA, dB, dC, C, stream, world, device):
         def e2e_step():
             binding.sgemm_host(hA, hB, hC, w.alpha, w.beta, stream=stream, tensor_cores=True)
 
-        e2e_step()
-        barrier(world, device)
-        t = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
-        e2e_s = max_over_ranks(world, time.perf_counter() - t, device)
-        out["e2e"] = {"value": round(w.flops * args.steps / e2e_s / 1e9 * world, 3),
-                      "unit": "GFLOP/s", "entry_point": "sgemm_host_3xtf32",
-                      "h2d_bytes_per_step": (hA.numel() + hB.numel()
-                                             + (hC.numel() if w.beta != 0 else 0)) * 4,
-                      "d2h_bytes_per_step": hC.numel() * 4,
-                      "ms_per_step": round(e2e_s / args.steps * 1e3, 3)}
+        out["e2e"] = time_e2e(e2e_step, w, args.steps, world, device, "sgemm_host_3xtf32",
+                              (hA.numel() + hB.numel() + (hC.numel() if w.beta != 0 else 0)) * 4,
+                              hC.numel() * 4)
     return out
 
 
@@ -486,20 +499,12 @@ def run_ours(args):
         hC = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
         if hC0 is not None:
             hC.copy_(hC0)
-        binding.sgemm_host(hA, hB, hC, w.alpha, w.beta, stream=stream)   # warm
-        barrier(world, device)
-        t = time.perf_counter()
         te0 = time.time()
-        for _ in range(args.steps):
-            binding.sgemm_host(hA, hB, hC, w.alpha, w.beta, stream=stream)
-        e2e_s = time.perf_counter() - t
+        e2e = time_e2e(lambda: binding.sgemm_host(hA, hB, hC, w.alpha, w.beta, stream=stream),
+                       w, args.steps, world, device, "sgemm_host",
+                       (hA.numel() + hB.numel() + (hC.numel() if w.beta != 0 else 0)) * 4,
+                       hC.numel() * 4)
         clocks.mark(te0, time.time())
-        e2e_s = max_over_ranks(world, e2e_s, device)
-        h2d = (hA.numel() + hB.numel() + (hC.numel() if w.beta != 0 else 0)) * 4
-        d2h = hC.numel() * 4
-        e2e = {"value": round(w.flops * args.steps / e2e_s / 1e9 * world, 3), "unit": "GFLOP/s",
-               "entry_point": "sgemm_host", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(e2e_s / args.steps * 1e3, 3)}
     main_windows = list(clocks.windows)
     tf32x3 = None
     if args.path == "ffma" and not args.no_tf32x3 and not w.extended:

@@ -636,11 +636,12 @@ struct EventSet {
     }
 };
 
-// The host-buffer GEMM, pipelined over row blocks of A and C: B goes in first;
-// then block i of A (and of C when beta != 0) is copied in on the h2d stream,
-// multiplied on the caller's stream while block i+1 is copied in, and copied
-// back on the d2h stream while block i+1 is multiplied.  `tensor` selects the
-// 3xTF32 path (B is split once, each block of A is split with its GEMM).
+// The host-buffer GEMM, pipelined over row blocks of A and C: block i of A
+// (and of C when beta != 0) is copied in on the h2d stream, multiplied on the
+// caller's stream while block i+1 is copied in, and copied back on the d2h
+// stream while block i+1 is multiplied.  B follows block 0 in k-chunks, and
+// block 0 is multiplied chunk by chunk as they land.  `tensor` selects the
+// 3xTF32 path (B is split chunk by chunk, each block of A with its GEMM).
 int host_gemm(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
               float beta, float *C, int ldc, cudaStream_t stream, bool tensor) {
     int st = checked_args(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta);
@@ -684,22 +685,20 @@ int host_gemm(int M, int N, int K, float alpha, const float *A, int lda, const f
         cudaStreamSynchronize(stream);
         return code;
     };
-    cudaEvent_t allocated = evs.make(), b_ready = evs.make(), done = evs.make();
-    if (!allocated || !b_ready || !done) return fail(SGEMM_ERR_CUDA);
+    cudaEvent_t allocated = evs.make(), done = evs.make();
+    if (!allocated || !done) return fail(SGEMM_ERR_CUDA);
     // the copy streams may touch the buffer only after its allocation on `stream`
     if ((e = cudaEventRecord(allocated, stream)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(cs->h2d, allocated, 0)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(cs->d2h, allocated, 0)) != cudaSuccess)
         return fail(cuda_fail(e));
-    if (need_ab) {
-        e = cudaMemcpy2DAsync(dB, size_t(N) * 4, B, size_t(ldb) * 4, size_t(N) * 4, size_t(K),
-                              cudaMemcpyHostToDevice, cs->h2d);
-        if (e == cudaSuccess) e = cudaEventRecord(b_ready, cs->h2d);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, b_ready, 0);
-        if (e != cudaSuccess) return fail(cuda_fail(e));
-        if (tensor && (st = t3_split_b(N, K, dB, N, Bh, Bl, ldk, stream)) != SGEMM_OK)
-            return fail(st);
-    }
+    // Block 0 is multiplied in k-chunks as the matching rows of B arrive, so
+    // the first GEMM starts after a quarter of B is in rather than all of it:
+    // copy order A_0, C_0, B chunk by chunk, then A_i, C_i of the later blocks.
+    // Later chunks accumulate into C_0 (beta = 1), which changes the rounding
+    // of block 0 but not its bound.
+    const int kchunks = (need_ab && K >= 4096) ? 4 : 1;
+    const int kc = need_ab ? int(round_up((K + kchunks - 1) / kchunks, 64)) : 0;
     for (int blk = 0; blk < nblk; ++blk) {
         const int r0 = blk * rows_per_blk;
         const int rows = std::min(rows_per_blk, M - r0);
@@ -716,18 +715,45 @@ int host_gemm(int M, int N, int K, float alpha, const float *A, int lda, const f
                                   size_t(ldc) * 4, size_t(N) * 4, size_t(rows),
                                   cudaMemcpyHostToDevice, cs->h2d);
         if (e == cudaSuccess) e = cudaEventRecord(in, cs->h2d);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, in, 0);
         if (e != cudaSuccess) return fail(cuda_fail(e));
         const float *a_blk = need_ab ? dA + (size_t)r0 * K : nullptr;
         float *c_blk = dC + (size_t)r0 * N;
-        if (!need_ab)
+        if (!need_ab) {
+            if ((e = cudaStreamWaitEvent(stream, in, 0)) != cudaSuccess) return fail(cuda_fail(e));
             st = sgemm_device(rows, N, K, alpha, nullptr, std::max(1, K), nullptr, std::max(1, N),
                               beta, c_blk, N, stream);
-        else if (tensor)
-            st = t3_run(rows, N, K, alpha, a_blk, K, Bh, Bl, ldk, beta, c_blk, N, Ah, Al,
-                        dev->sm_count, stream);
-        else
-            st = sgemm_device(rows, N, K, alpha, a_blk, K, dB, N, beta, c_blk, N, stream);
+        } else if (blk == 0) {
+            for (int c = 0; c < kchunks; ++c) {
+                const int k0 = c * kc, kn = std::min(kc, K - k0);
+                if (kn <= 0) break;
+                cudaEvent_t bin = evs.make();
+                if (!bin) return fail(SGEMM_ERR_CUDA);
+                e = cudaMemcpy2DAsync(dB + (size_t)k0 * N, size_t(N) * 4, B + (size_t)k0 * ldb,
+                                      size_t(ldb) * 4, size_t(N) * 4, size_t(kn),
+                                      cudaMemcpyHostToDevice, cs->h2d);
+                if (e == cudaSuccess) e = cudaEventRecord(bin, cs->h2d);
+                if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, bin, 0);
+                if (e != cudaSuccess) return fail(cuda_fail(e));
+                const float beta_c = c == 0 ? beta : 1.0f;
+                if (tensor) {
+                    if ((st = t3_split_b(N, kn, dB + (size_t)k0 * N, N, Bh + k0, Bl + k0, ldk,
+                                         stream)) != SGEMM_OK)
+                        return fail(st);
+                    st = t3_run(rows, N, kn, alpha, a_blk + k0, K, Bh + k0, Bl + k0, ldk, beta_c,
+                                c_blk, N, Ah, Al, dev->sm_count, stream);
+                } else {
+                    st = sgemm_device(rows, N, kn, alpha, a_blk + k0, K, dB + (size_t)k0 * N, N,
+                                      beta_c, c_blk, N, stream);
+                }
+                if (st != SGEMM_OK) return fail(st);
+            }
+        } else {
+            // block i >= 1: its copies follow all of B on the copy stream
+            if ((e = cudaStreamWaitEvent(stream, in, 0)) != cudaSuccess) return fail(cuda_fail(e));
+            st = tensor ? t3_run(rows, N, K, alpha, a_blk, K, Bh, Bl, ldk, beta, c_blk, N, Ah, Al,
+                                 dev->sm_count, stream)
+                        : sgemm_device(rows, N, K, alpha, a_blk, K, dB, N, beta, c_blk, N, stream);
+        }
         if (st != SGEMM_OK) return fail(st);
         e = cudaEventRecord(out, stream);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(cs->d2h, out, 0);

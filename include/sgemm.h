@@ -118,16 +118,19 @@ int sgemm_ex(int M, int N, int K, float alpha,
  * sgemm_host -- the same GEMM on HOST buffers; synchronous.
  *
  * A, B, C are host pointers (page-locked memory gives the fastest copies, but
- * pageable memory is accepted).  The call copies B to the device, then works
- * through row blocks of A and C (up to 8 blocks of at least 1024 rows): block
- * i is copied in on a host-to-device copy stream, multiplied on `stream` while
- * block i+1 is copied in, and copied back into C (respecting ldc) on a
- * device-to-host copy stream while block i+1 is multiplied.  Device buffers
- * come from the library pool; the two copy streams are the library's own (one
- * pair per device).  `stream` is synchronised before returning, so C holds
- * the result on return.  Results meet the same tolerance as sgemm(); when the
- * rows are split into blocks they need not be bitwise equal to one sgemm() call
- * on the whole matrix (the k split of leftover tiles depends on the shape).
+ * pageable memory is accepted).  The call works through row blocks of A and C
+ * (up to 8 blocks of at least 1024 rows): block i is copied in on a
+ * host-to-device copy stream, multiplied on `stream` while block i+1 is copied
+ * in, and copied back into C (respecting ldc) on a device-to-host copy stream
+ * while block i+1 is multiplied.  B is copied after block 0, in four k-chunks
+ * when K >= 4096, and block 0 is multiplied chunk by chunk (accumulating into
+ * its C rows) as the chunks land, so the first GEMM need not wait for all of
+ * B.  Device buffers come from the library pool; the two copy streams are the
+ * library's own (one pair per device).  `stream` is synchronised before
+ * returning, so C holds the result on return.  Results meet the same
+ * tolerance as sgemm(); they need not be bitwise equal to one sgemm() call on
+ * the whole matrix (row blocks change the k split of leftover tiles, and the
+ * k-chunks of block 0 round its partial sums in C).
  */
 int sgemm_host(int M, int N, int K, float alpha,
                const float *A, int lda,

@@ -284,3 +284,30 @@ def test_host_entry_point_pipelined_over_row_blocks(tensor_cores, pinned):
     assert_within_bound(got[:, cols], ref, bound, "host cols")
     assert np.isnan(got[:, N:]).all(), "C padding written"
     assert binding.device_status() == binding.SGEMM_OK
+
+
+@pytest.mark.parametrize("tensor_cores", [False, True])
+def test_host_entry_point_first_block_in_k_chunks(tensor_cores):
+    """K >= 4096: block 0 is multiplied in four k-chunks of B (1088, 1088,
+    1088 and 836 rows here, none a multiple of the tile depth at the end) as
+    they arrive, accumulating into its rows of C; block 1 takes the whole of
+    K.  beta != 0 and padded leading dimensions; oracle on rows of both
+    blocks and on columns."""
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    M, N, K = 2100, 300, 4100
+    A, B, C = make_inputs(M, N, K, "upm1", "upm1", "normal", seed=37, lda=K + 1, ldb=N + 3,
+                          ldc=N + 2)
+    tA = torch.from_numpy(A.base.copy()).pin_memory()[:, :K]
+    tB = torch.from_numpy(B.base.copy()).pin_memory()[:, :N]
+    cbuf = torch.from_numpy(C.base.copy()).pin_memory()
+    binding.sgemm_host(tA, tB, cbuf[:, :N], 0.75, 1.5, tensor_cores=tensor_cores)
+    rows = np.array([0, 1, 777, 1049, 1050, 1051, 2099], np.int64)
+    cols = np.array([0, 150, 299], np.int64)
+    got = cbuf.numpy()
+    ref, bound = oracle.sgemm_rows(A, B, C, 0.75, 1.5, rows)
+    assert_within_bound(got[rows, :N], ref, bound, "chunked host rows")
+    ref, bound = oracle.sgemm_cols(A, B, C, 0.75, 1.5, cols)
+    assert_within_bound(got[:, cols], ref, bound, "chunked host cols")
+    assert np.isnan(got[:, N:]).all(), "C padding written"
+    assert binding.device_status() == binding.SGEMM_OK
