@@ -1025,6 +1025,86 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// ------------------------------------------------------------------ small problems
+// C = alpha*A*B + beta*C for problems too small to fill the GPU with the
+// persistent kernel's 256x128 tiles: one CTA per TS x TS output tile (TS 64,
+// or 32 when 64x64 tiles would leave most SMs idle), reading A and B directly
+// (any leading dimension or alignment), no pre-pass, no workspace, one launch.
+// 256 threads in a 16x16 grid, (TS/16) x (TS/16) outputs each; k in steps of
+// 32 through shared memory (A stored transposed, as in the pages' tiled
+// kernel), the next step's operands loaded into registers meanwhile.  Every output sums its k terms in ascending order with fused
+// multiply-adds, so the result is deterministic.
+constexpr int SMALL_BK = 32;
+template <int TS>
+__global__ void __launch_bounds__(256)
+    sgemm_small_kernel(int M, int N, int K, float alpha, const float *__restrict__ A,
+                       long long lda, const float *__restrict__ B, long long ldb, float beta,
+                       float *__restrict__ C, long long ldc) {
+    constexpr int T = TS / 16;                       // outputs per thread along each side
+    constexpr int LOADS = TS * SMALL_BK / 256;       // elements of A (and of B) per thread
+    __shared__ float As[SMALL_BK][TS + 4];           // As[k][m]
+    __shared__ float Bs[SMALL_BK][TS + 4];           // Bs[k][n]
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const long long row0 = (long long)blockIdx.y * TS, col0 = (long long)blockIdx.x * TS;
+    float acc[T][T];
+#pragma unroll
+    for (int i = 0; i < T; ++i)
+#pragma unroll
+        for (int j = 0; j < T; ++j) acc[i][j] = 0.0f;
+    // TS x BK of A and BK x TS of B per step: consecutive threads along k for A
+    // and along n for B (coalesced); the next step's values are loaded into
+    // registers while the current step's FMAs run
+    float ra[LOADS], rb[LOADS];
+    auto fetch = [&](int k0) {
+#pragma unroll
+        for (int q = 0; q < LOADS; ++q) {
+            const int e = threadIdx.x + q * 256;
+            const long long gr = row0 + e / SMALL_BK;
+            const int gk = k0 + e % SMALL_BK;
+            ra[q] = (gr < M && gk < K) ? A[gr * lda + gk] : 0.0f;
+            const long long gc = col0 + e % TS;
+            const int gkb = k0 + e / TS;
+            rb[q] = (gkb < K && gc < N) ? B[(long long)gkb * ldb + gc] : 0.0f;
+        }
+    };
+    fetch(0);
+    for (int k0 = 0; k0 < K; k0 += SMALL_BK) {
+#pragma unroll
+        for (int q = 0; q < LOADS; ++q) {
+            const int e = threadIdx.x + q * 256;
+            As[e % SMALL_BK][e / SMALL_BK] = ra[q];
+            Bs[e / TS][e % TS] = rb[q];
+        }
+        __syncthreads();
+        if (k0 + SMALL_BK < K) fetch(k0 + SMALL_BK);
+#pragma unroll
+        for (int kk = 0; kk < SMALL_BK; ++kk) {
+            float a[T], b[T];
+#pragma unroll
+            for (int i = 0; i < T; ++i) a[i] = As[kk][ty * T + i];
+#pragma unroll
+            for (int j = 0; j < T; ++j) b[j] = Bs[kk][tx * T + j];
+#pragma unroll
+            for (int i = 0; i < T; ++i)
+#pragma unroll
+                for (int j = 0; j < T; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < T; ++i) {
+        const long long r = row0 + ty * T + i;
+        if (r >= M) continue;
+#pragma unroll
+        for (int j = 0; j < T; ++j) {
+            const long long c = col0 + tx * T + j;
+            if (c >= N) continue;
+            float *out = C + r * ldc + c;
+            *out = (beta != 0.0f) ? fmaf(alpha, acc[i][j], beta * *out) : alpha * acc[i][j];
+        }
+    }
+}
+
 // One thread waits on a barrier that nothing completes; the bounded wait must
 // expire, record ERR_SELFTEST and return.
 __global__ void wait_timeout_selftest_kernel(unsigned long long timeout_ns) {

@@ -362,6 +362,32 @@ sg::ExParams ex_params(const GemmCall &g, int a_planes, int b_planes) {
     return x;
 }
 
+// True when the default 256x128x64 tiling offers fewer slabs of work than
+// there are SMs: the persistent kernel would run a handful of CTAs, each
+// through a pre-pass, a slab and a stream-K fix-up.  Such GEMMs take the
+// direct small-problem kernel.
+bool small_problem(int M, int N, int K, int sms) {
+    const long long tiles = ((M + 255LL) / 256) * ((N + 127LL) / 128);
+    return tiles * ((K + 63LL) / 64) < sms;
+}
+
+int launch_small(const GemmCall &g, cudaStream_t stream, int sms) {
+    const long long t64 = ((g.M + 63LL) / 64) * ((g.N + 63LL) / 64);
+    ProfScope prof(stream, true);
+    if (t64 < sms) {
+        dim3 grid(unsigned((g.N + 31) / 32), unsigned((g.M + 31) / 32));
+        sg::sgemm_small_kernel<32><<<grid, 256, 0, stream>>>(g.M, g.N, g.K, g.alpha, g.A, g.lda, g.B,
+                                                            g.ldb, g.beta, g.C, g.ldc);
+    } else {
+        dim3 grid(unsigned((g.N + 63) / 64), unsigned((g.M + 63) / 64));
+        sg::sgemm_small_kernel<64><<<grid, 256, 0, stream>>>(g.M, g.N, g.K, g.alpha, g.A, g.lda, g.B,
+                                                            g.ldb, g.beta, g.C, g.ldc);
+    }
+    g_launches.fetch_add(1);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SGEMM_OK : cuda_fail(e);
+}
+
 int gemm_device(const GemmCall &g, cudaStream_t stream) {
     int st = checked_call(g);
     if (st != SGEMM_OK || g.M == 0 || g.N == 0 || g.batch == 0) return st;
@@ -372,6 +398,8 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
 
     const int M = g.M, N = g.N, K = g.K;
     const bool extended = g.batch > 1 || g.bias != nullptr || g.act != sg::ACT_NONE;
+    if (!extended && g_forced_variant.load() < 0 && small_problem(M, N, K, dev->sm_count))
+        return launch_small(g, stream, dev->sm_count);
     const Variant &var = extended ? kExVariant : kVariants[pick_variant(M, N, K)];
     // A and B enter as one plane per batch, or one plane for all batches when
     // their stride is 0

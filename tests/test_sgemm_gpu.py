@@ -16,12 +16,24 @@ def _gpu(cuda_device):
     yield
 
 
+@pytest.fixture(params=["auto", "tma"])
+def kernel(request):
+    """Run a test twice: with the library's own choice (problems too small for
+    the persistent kernel take the direct small-problem kernel) and with the
+    persistent TMA kernel forced (variant 0), so both stay covered at small
+    and ragged shapes."""
+    from dense_fp32_gemm_02_gb300 import binding
+    binding.set_variant(0 if request.param == "tma" else -1)
+    yield request.param
+    binding.set_variant(-1)
+
+
 SIZES_MN = [1, 7, 33, 64, 127, 128, 129, 255, 257]
 SIZES_K = [1, 5, 16, 17, 33, 100]
 
 
 @pytest.mark.parametrize("K", SIZES_K)
-def test_integer_inputs_bit_exact_over_shape_grid(K):
+def test_integer_inputs_bit_exact_over_shape_grid(K, kernel):
     """Integer inputs in [-4, 4]: every partial sum is an exact integer, so any
     summation order gives the oracle's bits.  alpha=1.5, beta=0.5 with integer
     C keeps the epilogue exact too."""
@@ -36,7 +48,7 @@ def test_integer_inputs_bit_exact_over_shape_grid(K):
 @pytest.mark.parametrize("M,N,K", [(300, 200, 100), (129, 257, 513), (1000, 33, 77),
                                    (5, 1100, 260), (640, 640, 640)])
 @pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (1.5, 0.5), (-0.75, 1.0), (2.0, -3.0)])
-def test_random_parity_within_bound(M, N, K, alpha, beta):
+def test_random_parity_within_bound(M, N, K, alpha, beta, kernel):
     A, B, C = make_inputs(M, N, K, "upm1", "normal", "normal", seed=M + N + K)
     ref, bound = oracle.sgemm(A, B, C if beta != 0 else None, alpha, beta)
     got = run_gpu(A, B, C if beta != 0 else None, alpha, beta).cpu().numpy()
@@ -45,7 +57,7 @@ def test_random_parity_within_bound(M, N, K, alpha, beta):
 
 @pytest.mark.parametrize("pads,offsets", [((3, 5, 2), (0, 0, 0)), ((0, 0, 0), (1, 1, 1)),
                                           ((4, 4, 4), (0, 2, 3)), ((1, 0, 7), (3, 0, 0))])
-def test_leading_dimensions_and_alignment(pads, offsets):
+def test_leading_dimensions_and_alignment(pads, offsets, kernel):
     """Row pitches above the minimum with NaN padding, and base addresses that
     are 4-byte but not 16-byte aligned: the TMA rule is met by the packing
     pass; NaN padding must never reach the result; C padding stays untouched."""
@@ -62,7 +74,7 @@ def test_leading_dimensions_and_alignment(pads, offsets):
         assert np.isnan(full[:, N:]).all(), "C padding columns were written"
 
 
-def test_edge_rows_and_columns_not_written_outside_block():
+def test_edge_rows_and_columns_not_written_outside_block(kernel):
     """Guard band: C is a window inside a NaN-filled buffer; nothing outside the
     M x N window may change."""
     import torch
@@ -81,7 +93,7 @@ def test_edge_rows_and_columns_not_written_outside_block():
     assert np.isnan(h[mask]).all()
 
 
-def test_beta_zero_does_not_read_c():
+def test_beta_zero_does_not_read_c(kernel):
     M, N, K = 150, 140, 130
     A, B, _ = make_inputs(M, N, K, "upm1", "upm1", None, seed=5)
     C = np.full((M, N), np.nan, np.float32)
@@ -205,11 +217,17 @@ def test_binding_rejects_bad_tensors():
 
 
 def test_kernel_launches_are_counted():
+    """A problem too small for the persistent kernel is one launch of the
+    direct kernel; a larger one is the A transpose plus the main kernel."""
     from dense_fp32_gemm_02_gb300 import binding
     before = binding.kernel_launch_count()
     A, B, _ = make_inputs(64, 64, 64, seed=23)
     run_gpu(A, B, None, 1.0, 0.0)
-    assert binding.kernel_launch_count() - before >= 2     # pack + main
+    assert binding.kernel_launch_count() - before == 1     # small-problem kernel
+    before = binding.kernel_launch_count()
+    A, B, _ = make_inputs(1024, 1024, 1024, seed=24)
+    run_gpu(A, B, None, 1.0, 0.0)
+    assert binding.kernel_launch_count() - before == 2     # A transpose + main kernel
 
 
 @pytest.mark.parametrize("M,N,K", [(600, 520, 300), (257, 1031, 95), (1, 300, 17)])
@@ -238,7 +256,7 @@ def test_every_kernel_variant_matches_oracle(M, N, K):
     (300, 4000, 16),      # one slab per tile: stream-K pieces are whole tiles, some CTAs idle
     (2048, 2048, 1056),   # 128 tiles, 33 slabs: the whole problem is stream-K
 ])
-def test_stream_k_split_matches_oracle(M, N, K):
+def test_stream_k_split_matches_oracle(M, N, K, kernel):
     """Shapes whose leftover tiles are split along k between CTAs: integer
     inputs must stay bit-exact (any order of exact partial sums), random inputs
     within the bound, and two runs must agree bitwise (the partial sums are
