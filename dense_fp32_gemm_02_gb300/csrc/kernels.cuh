@@ -123,7 +123,7 @@ struct MainParams {
     int M, N, K;
     float alpha, beta;
     int tiles_m, tiles_n, group_m;
-    int c_vec4;              // C base 16-byte aligned and ldc % 4 == 0 (and stride_c % 4 == 0)
+    int c_vec4;              // C base 16-byte aligned (rows then checked one by one)
     unsigned long long timeout_ns;
     // Work split.  Tiles [0, dp_tiles) are whole-tile work, CTA b taking tiles
     // b, b + gridDim.x, ...  The k-slabs of the remaining tiles, in tile-major
@@ -362,11 +362,14 @@ __device__ __forceinline__ void store_tile(const float (&acc)[Cfg::TM][Cfg::TN],
             const int row = row0 + s4 * 16 + r;
             if (row >= p.M) continue;
             float *crow = p.C + (long long)row * p.ldc;
+            // 128-bit accesses where this row starts 16-byte aligned (every row
+            // when ldc % 4 == 0; one row in four for an odd ldc)
+            const bool c_row_vec = p.c_vec4 && (reinterpret_cast<uintptr_t>(crow) & 15u) == 0;
 #pragma unroll
             for (int t = 0; t < Cfg::TN / 4; ++t) {
                 const int col = col0 + t * 32;
                 const float *v = &acc[4 * s4 + r][4 * t];
-                if (p.c_vec4 && col + 3 < p.N) {
+                if (c_row_vec && col + 3 < p.N) {
                     float4 o;
                     if (beta != 0.0f) {
                         const float4 c = __ldcs(reinterpret_cast<const float4 *>(crow + col));
@@ -428,11 +431,12 @@ __device__ __forceinline__ void store_tile_ex(const float (&acc)[Cfg::TM][Cfg::T
             const int row = row0 + s4 * 16 + r;
             if (row >= p.M) continue;
             float *crow = Cb + (long long)row * p.ldc;
+            const bool c_row_vec = p.c_vec4 && (reinterpret_cast<uintptr_t>(crow) & 15u) == 0;
 #pragma unroll
             for (int t = 0; t < Cfg::TN / 4; ++t) {
                 const int col = col0 + t * 32;
                 const float *v = &acc[4 * s4 + r][4 * t];
-                if (p.c_vec4 && col + 3 < p.N) {
+                if (c_row_vec && col + 3 < p.N) {
                     float4 o;
                     if (beta != 0.0f) {
                         const float4 c = __ldcs(reinterpret_cast<const float4 *>(crow + col));

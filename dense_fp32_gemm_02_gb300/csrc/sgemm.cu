@@ -503,7 +503,7 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
     p.tiles_m = int(tiles_m);
     p.tiles_n = int(tiles_n);
     p.group_m = var.group_m;
-    p.c_vec4 = (aligned16(g.C) && g.ldc % 4 == 0 && (g.batch == 1 || g.stride_c % 4 == 0)) ? 1 : 0;
+    p.c_vec4 = aligned16(g.C) ? 1 : 0;
     p.timeout_ns = g_timeout_ns.load();
     p.dp_tiles = int(dp_tiles);
     p.sk_slabs = sk_slabs;
@@ -921,7 +921,7 @@ int sgemm_device_noalloc(int M, int N, int K, float alpha, const float *A, int l
     p.tiles_m = int((M + var.bm - 1) / var.bm);
     p.tiles_n = int((N + var.bn - 1) / var.bn);
     p.group_m = 8;
-    p.c_vec4 = (aligned16(C) && ldc % 4 == 0) ? 1 : 0;
+    p.c_vec4 = aligned16(C) ? 1 : 0;
     p.timeout_ns = g_timeout_ns.load();
     const long long tiles = (long long)p.tiles_m * p.tiles_n;
     const int grid_main = int(std::min<long long>(tiles, dev->sm_count));
