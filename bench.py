@@ -375,7 +375,7 @@ def measure_tf32x3(args, w, binding, dA, dB, dC, C, stream, world, device):
     if binding.device_status(stream=stream) != 0:
         raise RuntimeError("device error word set during the 3xTF32 timed region")
     ms = max_over_ranks(world, start.elapsed_time(stop), device) / args.steps
-    main_ms = prof["main_ms"] / max(1, prof["main_launches"])
+    main_ms = prof["main_ms"] / args.steps   # every compute launch of a step
     # all pre-pass launches of a step (split of A and split+transpose of B)
     split_ms = prof["pack_ms"] / args.steps
     peak, src = tensor_peak_tf32()
@@ -521,7 +521,7 @@ def run_ours(args):
                             "power_w_median": tclk.get("power_w_median")}
 
     # ---- roofline of the main kernel
-    main_ms = prof["main_ms"] / max(1, prof["main_launches"])
+    main_ms = prof["main_ms"] / args.steps   # every compute launch of a step
     # all pre-pass launches of a step (transposes, re-pitching copies, splits)
     pack_ms = prof["pack_ms"] / args.steps
     peak_tflops = sms * FFMA_PER_SM_PER_CLK * 2 * SM_MAX_MHZ_FALLBACK * 1e6 / 1e12
