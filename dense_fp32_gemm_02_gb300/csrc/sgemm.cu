@@ -576,7 +576,10 @@ int t3_run(int M, int N, int K, float alpha, const float *A, int lda, const floa
     p.beta = beta;
     p.tiles_m = int((M + t3::BM - 1) / t3::BM);
     p.tiles_n = int((N + t3::BN - 1) / t3::BN);
-    p.group_m = 8;
+    // 16 tile rows per raster group: a wave of 152 tiles then covers 16 rows
+    // x 9.5 columns of tiles, the fewest distinct A and B panels; measured at
+    // 8192^3: group 4 3.28 ms, 8 3.18, 12 3.11, 16 3.07, 20 3.10, 32 3.18
+    p.group_m = 16;
     p.timeout_ns = g_timeout_ns.load();
     const long long tiles = (long long)p.tiles_m * p.tiles_n;
     if (tiles > 0x7fffffffLL) return SGEMM_ERR_INVALID_ARG;
