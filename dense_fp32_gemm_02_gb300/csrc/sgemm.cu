@@ -330,7 +330,7 @@ int checked_call(const GemmCall &g) {
     // an empty batch, like an empty matrix, reads and writes nothing
     const bool empty = g.batch == 0;
     int st = checked_args(g.M, empty ? 0 : g.N, g.K, g.A, g.lda, g.B, g.ldb, g.C,
-                          std::max(g.ldc, empty ? 1 : g.ldc), g.alpha, g.beta);
+                          empty ? std::max(g.ldc, 1) : g.ldc, g.alpha, g.beta);
     if (st != SGEMM_OK) return st;
     if (g.M == 0 || g.N == 0 || empty) return SGEMM_OK;
     if (g.bias && !aligned4(g.bias)) return SGEMM_ERR_INVALID_ARG;
