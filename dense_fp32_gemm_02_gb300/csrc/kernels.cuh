@@ -355,6 +355,23 @@ __device__ __forceinline__ void store_tile(const float (&acc)[Cfg::TM][Cfg::TN],
     const int row0 = tm * Cfg::BM + a_off;
     const int col0 = tn * Cfg::BN + b_off;
     const float alpha = p.alpha, beta = p.beta;
+    // The rows of C are read one after another below (a store to one row may
+    // alias the next row's load, so the loads cannot be hoisted); start all
+    // their lines towards L2 first, so only the first row waits for DRAM.
+    // Measured: ragged 4097x3001x1023 (beta 1) 2.5 % faster, 8192^3 (beta 0.5)
+    // 0.14 % faster.
+    if (beta != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < Cfg::TM; ++i) {
+            const int row = row0 + (i >> 2) * 16 + (i & 3);
+            if (row < p.M) {
+                const float *crow = p.C + (long long)row * p.ldc + col0;
+#pragma unroll
+                for (int t = 0; t < Cfg::TN / 4; ++t)
+                    if (col0 + t * 32 < p.N) prefetch_l2(crow + t * 32);
+            }
+        }
+    }
 #pragma unroll
     for (int s4 = 0; s4 < Cfg::TM / 4; ++s4) {
 #pragma unroll
@@ -412,6 +429,19 @@ __device__ __forceinline__ void store_tile_ex(const float (&acc)[Cfg::TM][Cfg::T
     float *const Cb = p.C + (long long)tb * x.stride_c;
     const float *const bias = x.bias ? x.bias + (long long)tb * x.stride_bias : nullptr;
     const bool fused = bias != nullptr || x.act != ACT_NONE;
+    // C's lines towards L2 before the row-by-row reads (as in store_tile)
+    if (beta != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < Cfg::TM; ++i) {
+            const int row = row0 + (i >> 2) * 16 + (i & 3);
+            if (row < p.M) {
+                const float *crow = Cb + (long long)row * p.ldc + col0;
+#pragma unroll
+                for (int t = 0; t < Cfg::TN / 4; ++t)
+                    if (col0 + t * 32 < p.N) prefetch_l2(crow + t * 32);
+            }
+        }
+    }
     // the bias of four columns (read where it is used: an L1 hit after the
     // first row, and four live registers instead of TN)
     auto bias4 = [&](int col) {

@@ -89,6 +89,11 @@ __device__ __forceinline__ void st_shared_flag(uint32_t addr, int v) {
 }
 
 // ---------------------------------------------------------------- TMA
+// Bring the 128-byte line that holds `ptr` into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void *ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
