@@ -59,6 +59,11 @@ def parse_args():
                          "tensor-core entry point, same tolerance, its own roofline")
     ap.add_argument("--variant", type=int, default=-1,
                     help="force a kernel variant (tile-configuration sweeps); -1 = automatic")
+    ap.add_argument("--oracle-table", action="store_true",
+                    help="time the CPU oracle on every workload with all host cores and with "
+                         "one, print one JSON line and exit (no GPU work)")
+    ap.add_argument("--oracle-budget", type=float, default=2.0,
+                    help="seconds of oracle work per --oracle-table measurement")
     return ap.parse_args()
 
 
@@ -212,9 +217,10 @@ def time_e2e(step, w, steps, world, device, entry_point, h2d_bytes, d2h_bytes):
             "statistic": "median of the timed calls"}
 
 
-def oracle_rows_fn(w, A, B, C):
+def oracle_rows_fn(w, A, B, C, threads=None):
     """f(idx): the oracle as it stands on full rows idx of the workload (batch 0
-    of a batched one, with its bias and activation)."""
+    of a batched one, with its bias and activation); `threads` host threads
+    (default: all)."""
     import oracle
     from dense_fp32_gemm_02_gb300.workloads import workload_bias
     if w.extended:
@@ -223,16 +229,17 @@ def oracle_rows_fn(w, A, B, C):
         C0 = None if (C is None or w.beta == 0) else (C[0] if w.batch > 1 else C)
         b0 = None if bias is None else bias[0]
         return lambda idx: oracle.sgemm_ex_rows(A0, B0, C0, w.alpha, w.beta, b0, w.act, idx,
-                                                with_bound=False)
+                                                threads=threads, with_bound=False)
     c_in = C if w.beta != 0 else None
-    return lambda idx: oracle.sgemm_rows(A, B, c_in, w.alpha, w.beta, idx, with_bound=False)
+    return lambda idx: oracle.sgemm_rows(A, B, c_in, w.alpha, w.beta, idx, threads=threads,
+                                         with_bound=False)
 
 
-def time_oracle_rows(w, A, B, C, row_budget_s=12.0, first=16, max_rows=None):
+def time_oracle_rows(w, A, B, C, row_budget_s=12.0, first=16, max_rows=None, threads=None):
     """The oracle as it stands on full rows of the workload; grows the sample
     until about `row_budget_s` seconds of CPU work.  Returns (gflops, rows, secs)."""
     import numpy as np
-    rows_fn = oracle_rows_fn(w, A, B, C)
+    rows_fn = oracle_rows_fn(w, A, B, C, threads)
     rows_done, secs, r0 = 0, 0.0, 0
     n = first
     max_rows = max_rows or w.M
@@ -298,6 +305,47 @@ def run_reference(args):
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------- oracle table
+def cpu_model():
+    """The host CPU's model line from /proc/cpuinfo, or the platform's name."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def run_oracle_table(args):
+    """The oracle as it stands, on every workload, once with all host cores and
+    once with one: GFLOP/s on a bounded sample of full output rows, and the time
+    the whole oracle of that workload would take at that rate."""
+    import platform
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    from dense_fp32_gemm_02_gb300.workloads import WORKLOADS, workload_inputs
+    cores = host_cores()
+    table = []
+    for name, w in WORKLOADS.items():
+        A, B, C = workload_inputs(w)
+        for threads in (cores, 1):
+            g, rows, secs = time_oracle_rows(w, A, B, C, row_budget_s=args.oracle_budget,
+                                             first=max(1, min(16, threads)), threads=threads)
+            table.append({"workload": name, "threads": threads, "gflops": round(g, 3),
+                          "rows": rows, "secs": round(secs, 3),
+                          "full_oracle_s": round(w.flops / (g * 1e9), 1)})
+        del A, B, C
+    print(json.dumps({"oracle_table": table, "unit": "GFLOP/s", "kind": "oracle",
+                      "host": {"machine": platform.machine(), "cpu": cpu_model(),
+                               "cores": cores}}), flush=True)
     return 0
 
 
@@ -606,6 +654,8 @@ def run_ours(args):
 
 def main():
     args = parse_args()
+    if args.oracle_table:
+        return run_oracle_table(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
