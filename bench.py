@@ -41,6 +41,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 # nominal dense TF32 / BF16 tensor throughput of GB300 (1.1 / 2.25 PFLOP/s)
 TF32_PER_BF16 = 1.1 / 2.25
 BF16_FALLBACK_TFLOPS = 1900.0
+HBM_FALLBACK_GBS = 6800.0
 
 
 def parse_args():
@@ -388,6 +389,21 @@ def tensor_peak_tf32():
     return bf16 * TF32_PER_BF16, src
 
 
+def dram_use(traffic, ms):
+    """{dram_gbs, dram_frac}: one launch's DRAM bytes (the ncu figure) over its
+    CUDA-event duration, and that rate against the measured copy bandwidth;
+    both None without a traffic figure for the current kernel."""
+    if not traffic or not ms or ms <= 0:
+        return {"dram_gbs": None, "dram_frac": None}
+    gbs = traffic / (ms * 1e-3) / 1e9
+    try:
+        with open(PEAKS_FILE) as f:
+            peak = float(json.load(f)["hbm_gbs"])
+    except (OSError, ValueError, KeyError):
+        peak = HBM_FALLBACK_GBS
+    return {"dram_gbs": round(gbs, 1), "dram_frac": round(gbs / peak, 4)}
+
+
 def measure_tf32x3(args, w, binding, dA, dB, dC, C, stream, world, device):
     """The 3xTF32 tensor-core entry point on the same workload: device-time
     rate, the main kernel against the TF32 tensor roofline, and end to end
@@ -434,6 +450,7 @@ def measure_tf32x3(args, w, binding, dA, dB, dC, C, stream, world, device):
         "roofline": {"bound": "tensor", "kernel": "sgemm_3xtf32_kernel",
                      "achieved": round(mma_tflops, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
                      "frac": round(mma_tflops / peak, 4), "traffic": load_traffic(w.name + ":tf32x3"),
+                     **dram_use(load_traffic(w.name + ":tf32x3"), main_ms),
                      "peak_source": src,
                      "algorithmic_flops_per_launch": 3.0 * w.flops,
                      "note": "three TF32 MMAs per fp32 product: achieved counts MMA FLOPs",
@@ -586,6 +603,7 @@ def run_ours(args):
             "peak": round(peak_tflops, 3), "unit": "TFLOP/s",
             "frac": round(achieved_tflops / peak_tflops, 4) if achieved_tflops else None,
             "traffic": load_traffic(w.name),
+            **dram_use(load_traffic(w.name), main_ms),
             "peak_source": f"derived: {sms} SMs x 128 FFMA/clk x 2 FLOP x 2070 MHz max SM clock",
             "frac_at_measured_clock": (round(achieved_tflops / peak_meas, 4)
                                        if (achieved_tflops and peak_meas) else None),
@@ -601,7 +619,8 @@ def run_ours(args):
             "achieved": round(mma_tflops, 3) if mma_tflops else None,
             "peak": round(tpeak, 3), "unit": "TFLOP/s",
             "frac": round(mma_tflops / tpeak, 4) if mma_tflops else None,
-            "traffic": load_traffic(w.name + ":tf32x3"), "peak_source": tsrc,
+            "traffic": load_traffic(w.name + ":tf32x3"),
+            **dram_use(load_traffic(w.name + ":tf32x3"), main_ms), "peak_source": tsrc,
             "main_kernel_ms": round(main_ms, 4), "split_kernels_ms": round(pack_ms, 4),
             "algorithmic_flops_per_launch": 3.0 * w.flops,
         }

@@ -25,3 +25,14 @@ def test_oracle_table_times_every_workload_with_all_cores_and_one(monkeypatch, c
         # the rate is 2 N K per row over the measured seconds (printed to the ms)
         assert r["gflops"] == pytest.approx(2.0 * r["rows"] * 256 * 256 / r["secs"] / 1e9,
                                             rel=0.05)
+
+
+def test_dram_use_is_traffic_over_time_against_the_measured_copy_bandwidth():
+    import bench
+    with open(bench.PEAKS_FILE) as f:
+        peak = json.load(f)["hbm_gbs"]
+    d = bench.dram_use(3.0e9, 15.0)              # 3 GB in 15 ms = 200 GB/s
+    assert d["dram_gbs"] == pytest.approx(200.0)
+    assert d["dram_frac"] == pytest.approx(200.0 / peak, abs=1e-4)
+    assert bench.dram_use(None, 15.0) == {"dram_gbs": None, "dram_frac": None}
+    assert bench.dram_use(3.0e9, 0.0) == {"dram_gbs": None, "dram_frac": None}
