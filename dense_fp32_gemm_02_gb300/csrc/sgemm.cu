@@ -71,15 +71,16 @@ using sg::MICRO_FFMA2;
 using sg::ISSUE_THREAD0;
 using sg::ISSUE_PRODUCER_WG;
 using sg::ISSUE_LAST_WARP;
-// Variant 0 is the default for every shape: it was the fastest or within 1%
-// of the fastest on every measured workload.  Its 16 consumer warps (four per
-// scheduler) hide the shared-memory latency of the fragment loads better than
-// 12 warps plus a producer warpgroup (16 consumer warps at 128 registers fill
-// the register file, so the two do not fit together), and the warp that
-// releases a stage last refills it, so no warp waits for the others.  The
-// others stay for sweeps and as evidence for the design choices (issuer,
-// tile shape, stream-K, warp specialisation, packed FP32x2 FMA, thread-tile
-// size, k depth of a stage).
+// Variant 0 is the default: it was the fastest or within 1% of the fastest on
+// every measured workload.  Its 16 consumer warps (four per scheduler) hide
+// the shared-memory latency of the fragment loads better than 12 warps plus a
+// producer warpgroup (16 consumer warps at 128 registers fill the register
+// file, so the two do not fit together), and the warp that releases a stage
+// last refills it, so no warp waits for the others.  Variant 1, the same tile
+// turned, takes the shapes that it pads less (pick_variant).  The others stay
+// for sweeps and as evidence for the design choices (issuer, tile shape,
+// stream-K, warp specialisation, packed FP32x2 FMA, thread-tile size, k depth
+// of a stage).
 const Variant kVariants[] = {
     make_variant<sg::TileConfig<256, 128, 64, 2, 8, 2, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>>(
         "ffma2 tile=256x128x64 stages=2 warps=16 issuer=last_warp thread=8x8 stream_k", true),
@@ -116,13 +117,20 @@ const Variant kExVariant =
         true);
 std::atomic<int> g_forced_variant{-1};
 
+// Shape heuristic between the two orientations of the default tile, 256x128
+// (variant 0) and 128x256 (variant 1): same kernel, same speed where both fit
+// the shape, so the one that pads C less wins; variant 0 on a tie.  Padding is
+// the FMA work spent on the rows and columns past M and N in edge tiles (M =
+// 4097: 17 tile rows of 256 or 33 of 128).
+long long padded_area(const Variant &v, int M, int N) {
+    return ((M + v.bm - 1LL) / v.bm) * v.bm * (((N + v.bn - 1LL) / v.bn) * v.bn);
+}
+
 int pick_variant(int M, int N, int K) {
     const int forced = g_forced_variant.load();
     if (forced >= 0 && forced < kNumVariants) return forced;
-    (void)M;
-    (void)N;
     (void)K;
-    return 0;
+    return padded_area(kVariants[1], M, N) < padded_area(kVariants[0], M, N) ? 1 : 0;
 }
 
 struct DeviceState {

@@ -176,3 +176,20 @@ def test_ex_single_batch_needs_no_c_stride(lib):
     # GPU the call gets as far as the device check
     st = _call_ex(lib, batch=1, stride_c=0, stride_a=0, stride_b=0)
     assert st != 1
+
+
+@pytest.mark.parametrize("M,N,K,tile", [
+    (8192, 8192, 8192, "256x128"),     # no padding either way: the default
+    (4096, 4096, 4096, "256x128"),
+    (16384, 16384, 512, "256x128"),
+    (4097, 3001, 1023, "128x256"),     # 17 x 256 rows pad more than 33 x 128
+    (300, 8192, 512, "128x256"),       # 512 rows against 384
+    (4096, 300, 64, "256x128"),        # 300 columns: 384 against 512
+])
+def test_shape_heuristic_takes_the_tile_orientation_that_pads_less(M, N, K, tile):
+    """Between the 256x128 tile and the same tile turned (128x256) the one that
+    pads C less is chosen, the 256x128 one on a tie."""
+    from dense_fp32_gemm_02_gb300 import binding
+    binding.set_variant(-1)
+    name = binding.config_string(M, N, K)
+    assert f"tile={tile}x64" in name and name in binding.variants()[:2]
