@@ -39,10 +39,10 @@ constexpr int BM = 128, BN = 256, BK = 16, STAGES = 4;
 constexpr int ROW_BYTES = BK * 4;
 static_assert(ROW_BYTES == 64 || ROW_BYTES == 128, "64- or 128-byte swizzle rows");
 constexpr uint32_t SWIZZLE_CODE = ROW_BYTES == 128 ? 2u : 4u;   // descriptor layout field
-constexpr int A_TILE = BM * BK;                       // floats, 16 KB
-constexpr int B_TILE = BN * BK;                       // floats, 32 KB
+constexpr int A_TILE = BM * BK;                       // floats, 8 KB
+constexpr int B_TILE = BN * BK;                       // floats, 16 KB
 constexpr int STAGE_FLOATS = 2 * A_TILE + 2 * B_TILE; // A_hi, A_lo, B_hi, B_lo
-constexpr uint32_t STAGE_BYTES = STAGE_FLOATS * 4u;   // 96 KB
+constexpr uint32_t STAGE_BYTES = STAGE_FLOATS * 4u;   // 48 KB
 constexpr uint32_t STAGE_BYTES_HALF = STAGE_BYTES - uint32_t(B_TILE) * 4u;   // B boxes of BN/2 rows
 constexpr int THREADS = 256;
 constexpr int EPI_WARPS = 4;                          // warps 4..7
