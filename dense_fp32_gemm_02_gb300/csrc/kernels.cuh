@@ -1059,6 +1059,20 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// C += beta * X over an M x N block (row pitches ldc and ldx): the deferred
+// beta * C_in term of the host-buffer pipeline's first row block.
+__global__ void __launch_bounds__(256)
+    add_scaled_kernel(float *C, long long ldc, const float *__restrict__ X, long long ldx, int M,
+                      int N, float beta) {
+    const long long total = (long long)M * N;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long i = idx / N, j = idx - i * N;
+        float *c = C + i * ldc + j;
+        *c = fmaf(beta, X[i * ldx + j], *c);
+    }
+}
+
 // ------------------------------------------------------------------ small problems
 // C = alpha*A*B + beta*C for problems too small to fill the GPU with the
 // persistent kernel's 256x128 tiles: one CTA per TS x TS output tile (TS 64,

@@ -19,6 +19,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "../../include/sgemm.h"
@@ -675,12 +676,52 @@ struct EventSet {
     }
 };
 
-// The host-buffer GEMM, pipelined over row blocks of A and C: block i of A
-// (and of C when beta != 0) is copied in on the h2d stream, multiplied on the
-// caller's stream while block i+1 is copied in, and copied back on the d2h
-// stream while block i+1 is multiplied.  B follows block 0 in k-chunks, and
-// block 0 is multiplied chunk by chunk as they land.  `tensor` selects the
-// 3xTF32 path (B is split chunk by chunk, each block of A with its GEMM).
+// Row blocks of the host-buffer pipeline: a first block of kEdgeRows rows (the
+// first multiply waits only for its own operands), a last one of kEdgeRows (the
+// copy back after the last multiply is short) and blocks of about kMidRows rows
+// between them (fewer launches); `uniform`: equal blocks of at least kEdgeRows
+// rows, at most 8.  One block when M < 2 * kEdgeRows or when nothing is
+// multiplied.  Returns (first row, rows) per block.
+constexpr int kEdgeRows = 1024, kMidRows = 2048;
+std::vector<std::pair<int, int>> host_row_blocks(int M, bool multiply, bool uniform) {
+    std::vector<std::pair<int, int>> b;
+    if (!multiply || M < 2 * kEdgeRows) {
+        b.emplace_back(0, M);
+        return b;
+    }
+    if (uniform) {
+        // equal blocks of at least kEdgeRows rows, at most 8
+        const int n = std::min(8, M / kEdgeRows), per = (M + n - 1) / n;
+        for (int r0 = 0; r0 < M; r0 += per) b.emplace_back(r0, std::min(per, M - r0));
+        return b;
+    }
+    b.emplace_back(0, kEdgeRows);
+    const int rest = M - kEdgeRows;
+    if (rest <= kMidRows) {
+        b.emplace_back(kEdgeRows, rest);
+        return b;
+    }
+    const int mid = rest - kEdgeRows;
+    const int nmid = (mid + kMidRows - 1) / kMidRows;
+    for (int i = 0; i < nmid; ++i) {
+        const int r0 = kEdgeRows + int((long long)mid * i / nmid);
+        const int r1 = kEdgeRows + int((long long)mid * (i + 1) / nmid);
+        b.emplace_back(r0, r1 - r0);
+    }
+    b.emplace_back(M - kEdgeRows, kEdgeRows);
+    return b;
+}
+
+// The host-buffer GEMM, pipelined over row blocks of A and C (host_row_blocks):
+// block i of A (and of C when beta != 0) is copied in on the h2d stream,
+// multiplied on the caller's stream while block i+1 is copied in, and copied
+// back on the d2h stream while block i+1 is multiplied.  Block 0 is multiplied
+// in k-chunks as the matching columns of A and rows of B arrive (B follows
+// block 0 chunk by chunk), so the first multiply waits for a quarter of B
+// rather than for all of it and for none of C: the first chunk runs with
+// beta = 0, later ones accumulate (beta = 1), and beta * C_in is added once
+// block 0's C_in has arrived.  `tensor` selects the 3xTF32 path (B is split
+// chunk by chunk, each block of A with its GEMM).
 int host_gemm(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
               float beta, float *C, int ldc, cudaStream_t stream, bool tensor) {
     int st = checked_args(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta);
@@ -693,17 +734,27 @@ int host_gemm(int M, int N, int K, float alpha, const float *A, int lda, const f
     const bool need_ab = (K > 0 && alpha != 0.0f);
     const bool need_c_in = (beta != 0.0f);
     const long long ldk = round_up(std::max(K, 1), 4);
-    // row blocks: about 1024 rows or more, at most 8 blocks
-    const int nblk = need_ab ? std::max(1, std::min(8, M / 1024)) : 1;
-    const int rows_per_blk = (M + nblk - 1) / nblk;
+    const std::vector<std::pair<int, int>> blocks = host_row_blocks(M, need_ab, tensor);
+    int max_rows = 0;
+    for (const auto &b : blocks) max_rows = std::max(max_rows, b.second);
+    // block 0 in k-chunks when K is long enough for the copies of B to matter
+    const int kchunks = (need_ab && K >= 4096) ? 4 : 1;
+    const int kc = need_ab ? int(round_up((K + kchunks - 1) / kchunks, 64)) : 0;
+    // The 3xTF32 path is bound by the host link, not by its first multiply:
+    // it keeps equal row blocks and C_in in front of B (the deferred add and
+    // the unequal blocks measured 0.4-1.3 % slower there, 2.2 % faster on the
+    // FFMA path at 8192^3).
+    const bool defer_c_in = kchunks > 1 && need_c_in && !tensor;
 
     const size_t a_bytes = need_ab ? round_up((long long)M * K * 4, 256) : 0;
     const size_t b_bytes = need_ab ? round_up((long long)K * N * 4, 256) : 0;
     const size_t c_bytes = round_up((long long)M * N * 4, 256);
+    // block 0's C_in while its chunks accumulate
+    const size_t cin_bytes = defer_c_in ? round_up((long long)blocks[0].second * N * 4, 256) : 0;
     // 3xTF32: split parts of B (2 x N x ldk) and of the largest block of A
     const size_t bs_bytes = (need_ab && tensor) ? round_up((long long)N * ldk * 4, 256) : 0;
-    const size_t as_bytes = (need_ab && tensor) ? round_up((long long)rows_per_blk * ldk * 4, 256) : 0;
-    const size_t total = a_bytes + b_bytes + c_bytes + 2 * bs_bytes + 2 * as_bytes;
+    const size_t as_bytes = (need_ab && tensor) ? round_up((long long)max_rows * ldk * 4, 256) : 0;
+    const size_t total = a_bytes + b_bytes + c_bytes + cin_bytes + 2 * bs_bytes + 2 * as_bytes;
     void *buf = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&buf, total, dev->pool, stream);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -711,9 +762,10 @@ int host_gemm(int M, int N, int K, float alpha, const float *A, int lda, const f
     float *dA = reinterpret_cast<float *>(base);
     float *dB = reinterpret_cast<float *>(base + a_bytes);
     float *dC = reinterpret_cast<float *>(base + a_bytes + b_bytes);
-    float *Bh = reinterpret_cast<float *>(base + a_bytes + b_bytes + c_bytes);
+    float *dCin = reinterpret_cast<float *>(base + a_bytes + b_bytes + c_bytes);
+    float *Bh = reinterpret_cast<float *>(base + a_bytes + b_bytes + c_bytes + cin_bytes);
     float *Bl = Bh + bs_bytes / 4;
-    float *Ah = reinterpret_cast<float *>(base + a_bytes + b_bytes + c_bytes + 2 * bs_bytes);
+    float *Ah = reinterpret_cast<float *>(base + a_bytes + b_bytes + c_bytes + cin_bytes + 2 * bs_bytes);
     float *Al = Ah + as_bytes / 4;
 
     EventSet evs;
@@ -731,69 +783,77 @@ int host_gemm(int M, int N, int K, float alpha, const float *A, int lda, const f
         (e = cudaStreamWaitEvent(cs->h2d, allocated, 0)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(cs->d2h, allocated, 0)) != cudaSuccess)
         return fail(cuda_fail(e));
-    // Block 0 is multiplied in k-chunks as the matching rows of B arrive, so
-    // the first GEMM starts after a quarter of B is in rather than all of it:
-    // copy order A_0, C_0, B chunk by chunk, then A_i, C_i of the later blocks.
-    // Later chunks accumulate into C_0 (beta = 1), which changes the rounding
-    // of block 0 but not its bound.
-    const int kchunks = (need_ab && K >= 4096) ? 4 : 1;
-    const int kc = need_ab ? int(round_up((K + kchunks - 1) / kchunks, 64)) : 0;
-    for (int blk = 0; blk < nblk; ++blk) {
-        const int r0 = blk * rows_per_blk;
-        const int rows = std::min(rows_per_blk, M - r0);
-        if (rows <= 0) break;
+    // copy in on the h2d stream, then make `stream` wait for it
+    auto arrive = [&](cudaEvent_t ev) {
+        cudaError_t r = cudaEventRecord(ev, cs->h2d);
+        return r == cudaSuccess ? cudaStreamWaitEvent(stream, ev, 0) : r;
+    };
+    auto gemm = [&](int rows, int k, const float *a, const float *b, float *Bhi, float *Blo,
+                    float beta_x, float *c) {
+        if (!tensor) return sgemm_device(rows, N, k, alpha, a, K, b, N, beta_x, c, N, stream);
+        return t3_run(rows, N, k, alpha, a, K, Bhi, Blo, ldk, beta_x, c, N, Ah, Al,
+                      dev->sm_count, stream);
+    };
+    for (size_t bi = 0; bi < blocks.size(); ++bi) {
+        const int r0 = blocks[bi].first, rows = blocks[bi].second;
         cudaEvent_t in = evs.make(), out = evs.make();
         if (!in || !out) return fail(SGEMM_ERR_CUDA);
-        e = cudaSuccess;
-        if (need_ab)
-            e = cudaMemcpy2DAsync(dA + (size_t)r0 * K, size_t(K) * 4, A + (size_t)r0 * lda,
-                                  size_t(lda) * 4, size_t(K) * 4, size_t(rows),
-                                  cudaMemcpyHostToDevice, cs->h2d);
-        if (e == cudaSuccess && need_c_in)
-            e = cudaMemcpy2DAsync(dC + (size_t)r0 * N, size_t(N) * 4, C + (size_t)r0 * ldc,
-                                  size_t(ldc) * 4, size_t(N) * 4, size_t(rows),
-                                  cudaMemcpyHostToDevice, cs->h2d);
-        if (e == cudaSuccess) e = cudaEventRecord(in, cs->h2d);
-        if (e != cudaSuccess) return fail(cuda_fail(e));
         const float *a_blk = need_ab ? dA + (size_t)r0 * K : nullptr;
         float *c_blk = dC + (size_t)r0 * N;
-        if (!need_ab) {
-            if ((e = cudaStreamWaitEvent(stream, in, 0)) != cudaSuccess) return fail(cuda_fail(e));
-            st = sgemm_device(rows, N, K, alpha, nullptr, std::max(1, K), nullptr, std::max(1, N),
-                              beta, c_blk, N, stream);
-        } else if (blk == 0) {
+        if (bi == 0 && need_ab) {
+            // block 0: copy order A_0 chunk, (C_0 unless deferred), B chunk, ...
             for (int c = 0; c < kchunks; ++c) {
                 const int k0 = c * kc, kn = std::min(kc, K - k0);
                 if (kn <= 0) break;
-                cudaEvent_t bin = evs.make();
-                if (!bin) return fail(SGEMM_ERR_CUDA);
-                e = cudaMemcpy2DAsync(dB + (size_t)k0 * N, size_t(N) * 4, B + (size_t)k0 * ldb,
-                                      size_t(ldb) * 4, size_t(N) * 4, size_t(kn),
-                                      cudaMemcpyHostToDevice, cs->h2d);
-                if (e == cudaSuccess) e = cudaEventRecord(bin, cs->h2d);
-                if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, bin, 0);
+                cudaEvent_t chunk = evs.make();
+                if (!chunk) return fail(SGEMM_ERR_CUDA);
+                e = cudaMemcpy2DAsync(dA + k0, size_t(K) * 4, A + k0, size_t(lda) * 4,
+                                      size_t(kn) * 4, size_t(rows), cudaMemcpyHostToDevice, cs->h2d);
+                if (e == cudaSuccess && c == 0 && need_c_in && !defer_c_in)
+                    e = cudaMemcpy2DAsync(c_blk, size_t(N) * 4, C, size_t(ldc) * 4, size_t(N) * 4,
+                                          size_t(rows), cudaMemcpyHostToDevice, cs->h2d);
+                if (e == cudaSuccess)
+                    e = cudaMemcpy2DAsync(dB + (size_t)k0 * N, size_t(N) * 4, B + (size_t)k0 * ldb,
+                                          size_t(ldb) * 4, size_t(N) * 4, size_t(kn),
+                                          cudaMemcpyHostToDevice, cs->h2d);
+                if (e == cudaSuccess) e = arrive(chunk);
                 if (e != cudaSuccess) return fail(cuda_fail(e));
-                const float beta_c = c == 0 ? beta : 1.0f;
-                if (tensor) {
-                    if ((st = t3_split_b(N, kn, dB + (size_t)k0 * N, N, Bh + k0, Bl + k0, ldk,
-                                         stream)) != SGEMM_OK)
-                        return fail(st);
-                    st = t3_run(rows, N, kn, alpha, a_blk + k0, K, Bh + k0, Bl + k0, ldk, beta_c,
-                                c_blk, N, Ah, Al, dev->sm_count, stream);
-                } else {
-                    st = sgemm_device(rows, N, kn, alpha, a_blk + k0, K, dB + (size_t)k0 * N, N,
-                                      beta_c, c_blk, N, stream);
-                }
-                if (st != SGEMM_OK) return fail(st);
+                if (tensor && (st = t3_split_b(N, kn, dB + (size_t)k0 * N, N, Bh + k0, Bl + k0,
+                                               ldk, stream)) != SGEMM_OK)
+                    return fail(st);
+                const float beta_c = c > 0 ? 1.0f : (defer_c_in ? 0.0f : beta);
+                if ((st = gemm(rows, kn, a_blk + k0, dB + (size_t)k0 * N, Bh + k0, Bl + k0,
+                               beta_c, c_blk)) != SGEMM_OK)
+                    return fail(st);
+            }
+            if (defer_c_in) {
+                e = cudaMemcpy2DAsync(dCin, size_t(N) * 4, C, size_t(ldc) * 4, size_t(N) * 4,
+                                      size_t(rows), cudaMemcpyHostToDevice, cs->h2d);
+                if (e == cudaSuccess) e = arrive(in);
+                if (e != cudaSuccess) return fail(cuda_fail(e));
+                const long long n = (long long)rows * N;
+                const int grid = int(std::min<long long>((n + 255) / 256, (long long)dev->sm_count * 8));
+                sg::add_scaled_kernel<<<grid, 256, 0, stream>>>(c_blk, N, dCin, N, rows, N, beta);
+                g_launches.fetch_add(1);
+                if ((e = cudaGetLastError()) != cudaSuccess) return fail(cuda_fail(e));
             }
         } else {
-            // block i >= 1: its copies follow all of B on the copy stream
-            if ((e = cudaStreamWaitEvent(stream, in, 0)) != cudaSuccess) return fail(cuda_fail(e));
-            st = tensor ? t3_run(rows, N, K, alpha, a_blk, K, Bh, Bl, ldk, beta, c_blk, N, Ah, Al,
-                                 dev->sm_count, stream)
-                        : sgemm_device(rows, N, K, alpha, a_blk, K, dB, N, beta, c_blk, N, stream);
+            // later blocks (all of B already copied) and the no-multiply case
+            e = cudaSuccess;
+            if (need_ab)
+                e = cudaMemcpy2DAsync(dA + (size_t)r0 * K, size_t(K) * 4, A + (size_t)r0 * lda,
+                                      size_t(lda) * 4, size_t(K) * 4, size_t(rows),
+                                      cudaMemcpyHostToDevice, cs->h2d);
+            if (e == cudaSuccess && need_c_in)
+                e = cudaMemcpy2DAsync(c_blk, size_t(N) * 4, C + (size_t)r0 * ldc, size_t(ldc) * 4,
+                                      size_t(N) * 4, size_t(rows), cudaMemcpyHostToDevice, cs->h2d);
+            if (e == cudaSuccess) e = arrive(in);
+            if (e != cudaSuccess) return fail(cuda_fail(e));
+            st = need_ab ? gemm(rows, K, a_blk, dB, Bh, Bl, beta, c_blk)
+                         : sgemm_device(rows, N, K, alpha, nullptr, std::max(1, K), nullptr,
+                                        std::max(1, N), beta, c_blk, N, stream);
+            if (st != SGEMM_OK) return fail(st);
         }
-        if (st != SGEMM_OK) return fail(st);
         e = cudaEventRecord(out, stream);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(cs->d2h, out, 0);
         if (e == cudaSuccess)

@@ -119,18 +119,21 @@ int sgemm_ex(int M, int N, int K, float alpha,
  *
  * A, B, C are host pointers (page-locked memory gives the fastest copies, but
  * pageable memory is accepted).  The call works through row blocks of A and C
- * (up to 8 blocks of at least 1024 rows): block i is copied in on a
- * host-to-device copy stream, multiplied on `stream` while block i+1 is copied
- * in, and copied back into C (respecting ldc) on a device-to-host copy stream
- * while block i+1 is multiplied.  B is copied after block 0, in four k-chunks
- * when K >= 4096, and block 0 is multiplied chunk by chunk (accumulating into
- * its C rows) as the chunks land, so the first GEMM need not wait for all of
- * B.  Device buffers come from the library pool; the two copy streams are the
- * library's own (one pair per device).  `stream` is synchronised before
- * returning, so C holds the result on return.  Results meet the same
- * tolerance as sgemm(); they need not be bitwise equal to one sgemm() call on
- * the whole matrix (row blocks change the k split of leftover tiles, and the
- * k-chunks of block 0 round its partial sums in C).
+ * (M >= 2048: a first and a last block of 1024 rows, blocks of about 2048 rows
+ * between them; one block otherwise): block i is copied in on a host-to-device
+ * copy stream, multiplied on `stream` while block i+1 is copied in, and copied
+ * back into C (respecting ldc) on a device-to-host copy stream while block i+1
+ * is multiplied.  When K >= 4096, block 0 and B are copied in four k-chunks
+ * (columns of A, rows of B) and block 0 is multiplied chunk by chunk as they
+ * land, the first chunk with beta = 0 and the others accumulating into its C
+ * rows; beta * C_in is added to block 0 after its C_in has been copied in
+ * behind the chunks.  So the first GEMM waits for a quarter of B and of A's
+ * first block only.  Device buffers come from the library pool; the two copy
+ * streams are the library's own (one pair per device).  `stream` is
+ * synchronised before returning, so C holds the result on return.  Results
+ * meet the same tolerance as sgemm(); they need not be bitwise equal to one
+ * sgemm() call on the whole matrix (row blocks change the k split of leftover
+ * tiles, and the k-chunks of block 0 round its partial sums in C).
  */
 int sgemm_host(int M, int N, int K, float alpha,
                const float *A, int lda,
@@ -160,8 +163,11 @@ int sgemm_3xtf32(int M, int N, int K, float alpha,
 /*
  * sgemm_host_3xtf32 -- sgemm_host() through the 3xTF32 tensor-core path: B is
  * split once on the device, each row block of A is split and multiplied as
- * in sgemm_3xtf32().  Same arguments, pipelining and synchronisation as
- * sgemm_host(); same tolerance as sgemm_3xtf32().
+ * in sgemm_3xtf32().  Same arguments and synchronisation as sgemm_host(); the
+ * pipeline differs in two points (this path is bound by the host link, not
+ * by its first multiply): equal row blocks of at least 1024 rows (at most 8),
+ * and block 0's C_in is copied in front of its first chunk.  Same tolerance as
+ * sgemm_3xtf32().
  */
 int sgemm_host_3xtf32(int M, int N, int K, float alpha,
                       const float *A, int lda,

@@ -278,8 +278,9 @@ def test_stream_k_split_matches_oracle(M, N, K, kernel):
 @pytest.mark.parametrize("pinned", [True, False])
 def test_host_entry_point_pipelined_over_row_blocks(tensor_cores, pinned):
     """M = 4100 splits into four row blocks (copy in, multiply, copy back
-    overlap); padded leading dimensions and beta != 0; checked against the
-    oracle on seeded rows (including block boundaries) and columns."""
+    overlap): 1024, 1026, 1026 and 1024 rows on the FFMA path, four of 1025 on
+    the 3xTF32 path; padded leading dimensions and beta != 0; checked against
+    the oracle on rows at every block boundary of both and on columns."""
     import torch
     from dense_fp32_gemm_02_gb300 import binding
     M, N, K = 4100, 777, 515
@@ -293,7 +294,7 @@ def test_host_entry_point_pipelined_over_row_blocks(tensor_cores, pinned):
         tB = torch.from_numpy(B.base.copy()).pin_memory()[:, :N]
         cbuf = cbuf.pin_memory()
     binding.sgemm_host(tA, tB, cbuf[:, :N], 1.25, -0.5, tensor_cores=tensor_cores)
-    rows = np.array([0, 1, 1024, 1025, 2049, 3074, 3075, 4099], np.int64)
+    rows = np.array([0, 1, 1023, 1024, 2049, 2050, 3075, 3076, 4099], np.int64)
     cols = np.array([0, 5, 300, 776], np.int64)
     got = cbuf.numpy()
     ref, bound = oracle.sgemm_rows(A, B, C, 1.25, -0.5, rows)
@@ -306,11 +307,14 @@ def test_host_entry_point_pipelined_over_row_blocks(tensor_cores, pinned):
 
 @pytest.mark.parametrize("tensor_cores", [False, True])
 def test_host_entry_point_first_block_in_k_chunks(tensor_cores):
-    """K >= 4096: block 0 is multiplied in four k-chunks of B (1088, 1088,
-    1088 and 836 rows here, none a multiple of the tile depth at the end) as
-    they arrive, accumulating into its rows of C; block 1 takes the whole of
-    K.  beta != 0 and padded leading dimensions; oracle on rows of both
-    blocks and on columns."""
+    """K >= 4096: block 0 is multiplied in four k-chunks of A and B (1088,
+    1088, 1088 and 836 here, the last not a multiple of the tile depth) as
+    they arrive, accumulating into its rows of C.  FFMA path: blocks of 1024
+    and 1076 rows, the first chunk with beta = 0 and beta * C_in added once
+    C_in has arrived; 3xTF32 path: two blocks of 1050 rows, C_in copied in
+    front.  The other block takes the whole of K.  beta != 0 and padded
+    leading dimensions; oracle on rows at both plans' boundaries and on
+    columns."""
     import torch
     from dense_fp32_gemm_02_gb300 import binding
     M, N, K = 2100, 300, 4100
@@ -320,7 +324,7 @@ def test_host_entry_point_first_block_in_k_chunks(tensor_cores):
     tB = torch.from_numpy(B.base.copy()).pin_memory()[:, :N]
     cbuf = torch.from_numpy(C.base.copy()).pin_memory()
     binding.sgemm_host(tA, tB, cbuf[:, :N], 0.75, 1.5, tensor_cores=tensor_cores)
-    rows = np.array([0, 1, 777, 1049, 1050, 1051, 2099], np.int64)
+    rows = np.array([0, 1, 777, 1023, 1024, 1025, 1049, 1050, 2099], np.int64)
     cols = np.array([0, 150, 299], np.int64)
     got = cbuf.numpy()
     ref, bound = oracle.sgemm_rows(A, B, C, 0.75, 1.5, rows)
@@ -329,3 +333,22 @@ def test_host_entry_point_first_block_in_k_chunks(tensor_cores):
     assert_within_bound(got[:, cols], ref, bound, "chunked host cols")
     assert np.isnan(got[:, N:]).all(), "C padding written"
     assert binding.device_status() == binding.SGEMM_OK
+
+
+@pytest.mark.parametrize("tensor_cores", [False, True])
+def test_host_entry_point_k_chunks_with_beta_zero_never_read_c(tensor_cores):
+    """K >= 4096 and beta = 0: block 0's chunks start from beta = 0 with no
+    C_in to add, and C_in (NaN here) is never copied in or read."""
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    M, N, K = 2300, 260, 4096
+    A, B, _ = make_inputs(M, N, K, "upm1", "upm1", None, seed=41)
+    tA = torch.from_numpy(np.ascontiguousarray(A)).pin_memory()
+    tB = torch.from_numpy(np.ascontiguousarray(B)).pin_memory()
+    hC = torch.full((M, N), float("nan")).pin_memory()
+    binding.sgemm_host(tA, tB, hC, -1.5, 0.0, tensor_cores=tensor_cores)
+    rows = np.array([0, 1023, 1024, 1276, 2299], np.int64)
+    ref, bound = oracle.sgemm_rows(A, B, None, -1.5, 0.0, rows)
+    got = hC.numpy()
+    assert not np.isnan(got).any()
+    assert_within_bound(got[rows], ref, bound, "beta = 0 chunked host rows")
