@@ -96,6 +96,7 @@ struct TileConfig {
     // epilogue (see ExConfig); the plain kernel leaves that code out, which
     // keeps its main loop under the register cap.
     static constexpr bool EX = false;
+    static constexpr bool BATCH = false;
 
     static_assert(WM * WARPS_M == BM && WN * WARPS_N == BN, "warp grid must cover the tile");
     static_assert(TM % 4 == 0 && TN % 4 == 0, "thread tile is made of 4x4 sub-tiles");
@@ -115,6 +116,16 @@ enum Act : int { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU = 2 };
 template <class Base>
 struct ExConfig : Base {
     static constexpr bool EX = true;
+    static constexpr bool BATCH = true;
+};
+
+// The same tile configuration with the fused epilogue but one GEMM (2-D
+// tensor maps, no batch coordinate): a bias or an activation on an unbatched
+// call.
+template <class Base>
+struct FusedConfig : Base {
+    static constexpr bool EX = true;
+    static constexpr bool BATCH = false;
 };
 
 struct MainParams {
@@ -627,7 +638,7 @@ __device__ __forceinline__ bool issue_one(State &st, const Ring<Cfg> &ring,
         st.have = 1;
         st.slab = sg.kb;
         int tm, tn;
-        if constexpr (Cfg::EX) {
+        if constexpr (Cfg::BATCH) {
             int tb;
             decode_tile(p, sg.tile, tb, tm, tn);
             st.tb = tb;
@@ -646,7 +657,7 @@ __device__ __forceinline__ bool issue_one(State &st, const Ring<Cfg> &ring,
         return false;
     }
     mbar_arrive_expect_tx_at(ring.full(s), Cfg::STAGE_BYTES);
-    if constexpr (Cfg::EX) {
+    if constexpr (Cfg::BATCH) {
         tma_load_3d_at(ring.a(s), tmA, ring.full(s), st.tm * Cfg::BM, st.slab * Cfg::BK,
                        x.a_planes > 1 ? st.tb : 0);
         tma_load_3d_at(ring.b(s), tmB, ring.full(s), st.tn * Cfg::BN, st.slab * Cfg::BK,
@@ -827,10 +838,13 @@ __device__ __forceinline__ void consumer_loop(const Ring<Cfg> &ring, const MainP
             Segment seg;
             segment_at(p, k_tiles, si, seg);
             int tm, tn;
-            if constexpr (Cfg::EX) {
+            if constexpr (Cfg::BATCH) {
                 int tb;
                 decode_tile(p, seg.tile, tb, tm, tn);
                 store_tile_ex<Cfg>(acc, p, x, tb, tm, tn, a_off(), b_off());
+            } else if constexpr (Cfg::EX) {
+                tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                store_tile_ex<Cfg>(acc, p, x, 0, tm, tn, a_off(), b_off());
             } else {
                 tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
                 store_tile<Cfg>(acc, p, tm, tn, a_off(), b_off());
@@ -877,7 +891,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     __shared__ FixInfo fix;
     // issuer state in shared memory (ISSUE_THREAD0, ISSUE_LAST_WARP): keeping
     // it out of registers leaves them to the accumulators
-    __shared__ typename std::conditional<Cfg::EX, IssueStateEx, IssueState>::type ist;
+    __shared__ typename std::conditional<Cfg::BATCH, IssueStateEx, IssueState>::type ist;
     __shared__ int released[STAGES];   // ISSUE_LAST_WARP: warps done with a stage
 
     const int warp = threadIdx.x >> 5;
@@ -904,7 +918,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // ======================================================== producer
             regs_decrease<Cfg::PRODUCER_REGS>();
             if (warp != 0) return;
-            typename std::conditional<Cfg::EX, IssueStateEx, IssueState>::type st;
+            typename std::conditional<Cfg::BATCH, IssueStateEx, IssueState>::type st;
             st.init(p);
             if (lane == 0) {
                 tma_prefetch_desc(&tmA);

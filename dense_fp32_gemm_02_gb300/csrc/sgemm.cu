@@ -110,11 +110,17 @@ const Variant kVariants[] = {
 };
 constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
 
-// Batched calls and calls with a bias or an activation run the default
-// configuration compiled with the batch and fused-epilogue code.
+// Batched calls run the default configuration compiled with the batch
+// coordinate (3-D tensor maps) and the fused epilogue; unbatched calls with a
+// bias or an activation run it with the fused epilogue alone (2-D maps), which
+// keeps the plain kernel's 123 registers (the batched one needs 128).
 const Variant kExVariant =
     make_variant<sg::ExConfig<sg::TileConfig<256, 128, 64, 2, 8, 2, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>>>(
         "ffma2 tile=256x128x64 stages=2 warps=16 issuer=last_warp thread=8x8 stream_k batched+epilogue",
+        true);
+const Variant kFusedVariant =
+    make_variant<sg::FusedConfig<sg::TileConfig<256, 128, 64, 2, 8, 2, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>>>(
+        "ffma2 tile=256x128x64 stages=2 warps=16 issuer=last_warp thread=8x8 stream_k epilogue",
         true);
 std::atomic<int> g_forced_variant{-1};
 
@@ -250,6 +256,7 @@ int device_state(DeviceState **out) {
             for (const Variant &v : kVariants)
                 if ((e = v.set_attr()) != cudaSuccess) return cuda_fail(e);
             if ((e = kExVariant.set_attr()) != cudaSuccess) return cuda_fail(e);
+            if ((e = kFusedVariant.set_attr()) != cudaSuccess) return cuda_fail(e);
             e = cudaFuncSetAttribute(sg::t3::sgemm_3xtf32_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      int(sg::t3::SMEM_BYTES));
@@ -406,10 +413,11 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
     if (g.K == 0 || g.alpha == 0.0f) return launch_scale(stream, g, dev->sm_count);
 
     const int M = g.M, N = g.N, K = g.K;
-    const bool extended = g.batch > 1 || g.bias != nullptr || g.act != sg::ACT_NONE;
+    const bool batched = g.batch > 1;
+    const bool extended = batched || g.bias != nullptr || g.act != sg::ACT_NONE;
     if (!extended && g_forced_variant.load() < 0 && small_problem(M, N, K, dev->sm_count))
         return launch_small(g, stream, dev->sm_count);
-    const Variant &var = extended ? kExVariant : kVariants[pick_variant(M, N, K)];
+    const Variant &var = batched ? kExVariant : extended ? kFusedVariant : kVariants[pick_variant(M, N, K)];
     // A and B enter as one plane per batch, or one plane for all batches when
     // their stride is 0
     const int a_planes = (g.batch > 1 && g.stride_a != 0) ? g.batch : 1;
@@ -486,9 +494,9 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
         return cuda_fail(e);
     }
 
-    // the plain kernel takes 2-D tensor maps, the batched one 3-D maps
+    // the batched kernel takes 3-D tensor maps, the others 2-D maps
     CUtensorMap tmA, tmB;
-    if (extended) {
+    if (batched) {
         if ((st = encode_3d(&tmA, At, M, K, a_planes, ldat, at_plane, var.bm, var.bk)) == SGEMM_OK)
             st = encode_3d(&tmB, Bp, N, K, b_planes, ldbp, b_planes > 1 ? bp_plane : K * ldbp,
                            var.bn, var.bk);

@@ -82,9 +82,11 @@ def _check(got, As, Bs, Cs, alpha, beta, biases, act, what, exact=False):
 
 
 @pytest.mark.parametrize("act", ["none", "relu"])
-def test_integer_grid_bit_exact(act):
-    # integers in [-4, 4] and integer bias/C: exact in any summation order
-    batch, M, N, K = 3, 300, 257, 129
+@pytest.mark.parametrize("batch", [1, 3])
+def test_integer_grid_bit_exact(act, batch):
+    # integers in [-4, 4] and integer bias/C: exact in any summation order;
+    # batch 1 runs the unbatched fused-epilogue kernel, 3 the batched one
+    M, N, K = 300, 257, 129
     As, Bs, Cs = _inputs(batch, M, N, K, "int4", "int4", seed=1)
     rng = np.random.default_rng(2)
     biases = [rng.integers(-50, 51, N).astype(np.float32) for _ in range(batch)]
@@ -93,7 +95,7 @@ def test_integer_grid_bit_exact(act):
 
 
 @pytest.mark.parametrize("shape", [(2, 513, 385, 200), (3, 300, 257, 129), (5, 64, 72, 1023),
-                                   (1, 1030, 700, 515)])
+                                   (1, 1030, 700, 515), (1, 2048, 1100, 1056)])
 @pytest.mark.parametrize("act", ["none", "relu", "gelu"])
 def test_random_parity(shape, act):
     batch, M, N, K = shape
