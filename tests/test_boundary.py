@@ -62,8 +62,9 @@ def test_status_strings_and_version(lib):
     assert lib.sgemm_version() >= 10000
 
 
-def _call(lib, M, N, K, A=1, lda=None, B=1, ldb=None, C=1, ldc=None, alpha=1.0, beta=0.0):
-    f = lib.sgemm
+def _call(lib, M, N, K, A=1, lda=None, B=1, ldb=None, C=1, ldc=None, alpha=1.0, beta=0.0,
+          entry="sgemm"):
+    f = getattr(lib, entry)
     f.argtypes = [ctypes.c_int] * 3 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_int,
                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_float,
                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
@@ -90,9 +91,14 @@ INVALID = [
 ]
 
 
+# every entry point with the sgemm() argument list
+ENTRIES = ["sgemm", "sgemm_host", "sgemm_3xtf32", "sgemm_host_3xtf32", "sgemm_noalloc"]
+
+
+@pytest.mark.parametrize("entry", ENTRIES)
 @pytest.mark.parametrize("kw", INVALID)
-def test_invalid_arguments_rejected_without_gpu(lib, kw):
-    assert _call(lib, **kw) == 1  # SGEMM_ERR_INVALID_ARG
+def test_invalid_arguments_rejected_without_gpu(lib, kw, entry):
+    assert _call(lib, entry=entry, **kw) == 1  # SGEMM_ERR_INVALID_ARG
 
 
 def test_misaligned_pointer_rejected(lib):
@@ -104,11 +110,12 @@ def test_misaligned_pointer_rejected(lib):
     assert f(4, 4, 4, 1.0, 0x100000, 4, 0x200000, 4, 0.0, 0x300002, 4, None) == 1
 
 
+@pytest.mark.parametrize("entry", ENTRIES)
 @pytest.mark.parametrize("kw", [dict(M=0, N=4, K=4), dict(M=4, N=0, K=4),
                                 dict(M=0, N=0, K=0, A=None, B=None, C=None)])
-def test_empty_output_is_a_no_op_without_gpu(lib, kw):
+def test_empty_output_is_a_no_op_without_gpu(lib, kw, entry):
     # nothing to compute: success without any CUDA call, pointers not read
-    assert _call(lib, **kw) == 0
+    assert _call(lib, entry=entry, **kw) == 0
 
 
 def test_variant_selection_validates(lib):
