@@ -22,8 +22,10 @@
  *  - Pointers must be 4-byte aligned; no other alignment is required.
  *  - C must not overlap A or B (not checked).
  *  - Summation order is fixed per build and shape: results are bitwise
- *    reproducible run to run.  Each element is one fp32 fused-multiply-add chain
- *    over k ascending, then alpha and beta are applied once.
+ *    reproducible run to run.  On the FFMA path each element's k terms are
+ *    accumulated by fp32 fused multiply-adds over k ascending; where the work
+ *    split cuts a tile along k (stream-K), the pieces' partial sums are added in
+ *    k order.  alpha and beta are applied once, after the sum.
  *  - Nothing here exits or aborts the process: every failure is a status code.
  */
 #ifndef DENSE_FP32_GEMM_02_GB300_SGEMM_H
