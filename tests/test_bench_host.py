@@ -36,3 +36,23 @@ def test_dram_use_is_traffic_over_time_against_the_measured_copy_bandwidth():
     assert d["dram_frac"] == pytest.approx(200.0 / peak, abs=1e-4)
     assert bench.dram_use(None, 15.0) == {"dram_gbs": None, "dram_frac": None}
     assert bench.dram_use(3.0e9, 0.0) == {"dram_gbs": None, "dram_frac": None}
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
+    """Rank 0 of the reference arm times the oracle on rows of the workload and
+    prints one JSON line with the bench contract's keys (no GPU)."""
+    import bench
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    args = argparse.Namespace(workload="sgemm_256", steps=2, warmup=1, gpus=1)
+    assert bench.run_reference(args) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "GFLOP/s" and line["value"] > 0 and line["higher_is_better"] is True
+    assert (line["steps"], line["warmup"], line["n_gpus"]) == (2, 1, 1)
+    cpu = line["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] == bench.host_cores()
+    assert cpu["value"] == line["value"] and "rows" in cpu["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"] == "sgemm_256"
