@@ -28,9 +28,13 @@ def test_oracle_table_times_every_workload_with_all_cores_and_one(monkeypatch, c
 
 
 def test_dram_use_is_traffic_over_time_against_the_measured_copy_bandwidth():
+    import os
     import bench
-    with open(bench.PEAKS_FILE) as f:
-        peak = json.load(f)["hbm_gbs"]
+    if os.path.exists(bench.PEAKS_FILE):      # driver-written; the fallback otherwise
+        with open(bench.PEAKS_FILE) as f:
+            peak = json.load(f)["hbm_gbs"]
+    else:
+        peak = bench.HBM_FALLBACK_GBS
     d = bench.dram_use(3.0e9, 15.0)              # 3 GB in 15 ms = 200 GB/s
     assert d["dram_gbs"] == pytest.approx(200.0)
     assert d["dram_frac"] == pytest.approx(200.0 / peak, abs=1e-4)
