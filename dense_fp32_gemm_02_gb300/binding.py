@@ -65,6 +65,8 @@ lib.sgemm_variant_name.argtypes = [_i]
 lib.sgemm_variant_name.restype = ctypes.c_char_p
 lib.sgemm_set_variant.argtypes = [_i]
 lib.sgemm_set_variant.restype = _i
+lib.sgemm_set_3xtf32_kernel.argtypes = [_i]
+lib.sgemm_set_3xtf32_kernel.restype = _i
 
 SGEMM_OK = 0
 SGEMM_ERR_INVALID_ARG = 1
@@ -315,3 +317,9 @@ def variants() -> list:
 def set_variant(variant_id: int) -> None:
     """Force a kernel variant for later calls (-1: automatic choice)."""
     check(lib.sgemm_set_variant(int(variant_id)))
+
+
+def set_3xtf32_kernel(pair: bool) -> None:
+    """3xTF32 main kernel for later calls: the CTA pair (True) or the
+    single-CTA kernel (False, the default)."""
+    check(lib.sgemm_set_3xtf32_kernel(1 if pair else 0))

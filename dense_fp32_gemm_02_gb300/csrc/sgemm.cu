@@ -25,6 +25,7 @@
 #include "../../include/sgemm.h"
 #include "kernels.cuh"
 #include "tf32x3.cuh"
+#include "tf32x3_pair.cuh"
 
 #define SGEMM_API extern "C" __attribute__((visibility("default")))
 
@@ -123,6 +124,8 @@ const Variant kFusedVariant =
         "ffma2 tile=256x128x64 stages=2 warps=16 issuer=last_warp thread=8x8 stream_k epilogue",
         true);
 std::atomic<int> g_forced_variant{-1};
+// 3xTF32 main kernel: 0 = the single-CTA kernel (default), 1 = the CTA pair
+std::atomic<int> g_t3_pair{0};
 
 // Shape heuristic between the two orientations of the default tile, 256x128
 // (variant 0) and 128x256 (variant 1): same kernel, same speed where both fit
@@ -257,6 +260,10 @@ int device_state(DeviceState **out) {
                 if ((e = v.set_attr()) != cudaSuccess) return cuda_fail(e);
             if ((e = kExVariant.set_attr()) != cudaSuccess) return cuda_fail(e);
             if ((e = kFusedVariant.set_attr()) != cudaSuccess) return cuda_fail(e);
+            if ((e = cudaFuncSetAttribute(sg::t3::sgemm_3xtf32_pair_kernel,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          int(sg::t3::P_SMEM_BYTES))) != cudaSuccess)
+                return cuda_fail(e);
             e = cudaFuncSetAttribute(sg::t3::sgemm_3xtf32_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      int(sg::t3::SMEM_BYTES));
@@ -574,14 +581,19 @@ int t3_run(int M, int N, int K, float alpha, const float *A, int lda, const floa
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
-    CUtensorMap mAh, mAl, mBh, mBl, mBh2, mBl2;   // *2: boxes of BN/2 rows (half-width tiles)
+    // The CTA-pair kernel needs an even number of SMs (pairs of CTAs, one per SM).
+    const bool pair = g_t3_pair.load() != 0 && sm_count >= 2;
+    // B boxes: the rows of B^T one CTA copies for a whole tile, and half that
+    // for the half-width tiles of the last wave (*2)
+    const int b_rows = pair ? t3::P_BN / 2 : t3::BN;
+    CUtensorMap mAh, mAl, mBh, mBl, mBh2, mBl2;
     const auto sw = t3::ROW_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     if ((st = encode_2d(&mAh, Ah, K, M, ldk, t3::BK, t3::BM, sw)) != SGEMM_OK ||
         (st = encode_2d(&mAl, Al, K, M, ldk, t3::BK, t3::BM, sw)) != SGEMM_OK ||
-        (st = encode_2d(&mBh, Bh, K, N, ldk, t3::BK, t3::BN, sw)) != SGEMM_OK ||
-        (st = encode_2d(&mBl, Bl, K, N, ldk, t3::BK, t3::BN, sw)) != SGEMM_OK ||
-        (st = encode_2d(&mBh2, Bh, K, N, ldk, t3::BK, t3::BN / 2, sw)) != SGEMM_OK ||
-        (st = encode_2d(&mBl2, Bl, K, N, ldk, t3::BK, t3::BN / 2, sw)) != SGEMM_OK)
+        (st = encode_2d(&mBh, Bh, K, N, ldk, t3::BK, b_rows, sw)) != SGEMM_OK ||
+        (st = encode_2d(&mBl, Bl, K, N, ldk, t3::BK, b_rows, sw)) != SGEMM_OK ||
+        (st = encode_2d(&mBh2, Bh, K, N, ldk, t3::BK, b_rows / 2, sw)) != SGEMM_OK ||
+        (st = encode_2d(&mBl2, Bl, K, N, ldk, t3::BK, b_rows / 2, sw)) != SGEMM_OK)
         return st;
     t3::Params p;
     p.C = C;
@@ -591,20 +603,28 @@ int t3_run(int M, int N, int K, float alpha, const float *A, int lda, const floa
     p.K = K;
     p.alpha = alpha;
     p.beta = beta;
-    p.tiles_m = int((M + t3::BM - 1) / t3::BM);
-    p.tiles_n = int((N + t3::BN - 1) / t3::BN);
-    // 16 tile rows per raster group: a wave of 152 tiles then covers 16 rows
-    // x 9.5 columns of tiles, the fewest distinct A and B panels; measured at
-    // 8192^3: group 4 3.28 ms, 8 3.18, 12 3.11, 16 3.07, 20 3.10, 32 3.18
-    p.group_m = 16;
+    const int tile_m = pair ? t3::P_BM : t3::BM, tile_n = pair ? t3::P_BN : t3::BN;
+    p.tiles_m = int((M + tile_m - 1) / tile_m);
+    p.tiles_n = int((N + tile_n - 1) / tile_n);
+    // 2048 rows of C per raster group (16 rows of 128-row tiles, 8 of the
+    // pair's 256-row tiles): a wave then covers the fewest distinct A and B
+    // panels; measured at 8192^3 on the single-CTA kernel: group 4 3.28 ms,
+    // 8 3.18, 12 3.11, 16 3.07, 20 3.10, 32 3.18
+    p.group_m = 2048 / tile_m;
     p.timeout_ns = g_timeout_ns.load();
     const long long tiles = (long long)p.tiles_m * p.tiles_n;
     if (tiles > 0x7fffffffLL) return SGEMM_ERR_INVALID_ARG;
-    const unsigned grid = unsigned(std::min<long long>(tiles, sm_count));
     {
         ProfScope prof(stream, true);
-        t3::sgemm_3xtf32_kernel<<<grid, t3::THREADS, t3::SMEM_BYTES, stream>>>(mAh, mAl, mBh,
-                                                                               mBl, mBh2, mBl2, p);
+        if (pair) {
+            const unsigned pairs = unsigned(std::min<long long>(tiles, sm_count / 2));
+            t3::sgemm_3xtf32_pair_kernel<<<2 * pairs, t3::THREADS, t3::P_SMEM_BYTES, stream>>>(
+                mAh, mAl, mBh, mBl, mBh2, mBl2, p);
+        } else {
+            const unsigned grid = unsigned(std::min<long long>(tiles, sm_count));
+            t3::sgemm_3xtf32_kernel<<<grid, t3::THREADS, t3::SMEM_BYTES, stream>>>(
+                mAh, mAl, mBh, mBl, mBh2, mBl2, p);
+        }
         g_launches.fetch_add(1);
     }
     e = cudaGetLastError();
@@ -1144,6 +1164,12 @@ SGEMM_API const char *sgemm_variant_name(int id) {
 SGEMM_API int sgemm_set_variant(int id) {
     if (id < -1 || id >= kNumVariants) return SGEMM_ERR_INVALID_ARG;
     g_forced_variant.store(id);
+    return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_set_3xtf32_kernel(int pair) {
+    if (pair != 0 && pair != 1) return SGEMM_ERR_INVALID_ARG;
+    g_t3_pair.store(pair);
     return SGEMM_OK;
 }
 

@@ -101,3 +101,25 @@ def test_workloads_match_oracle(name):
     if cols is not None:
         ref, bound = oracle.sgemm_cols(A, B, c_in, w.alpha, w.beta, cols)
         assert_within_bound(dC[:, torch.from_numpy(cols).cuda()].cpu().numpy(), ref, bound, name)
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 513, 100), (1031, 777, 1500), (4100, 3001, 515),
+                                   (2048, 2048, 64), (4096, 4096, 64)])
+def test_cta_pair_kernel_matches_oracle(M, N, K):
+    """The CTA-pair main kernel (sgemm_set_3xtf32_kernel(1)): integer inputs bit-exact
+    and random inputs within the bound, on ragged pair tiles, fewer tiles than pairs
+    (2048^2: 64), several waves (4100 x 3001: 204 pair tiles over 76 pairs) and a
+    half-width last wave (4096^2: 256 tiles, the last 28 cut in halves)."""
+    from dense_fp32_gemm_02_gb300 import binding
+    binding.set_3xtf32_kernel(True)
+    try:
+        A, B, C = make_inputs(M, N, K, "int4", "int4", "int4", seed=M + 3 * N)
+        ref, _ = oracle.sgemm(A, B, C, 1.5, 0.5)
+        got = run3(A, B, C, 1.5, 0.5).cpu().numpy()
+        assert np.array_equal(got, ref), (M, N, K)
+        A, B, C = make_inputs(M, N, K, "upm1", "normal", "normal", seed=M + 5 * N)
+        ref, bound = oracle.sgemm(A, B, C, -0.75, 1.0)
+        got = run3(A, B, C, -0.75, 1.0).cpu().numpy()
+        assert_within_bound(got, ref, bound, f"pair {M}x{N}x{K}")
+    finally:
+        binding.set_3xtf32_kernel(False)
