@@ -319,7 +319,7 @@ def set_variant(variant_id: int) -> None:
     check(lib.sgemm_set_variant(int(variant_id)))
 
 
-def set_3xtf32_kernel(pair: bool) -> None:
-    """3xTF32 main kernel for later calls: the CTA pair (True) or the
-    single-CTA kernel (False, the default)."""
-    check(lib.sgemm_set_3xtf32_kernel(1 if pair else 0))
+def set_3xtf32_kernel(pair) -> None:
+    """3xTF32 main kernel for later calls: the CTA pair (True), the single-CTA
+    kernel (False) or the automatic choice per shape (None, the default)."""
+    check(lib.sgemm_set_3xtf32_kernel(-1 if pair is None else (1 if pair else 0)))

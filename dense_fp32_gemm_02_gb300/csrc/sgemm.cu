@@ -124,8 +124,9 @@ const Variant kFusedVariant =
         "ffma2 tile=256x128x64 stages=2 warps=16 issuer=last_warp thread=8x8 stream_k epilogue",
         true);
 std::atomic<int> g_forced_variant{-1};
-// 3xTF32 main kernel: 0 = the single-CTA kernel (default), 1 = the CTA pair
-std::atomic<int> g_t3_pair{0};
+// 3xTF32 main kernel: -1 = chosen per shape (t3_use_pair), 0 = the single-CTA
+// kernel, 1 = the CTA pair
+std::atomic<int> g_t3_pair{-1};
 
 // Shape heuristic between the two orientations of the default tile, 256x128
 // (variant 0) and 128x256 (variant 1): same kernel, same speed where both fit
@@ -567,6 +568,25 @@ int t3_split_b(int N, int K, const float *B, int ldb, float *Bh, float *Bl, long
 }
 
 // C = alpha*A*B + beta*C with B already split (Bh, Bl); Ah, Al: M x ldk scratch.
+// Waves of `tiles` equal tiles over `slots` CTAs (or CTA pairs), counting a
+// last partial wave of at most half the slots as half a wave (it runs as
+// half-width tiles).
+double t3_waves(long long tiles, long long slots) {
+    const long long w = tiles / slots, r = tiles % slots;
+    return double(w) + (r == 0 ? 0.0 : (2 * r <= slots ? 0.5 : 1.0));
+}
+
+// The CTA-pair kernel (256 x 256 tiles on 2 SMs) against the single-CTA one
+// (128 x 256 tiles): the same work per SM and tile, so the waves decide, with
+// the pair's faster main loop (about 5 % at 4096^3 and 8192^3, 13 % at
+// 16384x16384x512, same box) as the tie-break.  M = 2432, N = 2048 (152
+// single tiles, one wave; 80 pair tiles) stays on the single kernel.
+bool t3_use_pair(int M, int N, int sms) {
+    const long long ts = ((M + 127LL) / 128) * ((N + 255LL) / 256);
+    const long long tp = ((M + 255LL) / 256) * ((N + 255LL) / 256);
+    return 0.95 * t3_waves(tp, sms / 2) < t3_waves(ts, sms);
+}
+
 int t3_run(int M, int N, int K, float alpha, const float *A, int lda, const float *Bh,
            const float *Bl, long long ldk, float beta, float *C, int ldc, float *Ah, float *Al,
            int sm_count, cudaStream_t stream) {
@@ -581,8 +601,8 @@ int t3_run(int M, int N, int K, float alpha, const float *A, int lda, const floa
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
-    // The CTA-pair kernel needs an even number of SMs (pairs of CTAs, one per SM).
-    const bool pair = g_t3_pair.load() != 0 && sm_count >= 2;
+    const int forced = g_t3_pair.load();
+    const bool pair = sm_count >= 2 && (forced >= 0 ? forced == 1 : t3_use_pair(M, N, sm_count));
     // B boxes: the rows of B^T one CTA copies for a whole tile, and half that
     // for the half-width tiles of the last wave (*2)
     const int b_rows = pair ? t3::P_BN / 2 : t3::BN;
@@ -1168,7 +1188,7 @@ SGEMM_API int sgemm_set_variant(int id) {
 }
 
 SGEMM_API int sgemm_set_3xtf32_kernel(int pair) {
-    if (pair != 0 && pair != 1) return SGEMM_ERR_INVALID_ARG;
+    if (pair < -1 || pair > 1) return SGEMM_ERR_INVALID_ARG;
     g_t3_pair.store(pair);
     return SGEMM_OK;
 }

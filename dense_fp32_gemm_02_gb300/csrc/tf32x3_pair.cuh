@@ -69,7 +69,7 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
                  : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
                      bar),
                  "r"(bytes)
                  : "memory");

@@ -249,12 +249,13 @@ const char *sgemm_variant_name(int id);
 int sgemm_set_variant(int id);
 
 /*
- * Main kernel of the 3xTF32 entry points, for comparisons: 0 (the default) the
- * single-CTA kernel with 128 x 256 tiles, 1 each 256 x 256 tile on a pair of
- * SMs (a 2-CTA cluster sharing the MMA, tcgen05 cta_group::2; correct, but its
- * MMAs are not yet fed fast enough to beat the default).  Both meet the same
- * tolerance; results may differ in the last bits.  Applies to later calls in
- * this process; anything but 0 or 1 gives SGEMM_ERR_INVALID_ARG.
+ * Main kernel of the 3xTF32 entry points: -1 (the default) chooses per shape,
+ * 0 forces the single-CTA kernel (128 x 256 tiles), 1 the CTA-pair kernel (each
+ * 256 x 256 tile on a pair of SMs, a 2-CTA cluster sharing the MMA, tcgen05
+ * cta_group::2).  The automatic choice compares the two kernels' waves over the
+ * SMs and takes the pair on a tie (its main loop is faster).  Both meet the
+ * same tolerance; results may differ in the last bits.  Applies to later calls
+ * in this process; anything outside -1..1 gives SGEMM_ERR_INVALID_ARG.
  */
 int sgemm_set_3xtf32_kernel(int pair);
 

@@ -200,3 +200,10 @@ def test_shape_heuristic_takes_the_tile_orientation_that_pads_less(M, N, K, tile
     binding.set_variant(-1)
     name = binding.config_string(M, N, K)
     assert f"tile={tile}x64" in name and name in binding.variants()[:2]
+
+
+def test_3xtf32_kernel_choice_validates(lib):
+    lib.sgemm_set_3xtf32_kernel.argtypes = [ctypes.c_int]
+    for v in (-1, 0, 1, -1):
+        assert lib.sgemm_set_3xtf32_kernel(v) == 0
+    assert lib.sgemm_set_3xtf32_kernel(2) == 1 and lib.sgemm_set_3xtf32_kernel(-2) == 1

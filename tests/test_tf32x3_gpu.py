@@ -122,4 +122,4 @@ def test_cta_pair_kernel_matches_oracle(M, N, K):
         got = run3(A, B, C, -0.75, 1.0).cpu().numpy()
         assert_within_bound(got, ref, bound, f"pair {M}x{N}x{K}")
     finally:
-        binding.set_3xtf32_kernel(False)
+        binding.set_3xtf32_kernel(None)
