@@ -255,7 +255,10 @@ int sgemm_set_variant(int id);
  * cta_group::2).  The automatic choice compares the two kernels' waves over the
  * SMs and takes the pair on a tie (its main loop is faster).  Both meet the
  * same tolerance; results may differ in the last bits.  Applies to later calls
- * in this process; anything outside -1..1 gives SGEMM_ERR_INVALID_ARG.
+ * in this process; anything outside -1..1 gives SGEMM_ERR_INVALID_ARG.  The
+ * pair kernel is launched as 2-CTA clusters of one CTA per SM: where the
+ * device cannot hold them (a partitioned GPU), its launch fails with
+ * SGEMM_ERR_CUDA and 0 selects the single-CTA kernel.
  */
 int sgemm_set_3xtf32_kernel(int pair);
 
