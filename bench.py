@@ -14,7 +14,7 @@ so no flush is needed between steps.
            2 FLOP x 2070 MHz), timed with CUDA events on its own stream
   cpu_baseline  the CPU oracle on this host's cores on a bounded sample of rows
 
-`--impl reference` times the CPU oracle (the only reference this build has) on
+`--impl reference` times the CPU oracle (the only reference implementation) on
 a bounded sample of the same workload per step and prints the same line with
 "impl": "reference".
 """
