@@ -1,5 +1,7 @@
 """Host-only parts of bench.py: the oracle table (the CPU oracle timed with all
-host cores and with one) on the smallest workload.  No GPU is involved."""
+host cores and with one) on the smallest workload, the reference arm's line,
+the clock summary from nvidia-smi samples, the whole-job rate, and the DRAM,
+traffic and peak figures of the roofline object.  No GPU is involved."""
 import argparse
 import json
 
@@ -60,3 +62,90 @@ def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
     assert line["e2e"] == {"value": line["value"], "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["config"]["workload"] == "sgemm_256"
+
+
+def _smi_row(ts, sm, sm_max, power, reasons=()):
+    """One line of `nvidia-smi --format=csv,noheader,nounits` for ClockSampler.FIELDS."""
+    flags = ["Active" if n in reasons else "Not Active"
+             for n in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")]
+    stamp = ts.strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    return ", ".join([stamp, "0", str(sm), str(sm_max), f"{power:.2f}", "0x0000000000000000"] + flags)
+
+
+def test_clock_summary_keeps_only_the_samples_inside_the_timed_windows(tmp_path):
+    """Median SM clock, maximum clock, throttle reasons and power come from the
+    samples inside the marked windows; the idle samples around them (low clock,
+    a power-cap flag) do not count, and malformed lines are skipped."""
+    import datetime
+    import bench
+    t = datetime.datetime(2026, 1, 5, 12, 0, 0)
+    sec = datetime.timedelta(seconds=1)
+    lines = [_smi_row(t, 345, 2070, 90.0, {"sw_power_cap"}),            # before the window
+             "garbage line",
+             _smi_row(t + 2 * sec, 1965, 2070, 1100.0),
+             _smi_row(t + 3 * sec, 1980, 2070, 1150.0, {"sw_power_cap"}),
+             _smi_row(t + 4 * sec, 1950, 2070, 1120.0),
+             _smi_row(t + 9 * sec, 400, 2070, 95.0, {"hw_slowdown"})]        # after it
+    path = tmp_path / "clocks.csv"
+    path.write_text("\n".join(lines) + "\n")
+    s = bench.ClockSampler(0)
+    s.path = str(path)
+    s.mark((t + 2 * sec).timestamp(), (t + 4 * sec).timestamp())
+    out = s.summary()
+    assert out["samples"] == 3 and out["in_window"] is True
+    assert out["sm_mhz"] == 1965 and out["sm_max_mhz"] == 2070
+    assert out["reasons"] == ["sw_power_cap"]
+    assert out["power_w_median"] == pytest.approx(1120.0)
+    # a window with no samples falls back to every sample, and says so
+    late = (t + 60 * sec).timestamp()
+    out = s.summary(windows=[(late, late + 1)])
+    assert out["samples"] == 5 and out["in_window"] is False
+    assert out["reasons"] == ["hw_slowdown", "sw_power_cap"]
+
+
+def test_clock_summary_without_samples(tmp_path):
+    import bench
+    s = bench.ClockSampler(0)
+    s.path = str(tmp_path / "missing.csv")
+    out = s.summary()
+    assert out["sm_mhz"] is None and out["samples"] == 0
+    assert out["reasons"] == ["no nvidia-smi samples"]
+
+
+def test_whole_job_rate_counts_every_replica_at_the_slowest_rank_time():
+    import bench
+    flops = 2.0 * 8192 ** 3
+    assert bench.aggregate_gflops(flops, 15.0, 1) == pytest.approx(flops / 0.015 / 1e9)
+    assert bench.aggregate_gflops(flops, 15.0, 4) == pytest.approx(4 * flops / 0.015 / 1e9)
+
+
+def test_l2_note_says_whether_the_inputs_outgrow_l2():
+    import bench
+    from dense_fp32_gemm_02_gb300.workloads import WORKLOADS
+    assert bench.l2_note(WORKLOADS["sgemm_8192_ab"]).startswith("inputs larger than L2 (A, B, C 805 MB")
+    assert "not larger than" in bench.l2_note(WORKLOADS["sgemm_256"])
+
+
+def test_traffic_figure_counts_only_for_the_kernel_sources_it_was_taken_on(monkeypatch):
+    import bench
+    with open(bench.PROFILE_SUMMARY) as f:
+        stored = json.load(f)["sgemm_8192_ab"]
+    monkeypatch.setattr(bench, "kernel_revision", lambda: stored["kernel_revision"])
+    assert bench.load_traffic("sgemm_8192_ab") == stored["dram_bytes_per_launch"]
+    assert bench.load_traffic("no_such_workload") is None
+    monkeypatch.setattr(bench, "kernel_revision", lambda: "0" * 16)
+    assert bench.load_traffic("sgemm_8192_ab") is None
+
+
+def test_tensor_peak_comes_from_the_measured_bf16_figure_else_the_fallback(monkeypatch, tmp_path):
+    import bench
+    monkeypatch.setattr(bench, "PEAKS_FILE", str(tmp_path / "absent.json"))
+    peak, src = bench.tensor_peak_tf32()
+    assert peak == pytest.approx(bench.BF16_FALLBACK_TFLOPS * bench.TF32_PER_BF16)
+    assert src.startswith("fallback")
+    p = tmp_path / "peaks.json"
+    p.write_text(json.dumps({"bf16_tflops": 2000.0, "hbm_gbs": 7000.0}))
+    monkeypatch.setattr(bench, "PEAKS_FILE", str(p))
+    peak, src = bench.tensor_peak_tf32()
+    assert peak == pytest.approx(2000.0 * bench.TF32_PER_BF16) and src.startswith("measured")
+    assert bench.dram_use(7.0e9, 10.0)["dram_frac"] == pytest.approx(0.1)
