@@ -128,15 +128,22 @@ def _shapes(A, B, C):
     return M, N, K
 
 
+def _cuda_f32(*named):
+    """TypeError unless every (name, tensor) pair holds a CUDA float32 tensor;
+    ValueError unless they all sit on one device."""
+    import torch
+    for name, t in named:
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA float32 tensor")
+    if len({t.device for _, t in named}) > 1:
+        raise ValueError(", ".join(n for n, _ in named) + " must be on one device")
+
+
 def sgemm_into(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
     """C <- alpha*A@B + beta*C on CUDA float32 tensors (row-major, any row pitch).
     Asynchronous on `stream` (default: torch's current stream of C's device)."""
     import torch
-    for name, t in (("A", A), ("B", B), ("C", C)):
-        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda:
-            raise TypeError(f"{name} must be a CUDA float32 tensor")
-    if not (A.device == B.device == C.device):
-        raise ValueError("A, B and C must be on the same device")
+    _cuda_f32(("A", A), ("B", B), ("C", C))
     M, N, K = _shapes(A, B, C)
     with torch.cuda.device(C.device):
         st = lib.sgemm(M, N, K, float(alpha), A.data_ptr(), _ld(A, K), B.data_ptr(), _ld(B, N),
@@ -165,11 +172,9 @@ def sgemm_ex_into(A, B, C, alpha: float = 1.0, beta: float = 0.0, bias=None, act
     batch or 2-D (shared by all batches); bias is None, a length-N vector
     (shared) or (batch, N).  Asynchronous on `stream`."""
     import torch
-    for name, t in (("A", A), ("B", B), ("C", C)) + ((("bias", bias),) if bias is not None else ()):
-        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda:
-            raise TypeError(f"{name} must be a CUDA float32 tensor")
-        if t.device != C.device:
-            raise ValueError(f"{name} must be on C's device")
+    _cuda_f32(("A", A), ("B", B), ("C", C), *((("bias", bias),) if bias is not None else ()))
+    if act not in ACTIVATIONS:
+        raise ValueError(f"act must be one of {sorted(ACTIVATIONS)}, got {act!r}")
     C0, batch, sc = _batched(C, "C")
     A0, ba, sa = _batched(A, "A")
     B0, bb, sb = _batched(B, "B")
@@ -200,11 +205,7 @@ def sgemm_3xtf32_into(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=Non
     """Like sgemm_into(), on the tensor cores by the 3xTF32 split (same FP32
     tolerance, not bitwise equal to sgemm_into)."""
     import torch
-    for name, t in (("A", A), ("B", B), ("C", C)):
-        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda:
-            raise TypeError(f"{name} must be a CUDA float32 tensor")
-    if not (A.device == B.device == C.device):
-        raise ValueError("A, B and C must be on the same device")
+    _cuda_f32(("A", A), ("B", B), ("C", C))
     M, N, K = _shapes(A, B, C)
     with torch.cuda.device(C.device):
         st = lib.sgemm_3xtf32(M, N, K, float(alpha), A.data_ptr(), _ld(A, K), B.data_ptr(),
@@ -218,11 +219,7 @@ def sgemm_noalloc_into(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=No
     """Like sgemm_into(), through the entry point that allocates no device
     memory (its workspace is a fixed array; see include/sgemm.h)."""
     import torch
-    for name, t in (("A", A), ("B", B), ("C", C)):
-        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda:
-            raise TypeError(f"{name} must be a CUDA float32 tensor")
-    if not (A.device == B.device == C.device):
-        raise ValueError("A, B and C must be on the same device")
+    _cuda_f32(("A", A), ("B", B), ("C", C))
     M, N, K = _shapes(A, B, C)
     with torch.cuda.device(C.device):
         st = lib.sgemm_noalloc(M, N, K, float(alpha), A.data_ptr(), _ld(A, K), B.data_ptr(),
