@@ -255,6 +255,8 @@ def test_every_kernel_variant_matches_oracle(M, N, K):
     (512, 256, 64),       # 4 tiles, 2 slabs each: every tile split in two pieces
     (300, 4000, 16),      # one slab per tile: stream-K pieces are whole tiles, some CTAs idle
     (2048, 2048, 1056),   # 128 tiles, 33 slabs: the whole problem is stream-K
+    (200, 100, 16384),    # one tile of 256 slabs: its pieces sit on every CTA
+    (3, 5, 100003),       # one tile of 1563 slabs; rows of A, B and C not 16-byte aligned
 ])
 def test_stream_k_split_matches_oracle(M, N, K, kernel):
     """Shapes whose leftover tiles are split along k between CTAs: integer
