@@ -207,3 +207,38 @@ def test_3xtf32_kernel_choice_validates(lib):
     for v in (-1, 0, 1, -1):
         assert lib.sgemm_set_3xtf32_kernel(v) == 0
     assert lib.sgemm_set_3xtf32_kernel(2) == 1 and lib.sgemm_set_3xtf32_kernel(-2) == 1
+
+
+def test_every_declared_function_is_documented_in_the_header():
+    """Each declaration sits directly under a comment, or directly under
+    another declaration of the same documented group (e.g. the variant
+    functions), and the header names the page that defines the operation."""
+    for h in HEADERS:
+        text = open(h).read()
+        comments = [(m.start(), m.end()) for m in re.finditer(r"/\*.*?\*/", text, flags=re.S)]
+
+        def outside_comments(pos):
+            return all(not (a <= pos < b) for a, b in comments)
+
+        documented = {}
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(sgemm\w*)\s*\(", text, flags=re.M):
+            if not outside_comments(m.start()):
+                continue
+            start = m.start()
+            last_comment_end = max((b for a, b in comments if b <= start), default=-1)
+            semis = [i for i in range(start) if text[i] == ";" and outside_comments(i)]
+            last_semi = semis[-1] if semis else -1
+            if last_comment_end > last_semi and not text[last_comment_end:start].strip():
+                documented[m.group(1)] = True
+            elif (last_semi > last_comment_end and not text[last_semi + 1:start].strip()
+                  and text[last_semi + 1:start].count("\n") <= 1):   # the next line: same group
+                documented[m.group(1)] = documented.get(prev, False)
+            else:
+                documented[m.group(1)] = False
+            prev = m.group(1)
+        missing = sorted(n for n, ok in documented.items() if not ok)
+        assert not missing, f"{os.path.basename(h)}: no comment above {missing}"
+    header = open(os.path.join(ROOT, "include", "sgemm.h")).read()
+    flat = re.sub(r"\s*\n\s*\*?\s*", " ", header)     # comment lines joined
+    assert "How to implement matrix multiplication efficiently" in flat
+    assert "Naive GEMM and prerequisites" in flat
