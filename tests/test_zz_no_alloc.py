@@ -4,9 +4,10 @@ Some callers cannot allocate device memory: a host framework that has handed
 all of it to its own allocator, or a latency-critical path where an allocation
 could synchronise the device or fail.  sgemm_noalloc serves them by keeping its
 workspace in a fixed device array.  These tests call it through the C ABI and
-compare it with the ordinary sgemm() entry point, on two calls in a row (the
-second call finds the first call's data still in the shared array), and check
-that a problem too large for the array is refused without any work.
+compare it with the CPU oracle and with the ordinary sgemm() entry point, on two
+calls in a row (the second call finds the first call's data still in the shared
+array), and check that a problem too large for the array is refused without any
+work.
 
 This file is named so that pytest collects it last.
 """
@@ -46,10 +47,13 @@ def test_no_alloc_matches_sgemm_on_two_calls_in_a_row():
         binding.sgemm_noalloc_into(dA, dB, c_new, alpha, beta)      # no-allocation entry point
         torch.cuda.synchronize()
         assert binding.device_status() == binding.SGEMM_OK
-        _, bound = oracle.sgemm(A, B, C, alpha, beta)
+        ref, bound = oracle.sgemm(A, B, C, alpha, beta)
         got_ref = c_ref.cpu().numpy()
         got_new = c_new.cpu().numpy()
         assert np.isfinite(got_new).all()
+        # against the CPU oracle first, so a fault both entry points share
+        # (packing, tensor maps, edge tiles) cannot hide
+        assert_within_bound(got_new, ref, bound, f"no-alloc vs oracle {M}x{N}x{K}")
         assert_within_bound(got_new, got_ref, bound, f"no-alloc vs sgemm {M}x{N}x{K}")
 
 
