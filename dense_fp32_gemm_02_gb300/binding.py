@@ -67,6 +67,8 @@ lib.sgemm_set_variant.argtypes = [_i]
 lib.sgemm_set_variant.restype = _i
 lib.sgemm_set_3xtf32_kernel.argtypes = [_i]
 lib.sgemm_set_3xtf32_kernel.restype = _i
+lib.sgemm_debug_drop_release.argtypes = [_i]
+lib.sgemm_debug_drop_release.restype = _i
 
 SGEMM_OK = 0
 SGEMM_ERR_INVALID_ARG = 1
@@ -320,3 +322,10 @@ def set_3xtf32_kernel(pair) -> None:
     """3xTF32 main kernel for later calls: the CTA pair (True), the single-CTA
     kernel (False) or the automatic choice per shape (None, the default)."""
     check(lib.sgemm_set_3xtf32_kernel(-1 if pair is None else (1 if pair else 0)))
+
+
+def debug_drop_release(on: bool) -> None:
+    """Failure-detection test switch: while on, plain sgemm() calls run the
+    test build of the default kernel in which one release is left out, so a
+    bounded wait expires and the kernel's abort path runs (include/sgemm.h)."""
+    check(lib.sgemm_debug_drop_release(1 if on else 0))

@@ -1,4 +1,5 @@
-"""Build libsgemm.so in-tree with nvcc for sm_103a (no torch extension machinery).
+"""Build libsgemm.so in-tree with nvcc for sm_103a (no torch extension machinery):
+the translation units under csrc/ compile in parallel, then one link.
 
 ``python -m dense_fp32_gemm_02_gb300.build`` or ``build()`` from Python.
 The library is written to ``dense_fp32_gemm_02_gb300/_build/libsgemm.so``;
@@ -11,6 +12,7 @@ import os
 import shutil
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG_DIR)
@@ -20,11 +22,11 @@ LIB_PATH = os.path.join(BUILD_DIR, "libsgemm.so")
 HEADER = os.path.join(ROOT, "include", "sgemm.h")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = [
-    "-O3", "-lineinfo", "-std=c++17", "--shared",
+COMPILE_FLAGS = [
+    "-O3", "-lineinfo", "-std=c++17",
     "-Xcompiler", "-fPIC,-fvisibility=hidden",
-    "-cudart", "static",
 ]
+LINK_FLAGS = ["--shared", "-cudart", "static"]
 
 
 def _nvcc() -> str:
@@ -36,9 +38,13 @@ def _nvcc() -> str:
     return cand
 
 
+def units():
+    """The library's translation units (compiled separately, in parallel)."""
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+
+
 def sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh"))
-                  + [HEADER])
+    return sorted(units() + glob.glob(os.path.join(CSRC, "*.cuh")) + [HEADER])
 
 
 def is_stale() -> bool:
@@ -49,17 +55,36 @@ def is_stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
+    """Compile every translation unit to an object at the same time, then link
+    libsgemm.so (no relocatable device code: each unit's kernels are complete)."""
     if not force and not is_stale():
         return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [_nvcc(), *ARCH_FLAGS, *NVCC_FLAGS, *(extra_flags or []),
-           os.path.join(CSRC, "sgemm.cu"), "-o", tmp]
+    obj_dir = os.path.join(BUILD_DIR, f"obj{os.getpid()}")
+    os.makedirs(obj_dir, exist_ok=True)
+    nvcc = _nvcc()
+    flags = [*ARCH_FLAGS, *COMPILE_FLAGS, *(extra_flags or [])]
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-        print(" ".join(cmd), file=sys.stderr)
-    subprocess.run(cmd, check=True)
+        flags.insert(0, "-Xptxas=-v")
+
+    def compile_unit(src):
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *flags, "-c", src, "-o", obj]
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.stdout or r.stderr:
+            sys.stderr.write(r.stdout + r.stderr)
+        if r.returncode != 0:
+            raise subprocess.CalledProcessError(r.returncode, cmd)
+        return obj
+
+    srcs = units()
+    with ThreadPoolExecutor(max_workers=len(srcs)) as ex:
+        objs = list(ex.map(compile_unit, srcs))
+    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.run([nvcc, *ARCH_FLAGS, *LINK_FLAGS, *objs, "-o", tmp], check=True)
     os.replace(tmp, LIB_PATH)
+    shutil.rmtree(obj_dir, ignore_errors=True)
     return LIB_PATH
 
 

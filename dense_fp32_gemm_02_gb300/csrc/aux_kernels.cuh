@@ -1,0 +1,220 @@
+// aux_kernels.cuh -- the kernels around the FP32 SGEMM's main kernel: the
+// A-transpose pre-pass (single and batched), the B re-pitch copy, the
+// alpha == 0 / K == 0 scaling kernel, the deferred beta * C_in addition of the
+// host-buffer pipeline, the direct kernel for small problems and the
+// bounded-wait self test.  Non-template kernels: included by sgemm.cu only.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kernels.cuh"
+
+namespace sg {
+
+// ------------------------------------------------------------------ pre-pass
+// At[k][m] = A[m][k] for one plane.  64x64 tiles through shared memory, 256
+// threads: each thread has 16 independent loads in flight (coalesced along k)
+// and then 16 stores (coalesced along m).
+__device__ __forceinline__ void transpose_plane(const float *__restrict__ A, long long lda, int M,
+                                                int K, float *__restrict__ At, long long ldat) {
+    __shared__ float tile[64][65];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;   // 8 warps
+    for (long long m0 = (long long)blockIdx.y * 64; m0 < M; m0 += (long long)gridDim.y * 64) {
+        for (long long k0 = (long long)blockIdx.x * 64; k0 < K; k0 += (long long)gridDim.x * 64) {
+            float v[16];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const long long m = m0 + w * 8 + r;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const long long k = k0 + lane + 32 * h;
+                    v[2 * r + h] = (m < M && k < K) ? __ldcs(A + m * lda + k) : 0.0f;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) tile[w * 8 + r][lane + 32 * h] = v[2 * r + h];
+            __syncthreads();
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const long long k = k0 + w * 8 + r;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const long long m = m0 + lane + 32 * h;
+                    if (k < K && m < M) At[k * ldat + m] = tile[lane + 32 * h][w * 8 + r];
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// The pre-pass of a single GEMM.  Block (0,0) also zeroes `zero_count` ints at
+// `zero` (the stream-K tile counters of the GEMM that follows on the stream).
+__global__ void __launch_bounds__(256)
+    pack_a_transpose_kernel(const float *__restrict__ A, long long lda, int M, int K,
+                            float *__restrict__ At, long long ldat, int *zero, int zero_count) {
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        for (int i = threadIdx.x; i < zero_count; i += blockDim.x) zero[i] = 0;
+    transpose_plane(A, lda, M, K, At, ldat);
+}
+
+// The batched pre-pass: plane z = blockIdx.z transposes A + z * stride_a into
+// At + z * at_plane (the host launches at most 65535 planes per call).  Held to
+// 64 registers (four blocks per SM).
+__global__ void __launch_bounds__(256, 4)
+    pack_a_transpose_batched_kernel(const float *__restrict__ A, long long lda, long long stride_a,
+                                    int M, int K, float *__restrict__ At, long long ldat,
+                                    long long at_plane, int *zero, int zero_count) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+        for (int i = threadIdx.x; i < zero_count; i += blockDim.x) zero[i] = 0;
+    transpose_plane(A + (long long)blockIdx.z * stride_a, lda, M, K,
+                    At + (long long)blockIdx.z * at_plane, ldat);
+}
+
+// Bp[k][n] = B[k][n] with a 16-byte row pitch (ldbp % 4 == 0) and a 16-byte
+// plane pitch for the TMA, plane by plane (batch z of B at B + z * stride_b).
+// One block row per k (grid-stride), threads along n.
+__global__ void __launch_bounds__(256)
+    pack_b_copy_kernel(const float *__restrict__ B, long long ldb, long long stride_b, int K,
+                       int N, float *__restrict__ Bp, long long ldbp, long long bp_plane,
+                       int planes) {
+    for (int z = blockIdx.z; z < planes; z += gridDim.z) {
+        for (long long k = blockIdx.y; k < K; k += gridDim.y) {
+            const float *src = B + (long long)z * stride_b + k * ldb;
+            float *dst = Bp + (long long)z * bp_plane + k * ldbp;
+            for (long long n = (long long)blockIdx.x * blockDim.x + threadIdx.x; n < N;
+                 n += (long long)gridDim.x * blockDim.x)
+                dst[n] = __ldcs(src + n);
+        }
+    }
+}
+
+// C = act(beta * C + bias) on each batch's M x N block (C not read when
+// beta == 0): the alpha == 0 / K == 0 case, where A and B are not read.
+__global__ void __launch_bounds__(256)
+    scale_c_kernel(float *C, long long ldc, long long stride_c, int M, int N, int batch,
+                   float beta, const float *bias, long long stride_bias, int act) {
+    const long long per = (long long)M * N, total = per * batch;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long b = idx / per, rem = idx - b * per;
+        const long long i = rem / N, j = rem - i * N;
+        float *c = C + b * stride_c + i * ldc + j;
+        float v = (beta == 0.0f) ? 0.0f : beta * *c;
+        if (bias) v += bias[b * stride_bias + j];
+        *c = activate(v, act);
+    }
+}
+
+// C += beta * X over an M x N block (row pitches ldc and ldx): the deferred
+// beta * C_in term of the host-buffer pipeline's first row block.
+__global__ void __launch_bounds__(256)
+    add_scaled_kernel(float *C, long long ldc, const float *__restrict__ X, long long ldx, int M,
+                      int N, float beta) {
+    const long long total = (long long)M * N;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long i = idx / N, j = idx - i * N;
+        float *c = C + i * ldc + j;
+        *c = fmaf(beta, X[i * ldx + j], *c);
+    }
+}
+
+// ------------------------------------------------------------------ small problems
+// C = alpha*A*B + beta*C for problems too small to fill the GPU with the
+// persistent kernel's 256x128 tiles: one CTA per TS x TS output tile (TS 64,
+// or 32 when 64x64 tiles would leave most SMs idle), reading A and B directly
+// (any leading dimension or alignment), no pre-pass, no workspace, one launch.
+// 256 threads in a 16x16 grid, (TS/16) x (TS/16) outputs each; k in steps of
+// 32 through shared memory (A stored transposed, as in the pages' tiled
+// kernel), the next step's operands loaded into registers meanwhile.  Every output sums its k terms in ascending order with fused
+// multiply-adds, so the result is deterministic.
+constexpr int SMALL_BK = 32;
+template <int TS>
+__global__ void __launch_bounds__(256)
+    sgemm_small_kernel(int M, int N, int K, float alpha, const float *__restrict__ A,
+                       long long lda, const float *__restrict__ B, long long ldb, float beta,
+                       float *__restrict__ C, long long ldc) {
+    constexpr int T = TS / 16;                       // outputs per thread along each side
+    constexpr int LOADS = TS * SMALL_BK / 256;       // elements of A (and of B) per thread
+    __shared__ float As[SMALL_BK][TS + 4];           // As[k][m]
+    __shared__ float Bs[SMALL_BK][TS + 4];           // Bs[k][n]
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const long long row0 = (long long)blockIdx.y * TS, col0 = (long long)blockIdx.x * TS;
+    float acc[T][T];
+#pragma unroll
+    for (int i = 0; i < T; ++i)
+#pragma unroll
+        for (int j = 0; j < T; ++j) acc[i][j] = 0.0f;
+    // TS x BK of A and BK x TS of B per step: consecutive threads along k for A
+    // and along n for B (coalesced); the next step's values are loaded into
+    // registers while the current step's FMAs run
+    float ra[LOADS], rb[LOADS];
+    auto fetch = [&](int k0) {
+#pragma unroll
+        for (int q = 0; q < LOADS; ++q) {
+            const int e = threadIdx.x + q * 256;
+            const long long gr = row0 + e / SMALL_BK;
+            const int gk = k0 + e % SMALL_BK;
+            ra[q] = (gr < M && gk < K) ? A[gr * lda + gk] : 0.0f;
+            const long long gc = col0 + e % TS;
+            const int gkb = k0 + e / TS;
+            rb[q] = (gkb < K && gc < N) ? B[(long long)gkb * ldb + gc] : 0.0f;
+        }
+    };
+    fetch(0);
+    for (int k0 = 0; k0 < K; k0 += SMALL_BK) {
+#pragma unroll
+        for (int q = 0; q < LOADS; ++q) {
+            const int e = threadIdx.x + q * 256;
+            As[e % SMALL_BK][e / SMALL_BK] = ra[q];
+            Bs[e / TS][e % TS] = rb[q];
+        }
+        __syncthreads();
+        if (k0 + SMALL_BK < K) fetch(k0 + SMALL_BK);
+#pragma unroll
+        for (int kk = 0; kk < SMALL_BK; ++kk) {
+            float a[T], b[T];
+#pragma unroll
+            for (int i = 0; i < T; ++i) a[i] = As[kk][ty * T + i];
+#pragma unroll
+            for (int j = 0; j < T; ++j) b[j] = Bs[kk][tx * T + j];
+#pragma unroll
+            for (int i = 0; i < T; ++i)
+#pragma unroll
+                for (int j = 0; j < T; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < T; ++i) {
+        const long long r = row0 + ty * T + i;
+        if (r >= M) continue;
+#pragma unroll
+        for (int j = 0; j < T; ++j) {
+            const long long c = col0 + tx * T + j;
+            if (c >= N) continue;
+            float *out = C + r * ldc + c;
+            *out = (beta != 0.0f) ? fmaf(alpha, acc[i][j], beta * *out) : alpha * acc[i][j];
+        }
+    }
+}
+
+// One thread waits on a barrier that nothing completes; the bounded wait must
+// expire, record ERR_SELFTEST and return.
+__global__ void wait_timeout_selftest_kernel(unsigned long long timeout_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (!mbar_wait(&bar, 0u, timeout_ns)) atomicOr(&g_error_word, ERR_SELFTEST);
+    }
+}
+
+}  // namespace sg

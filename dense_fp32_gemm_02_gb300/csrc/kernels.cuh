@@ -1,6 +1,7 @@
-// kernels.cuh -- device code of the FP32 SGEMM: the A-transpose pre-pass, the
-// B re-pitch copy, the persistent TMA-fed FFMA main kernel, the alpha==0 / K==0
-// scaling kernel and the bounded-wait self test.
+// kernels.cuh -- device code of the FP32 SGEMM's persistent TMA-fed FFMA main
+// kernel (tile configurations, work split, epilogue, the kernel template).
+// The pre-pass, scaling, small-problem and self-test kernels are in
+// aux_kernels.cuh.
 //
 // Design, in terms of the techniques the SGEMM pages describe:
 //  * block tiling with a K slab staged in shared memory per step and an
@@ -42,7 +43,18 @@ enum : unsigned {
 };
 
 // One word per device; every kernel of this library reports expiries here.
-__device__ unsigned int g_error_word = 0;
+// Internal linkage: each translation unit that includes this file has its own
+// copy, and the host reads and clears all of them (variant.cuh).
+static __device__ unsigned int g_error_word = 0;
+
+// Limit of the waits that, after an abort, let this CTA's own copies (and
+// tensor-core operations) in flight complete before it exits.  Those always
+// complete, so the wait only has to outlast them: it takes its own generous
+// limit rather than the caller's, which may be short and has just expired.
+constexpr unsigned long long kDrainLimitNs = 1000000000ull;   // 1 s
+__device__ __forceinline__ unsigned long long drain_limit_ns(unsigned long long timeout_ns) {
+    return timeout_ns > kDrainLimitNs ? timeout_ns : kDrainLimitNs;
+}
 
 // ------------------------------------------------------------------ configuration
 // Micro-kernel of the consumer warps.
@@ -97,6 +109,9 @@ struct TileConfig {
     // keeps its main loop under the register cap.
     static constexpr bool EX = false;
     static constexpr bool BATCH = false;
+    // Failure-detection test instantiation only (AbortTestConfig): the CTA
+    // slab at which consumer warp 0 of CTA 0 leaves out its release; -1 here.
+    static constexpr int DROP_RELEASE_SLAB = -1;
 
     static_assert(WM * WARPS_M == BM && WN * WARPS_N == BN, "warp grid must cover the tile");
     static_assert(TM % 4 == 0 && TN % 4 == 0, "thread tile is made of 4x4 sub-tiles");
@@ -126,6 +141,17 @@ template <class Base>
 struct FusedConfig : Base {
     static constexpr bool EX = true;
     static constexpr bool BATCH = false;
+};
+
+// The same tile configuration with one release left out on purpose: consumer
+// warp 0 of CTA 0 does not arrive on the empty barrier of the CTA's slab 2.
+// The issuer's wait for that stage then expires with no copy into it in
+// flight, and the kernel's abort path runs: error word, abort flag, no C
+// written for the CTA's tiles, copies drained.  Launched only by the library's
+// failure-detection test switch (sgemm_debug_drop_release); never by default.
+template <class Base>
+struct AbortTestConfig : Base {
+    static constexpr int DROP_RELEASE_SLAB = 2;
 };
 
 struct MainParams {
@@ -580,6 +606,19 @@ __device__ __forceinline__ void sum_pieces_row(float (&row)[Cfg::TN], const floa
     }
 }
 
+// After an abort: this CTA's partial sums may be wrong, so every stream-K
+// tile it holds a piece of is made impossible to complete: its counter is
+// raised far past any piece count, and no CTA ever sums the tile's pieces
+// into C.  Called by each thread that records an expiry, before it reaches the
+// consumer barrier at which thread 0 counts the CTA's piece, so it comes first
+// in the counter's order.  Several calls only add more.
+__device__ __forceinline__ void block_stream_k_tiles(const MainParams &p, int k_tiles) {
+    const long long x0 = sk_start(blockIdx.x, p.sk_slabs, gridDim.x);
+    const long long x1 = sk_start(blockIdx.x + 1, p.sk_slabs, gridDim.x);
+    for (long long t = x0 / k_tiles; x0 < x1 && t <= (x1 - 1) / k_tiles; ++t)
+        atomicAdd(&p.counters[t], 1 << 24);
+}
+
 // ------------------------------------------------------------------ main kernel
 // Shared-memory ring and flags of one CTA, addressed by 32-bit shared-window
 // addresses that all derive from one base register:
@@ -653,6 +692,7 @@ __device__ __forceinline__ bool issue_one(State &st, const Ring<Cfg> &ring,
     // first one and counts as complete
     if (!mbar_wait_at(ring.empty(s), st.phase ^ 1u, p.timeout_ns)) {
         atomicOr(&g_error_word, ERR_EMPTY_WAIT);
+        block_stream_k_tiles(p, k_tiles);
         ring.set_abort();
         return false;
     }
@@ -677,15 +717,17 @@ __device__ __forceinline__ bool issue_one(State &st, const Ring<Cfg> &ring,
     return true;
 }
 
-// After an abort: wait (bounded) for the last copies issued, so none is still
-// writing shared memory when the CTA exits.
+// After an abort: wait for the last copies issued, so none is still writing
+// shared memory when the CTA exits.  The wait is bounded by drain_limit_ns, not
+// by the caller's limit that has just expired.
 template <class Cfg>
 __device__ __forceinline__ void drain_copies(const Ring<Cfg> &ring, long long issued,
                                              const MainParams &p) {
     const long long first = issued > Cfg::STAGES ? issued - Cfg::STAGES : 0;
     for (long long q = first; q < issued; ++q) {
         const int s = int(q % Cfg::STAGES);
-        if (!mbar_wait_at(ring.full(s), uint32_t((q / Cfg::STAGES) & 1), p.timeout_ns)) {
+        if (!mbar_wait_at(ring.full(s), uint32_t((q / Cfg::STAGES) & 1),
+                          drain_limit_ns(p.timeout_ns))) {
             atomicOr(&g_error_word, ERR_DRAIN_WAIT);
             break;
         }
@@ -735,6 +777,7 @@ __device__ __forceinline__ void consumer_loop(const Ring<Cfg> &ring, const MainP
 
     int stage = 0;          // stage of the next slab to consume
     uint32_t phase = 0;     // parity of that stage's full barrier
+    int q = 0;              // slabs consumed so far (AbortTestConfig only)
     for (int si = 0;; ++si) {
         int nslabs, slot;
         {
@@ -774,7 +817,10 @@ __device__ __forceinline__ void consumer_loop(const Ring<Cfg> &ring, const MainP
                 bool ok = mbar_wait_at(ring.full(s), phase, p.timeout_ns);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) {
-                    if (lane == 0) atomicOr(&g_error_word, ERR_FULL_WAIT);
+                    if (lane == 0) {
+                        atomicOr(&g_error_word, ERR_FULL_WAIT);
+                        block_stream_k_tiles(p, k_tiles);
+                    }
                     ring.set_abort();
                 }
             }
@@ -793,9 +839,15 @@ __device__ __forceinline__ void consumer_loop(const Ring<Cfg> &ring, const MainP
             }
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive_at(ring.empty(s));
+                if constexpr (Cfg::DROP_RELEASE_SLAB >= 0) {
+                    if (!(blockIdx.x == 0 && cw == 0 && q == Cfg::DROP_RELEASE_SLAB))
+                        mbar_arrive_at(ring.empty(s));
+                } else {
+                    mbar_arrive_at(ring.empty(s));
+                }
                 after_release(s);
             }
+            ++q;
             if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1u;
@@ -873,9 +925,11 @@ __device__ __forceinline__ void consumer_loop(const Ring<Cfg> &ring, const MainP
 // waits for another.
 //
 // Expiry of a bounded wait sets a CTA-wide abort flag: from then on no thread
-// waits again and nothing more is written to C; every consumer still passes
-// the consumer barriers, and at the end the issuing thread waits (bounded) for
-// the copies it issued.
+// waits again and nothing more is written to C; the stream-K tiles the CTA
+// holds pieces of are made impossible to complete (block_stream_k_tiles), so
+// they stay unwritten too; every
+// consumer still passes the consumer barriers, and at the end the issuing
+// thread waits for the copies it issued (drain_limit_ns).
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     sgemm_tma_ffma_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -973,211 +1027,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // every warp is past its last issue before the copies are counted
         __syncthreads();
         if (threadIdx.x == 0 && ring.aborted()) drain_copies<Cfg>(ring, ist.issued, p);
-    }
-}
-
-// ------------------------------------------------------------------ pre-pass
-// At[k][m] = A[m][k] for one plane.  64x64 tiles through shared memory, 256
-// threads: each thread has 16 independent loads in flight (coalesced along k)
-// and then 16 stores (coalesced along m).
-__device__ __forceinline__ void transpose_plane(const float *__restrict__ A, long long lda, int M,
-                                                int K, float *__restrict__ At, long long ldat) {
-    __shared__ float tile[64][65];
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;   // 8 warps
-    for (long long m0 = (long long)blockIdx.y * 64; m0 < M; m0 += (long long)gridDim.y * 64) {
-        for (long long k0 = (long long)blockIdx.x * 64; k0 < K; k0 += (long long)gridDim.x * 64) {
-            float v[16];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const long long m = m0 + w * 8 + r;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const long long k = k0 + lane + 32 * h;
-                    v[2 * r + h] = (m < M && k < K) ? __ldcs(A + m * lda + k) : 0.0f;
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 8; ++r)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) tile[w * 8 + r][lane + 32 * h] = v[2 * r + h];
-            __syncthreads();
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const long long k = k0 + w * 8 + r;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const long long m = m0 + lane + 32 * h;
-                    if (k < K && m < M) At[k * ldat + m] = tile[lane + 32 * h][w * 8 + r];
-                }
-            }
-            __syncthreads();
-        }
-    }
-}
-
-// The pre-pass of a single GEMM.  Block (0,0) also zeroes `zero_count` ints at
-// `zero` (the stream-K tile counters of the GEMM that follows on the stream).
-__global__ void __launch_bounds__(256)
-    pack_a_transpose_kernel(const float *__restrict__ A, long long lda, int M, int K,
-                            float *__restrict__ At, long long ldat, int *zero, int zero_count) {
-    if (blockIdx.x == 0 && blockIdx.y == 0)
-        for (int i = threadIdx.x; i < zero_count; i += blockDim.x) zero[i] = 0;
-    transpose_plane(A, lda, M, K, At, ldat);
-}
-
-// The batched pre-pass: plane z = blockIdx.z transposes A + z * stride_a into
-// At + z * at_plane (the host launches at most 65535 planes per call).  Held to
-// 64 registers (four blocks per SM).
-__global__ void __launch_bounds__(256, 4)
-    pack_a_transpose_batched_kernel(const float *__restrict__ A, long long lda, long long stride_a,
-                                    int M, int K, float *__restrict__ At, long long ldat,
-                                    long long at_plane, int *zero, int zero_count) {
-    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
-        for (int i = threadIdx.x; i < zero_count; i += blockDim.x) zero[i] = 0;
-    transpose_plane(A + (long long)blockIdx.z * stride_a, lda, M, K,
-                    At + (long long)blockIdx.z * at_plane, ldat);
-}
-
-// Bp[k][n] = B[k][n] with a 16-byte row pitch (ldbp % 4 == 0) and a 16-byte
-// plane pitch for the TMA, plane by plane (batch z of B at B + z * stride_b).
-// One block row per k (grid-stride), threads along n.
-__global__ void __launch_bounds__(256)
-    pack_b_copy_kernel(const float *__restrict__ B, long long ldb, long long stride_b, int K,
-                       int N, float *__restrict__ Bp, long long ldbp, long long bp_plane,
-                       int planes) {
-    for (int z = blockIdx.z; z < planes; z += gridDim.z) {
-        for (long long k = blockIdx.y; k < K; k += gridDim.y) {
-            const float *src = B + (long long)z * stride_b + k * ldb;
-            float *dst = Bp + (long long)z * bp_plane + k * ldbp;
-            for (long long n = (long long)blockIdx.x * blockDim.x + threadIdx.x; n < N;
-                 n += (long long)gridDim.x * blockDim.x)
-                dst[n] = __ldcs(src + n);
-        }
-    }
-}
-
-// C = act(beta * C + bias) on each batch's M x N block (C not read when
-// beta == 0): the alpha == 0 / K == 0 case, where A and B are not read.
-__global__ void __launch_bounds__(256)
-    scale_c_kernel(float *C, long long ldc, long long stride_c, int M, int N, int batch,
-                   float beta, const float *bias, long long stride_bias, int act) {
-    const long long per = (long long)M * N, total = per * batch;
-    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (long long)gridDim.x * blockDim.x) {
-        const long long b = idx / per, rem = idx - b * per;
-        const long long i = rem / N, j = rem - i * N;
-        float *c = C + b * stride_c + i * ldc + j;
-        float v = (beta == 0.0f) ? 0.0f : beta * *c;
-        if (bias) v += bias[b * stride_bias + j];
-        *c = activate(v, act);
-    }
-}
-
-// C += beta * X over an M x N block (row pitches ldc and ldx): the deferred
-// beta * C_in term of the host-buffer pipeline's first row block.
-__global__ void __launch_bounds__(256)
-    add_scaled_kernel(float *C, long long ldc, const float *__restrict__ X, long long ldx, int M,
-                      int N, float beta) {
-    const long long total = (long long)M * N;
-    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (long long)gridDim.x * blockDim.x) {
-        const long long i = idx / N, j = idx - i * N;
-        float *c = C + i * ldc + j;
-        *c = fmaf(beta, X[i * ldx + j], *c);
-    }
-}
-
-// ------------------------------------------------------------------ small problems
-// C = alpha*A*B + beta*C for problems too small to fill the GPU with the
-// persistent kernel's 256x128 tiles: one CTA per TS x TS output tile (TS 64,
-// or 32 when 64x64 tiles would leave most SMs idle), reading A and B directly
-// (any leading dimension or alignment), no pre-pass, no workspace, one launch.
-// 256 threads in a 16x16 grid, (TS/16) x (TS/16) outputs each; k in steps of
-// 32 through shared memory (A stored transposed, as in the pages' tiled
-// kernel), the next step's operands loaded into registers meanwhile.  Every output sums its k terms in ascending order with fused
-// multiply-adds, so the result is deterministic.
-constexpr int SMALL_BK = 32;
-template <int TS>
-__global__ void __launch_bounds__(256)
-    sgemm_small_kernel(int M, int N, int K, float alpha, const float *__restrict__ A,
-                       long long lda, const float *__restrict__ B, long long ldb, float beta,
-                       float *__restrict__ C, long long ldc) {
-    constexpr int T = TS / 16;                       // outputs per thread along each side
-    constexpr int LOADS = TS * SMALL_BK / 256;       // elements of A (and of B) per thread
-    __shared__ float As[SMALL_BK][TS + 4];           // As[k][m]
-    __shared__ float Bs[SMALL_BK][TS + 4];           // Bs[k][n]
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    const long long row0 = (long long)blockIdx.y * TS, col0 = (long long)blockIdx.x * TS;
-    float acc[T][T];
-#pragma unroll
-    for (int i = 0; i < T; ++i)
-#pragma unroll
-        for (int j = 0; j < T; ++j) acc[i][j] = 0.0f;
-    // TS x BK of A and BK x TS of B per step: consecutive threads along k for A
-    // and along n for B (coalesced); the next step's values are loaded into
-    // registers while the current step's FMAs run
-    float ra[LOADS], rb[LOADS];
-    auto fetch = [&](int k0) {
-#pragma unroll
-        for (int q = 0; q < LOADS; ++q) {
-            const int e = threadIdx.x + q * 256;
-            const long long gr = row0 + e / SMALL_BK;
-            const int gk = k0 + e % SMALL_BK;
-            ra[q] = (gr < M && gk < K) ? A[gr * lda + gk] : 0.0f;
-            const long long gc = col0 + e % TS;
-            const int gkb = k0 + e / TS;
-            rb[q] = (gkb < K && gc < N) ? B[(long long)gkb * ldb + gc] : 0.0f;
-        }
-    };
-    fetch(0);
-    for (int k0 = 0; k0 < K; k0 += SMALL_BK) {
-#pragma unroll
-        for (int q = 0; q < LOADS; ++q) {
-            const int e = threadIdx.x + q * 256;
-            As[e % SMALL_BK][e / SMALL_BK] = ra[q];
-            Bs[e / TS][e % TS] = rb[q];
-        }
-        __syncthreads();
-        if (k0 + SMALL_BK < K) fetch(k0 + SMALL_BK);
-#pragma unroll
-        for (int kk = 0; kk < SMALL_BK; ++kk) {
-            float a[T], b[T];
-#pragma unroll
-            for (int i = 0; i < T; ++i) a[i] = As[kk][ty * T + i];
-#pragma unroll
-            for (int j = 0; j < T; ++j) b[j] = Bs[kk][tx * T + j];
-#pragma unroll
-            for (int i = 0; i < T; ++i)
-#pragma unroll
-                for (int j = 0; j < T; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-        }
-        __syncthreads();
-    }
-#pragma unroll
-    for (int i = 0; i < T; ++i) {
-        const long long r = row0 + ty * T + i;
-        if (r >= M) continue;
-#pragma unroll
-        for (int j = 0; j < T; ++j) {
-            const long long c = col0 + tx * T + j;
-            if (c >= N) continue;
-            float *out = C + r * ldc + c;
-            *out = (beta != 0.0f) ? fmaf(alpha, acc[i][j], beta * *out) : alpha * acc[i][j];
-        }
-    }
-}
-
-// One thread waits on a barrier that nothing completes; the bounded wait must
-// expire, record ERR_SELFTEST and return.
-__global__ void wait_timeout_selftest_kernel(unsigned long long timeout_ns) {
-    __shared__ uint64_t bar;
-    if (threadIdx.x == 0) {
-        mbar_init(&bar, 1);
-        fence_barrier_init();
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        if (!mbar_wait(&bar, 0u, timeout_ns)) atomicOr(&g_error_word, ERR_SELFTEST);
     }
 }
 

@@ -23,9 +23,11 @@
 #include <vector>
 
 #include "../../include/sgemm.h"
+#include "aux_kernels.cuh"
 #include "kernels.cuh"
 #include "tf32x3.cuh"
 #include "tf32x3_pair.cuh"
+#include "variant.cuh"
 
 #define SGEMM_API extern "C" __attribute__((visibility("default")))
 
@@ -40,38 +42,9 @@ thread_local int t_last_cuda_error = 0;
 // Every variant is the same persistent TMA/FFMA kernel with other tile sizes or
 // micro-kernel.  The default is chosen per shape by pick_variant(); a specific
 // one can be forced for tile-configuration sweeps with sgemm_set_variant().
-struct Variant {
-    const char *name;
-    int bm, bn, bk;
-    bool stream_k;
-    int group_m;
-    cudaError_t (*set_attr)();
-    void (*launch)(int grid, cudaStream_t s, const CUtensorMap &a, const CUtensorMap &b,
-                   const sg::MainParams &p, const sg::ExParams &x);
-};
-
-template <class Cfg>
-cudaError_t set_attr_t() {
-    return cudaFuncSetAttribute(sg::sgemm_tma_ffma_kernel<Cfg>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::SMEM_BYTES));
-}
-
-template <class Cfg>
-void launch_t(int grid, cudaStream_t s, const CUtensorMap &a, const CUtensorMap &b,
-              const sg::MainParams &p, const sg::ExParams &x) {
-    sg::sgemm_tma_ffma_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, s>>>(a, b, p, x);
-}
-
-template <class Cfg>
-constexpr Variant make_variant(const char *name, bool stream_k, int group_m = 8) {
-    return Variant{name, Cfg::BM, Cfg::BN, Cfg::BK, stream_k, group_m, &set_attr_t<Cfg>,
-                   &launch_t<Cfg>};
-}
-
-using sg::MICRO_FFMA;
+using sgv::make_variant;
+using sgv::Variant;
 using sg::MICRO_FFMA2;
-using sg::ISSUE_THREAD0;
-using sg::ISSUE_PRODUCER_WG;
 using sg::ISSUE_LAST_WARP;
 // Variant 0 is the default: it was the fastest or within 1% of the fastest on
 // every measured workload.  Its 16 consumer warps (four per scheduler) hide
@@ -79,51 +52,53 @@ using sg::ISSUE_LAST_WARP;
 // producer warpgroup (16 consumer warps at 128 registers fill the register
 // file, so the two do not fit together), and the warp that releases a stage
 // last refills it, so no warp waits for the others.  Variant 1, the same tile
-// turned, takes the shapes that it pads less (pick_variant).  The others stay
-// for sweeps and as evidence for the design choices (issuer, tile shape,
-// stream-K, warp specialisation, packed FP32x2 FMA, thread-tile size, k depth
-// of a stage).
-const Variant kVariants[] = {
-    make_variant<sg::TileConfig<256, 128, 64, 2, 8, 2, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>>(
+// turned, takes the shapes that it pads less (pick_variant).  Variant 3 is
+// variant 0's kernel with whole tiles only (no stream-K tail).  The others,
+// compiled in sweep_variants_a.cu and sweep_variants_b.cu, stay for sweeps
+// and as evidence for the design choices (issuer, tile shape, warp
+// specialisation, packed FP32x2 FMA, thread-tile size, k depth of a stage).
+using DefaultTile = sg::TileConfig<256, 128, 64, 2, 8, 2, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>;
+const Variant kMainVariants[] = {
+    make_variant<DefaultTile>(
         "ffma2 tile=256x128x64 stages=2 warps=16 issuer=last_warp thread=8x8 stream_k", true),
     make_variant<sg::TileConfig<128, 256, 64, 2, 4, 4, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>>(
         "ffma2 tile=128x256x64 stages=2 warps=16 issuer=last_warp thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<256, 128, 64, 2, 8, 2, 8, 8, MICRO_FFMA2, ISSUE_THREAD0>>(
-        "ffma2 tile=256x128x64 stages=2 warps=16 issuer=thread0 thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<256, 128, 64, 2, 8, 2, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>>(
+    make_variant<DefaultTile>(
         "ffma2 tile=256x128x64 stages=2 warps=16 issuer=last_warp thread=8x8 no_stream_k", false),
-    make_variant<sg::TileConfig<256, 128, 48, 3, 8, 2, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>>(
-        "ffma2 tile=256x128x48 stages=3 warps=16 issuer=last_warp thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<128, 192, 64, 2, 4, 3, 8, 8, MICRO_FFMA2, ISSUE_PRODUCER_WG>>(
-        "ffma2 tile=128x192x64 stages=2 warps=12+producer_wg thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<128, 192, 64, 2, 4, 3, 8, 8, MICRO_FFMA2, ISSUE_THREAD0>>(
-        "ffma2 tile=128x192x64 stages=2 warps=12 issuer=thread0 thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<128, 192, 64, 2, 4, 3, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>>(
-        "ffma2 tile=128x192x64 stages=2 warps=12 issuer=last_warp thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<192, 128, 64, 2, 6, 2, 8, 8, MICRO_FFMA2, ISSUE_PRODUCER_WG>>(
-        "ffma2 tile=192x128x64 stages=2 warps=12+producer_wg thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<128, 128, 48, 4, 4, 2, 8, 8, MICRO_FFMA2, ISSUE_PRODUCER_WG>>(
-        "ffma2 tile=128x128x48 stages=4 warps=8+producer_wg thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<128, 128, 48, 4, 4, 2, 8, 8, MICRO_FFMA, ISSUE_PRODUCER_WG>>(
-        "ffma tile=128x128x48 stages=4 warps=8+producer_wg thread=8x8 stream_k", true),
-    make_variant<sg::TileConfig<256, 128, 32, 4, 4, 2, 16, 8, MICRO_FFMA2, ISSUE_PRODUCER_WG>>(
-        "ffma2 tile=256x128x32 stages=4 warps=8+producer_wg thread=16x8 stream_k", true),
 };
-constexpr int kNumVariants = int(sizeof(kVariants) / sizeof(kVariants[0]));
+
+// All variants in variant-number order: 0, 1 and 3 from this file, 2 and 4-6
+// from sweep_variants_a.cu, 7-11 from sweep_variants_b.cu.
+struct VariantIndex {
+    const Variant *v[32];
+    int n = 0;
+    VariantIndex() {
+        const sgv::VariantTable a = sgv::sweep_variants_a(), b = sgv::sweep_variants_b();
+        v[n++] = &kMainVariants[0];
+        v[n++] = &kMainVariants[1];
+        v[n++] = &a.entries[0];
+        v[n++] = &kMainVariants[2];
+        for (int i = 1; i < a.count; ++i) v[n++] = &a.entries[i];
+        for (int i = 0; i < b.count; ++i) v[n++] = &b.entries[i];
+    }
+};
+const VariantIndex &variant_index() {
+    static const VariantIndex idx;
+    return idx;
+}
+int variant_count() { return variant_index().n; }
+const Variant &variant_at(int id) { return *variant_index().v[id]; }
 
 // Batched calls run the default configuration compiled with the batch
 // coordinate (3-D tensor maps) and the fused epilogue; unbatched calls with a
 // bias or an activation run it with the fused epilogue alone (2-D maps), which
-// keeps the plain kernel's 123 registers (the batched one needs 128).
-const Variant kExVariant =
-    make_variant<sg::ExConfig<sg::TileConfig<256, 128, 64, 2, 8, 2, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>>>(
-        "ffma2 tile=256x128x64 stages=2 warps=16 issuer=last_warp thread=8x8 stream_k batched+epilogue",
-        true);
-const Variant kFusedVariant =
-    make_variant<sg::FusedConfig<sg::TileConfig<256, 128, 64, 2, 8, 2, 8, 8, MICRO_FFMA2, ISSUE_LAST_WARP>>>(
-        "ffma2 tile=256x128x64 stages=2 warps=16 issuer=last_warp thread=8x8 stream_k epilogue",
-        true);
+// keeps the plain kernel's 123 registers (the batched one needs 128).  Both,
+// and the failure-detection test kernel, are compiled in extra_variants.cu.
+const Variant &ex_variant() { return sgv::extra_variants().entries[sgv::EXTRA_BATCHED]; }
+const Variant &fused_variant() { return sgv::extra_variants().entries[sgv::EXTRA_FUSED]; }
+const Variant &abort_test_variant() { return sgv::extra_variants().entries[sgv::EXTRA_DROP_RELEASE]; }
 std::atomic<int> g_forced_variant{-1};
+std::atomic<int> g_drop_release{0};
 // 3xTF32 main kernel: -1 = chosen per shape (t3_use_pair), 0 = the single-CTA
 // kernel, 1 = the CTA pair
 std::atomic<int> g_t3_pair{-1};
@@ -139,9 +114,9 @@ long long padded_area(const Variant &v, int M, int N) {
 
 int pick_variant(int M, int N, int K) {
     const int forced = g_forced_variant.load();
-    if (forced >= 0 && forced < kNumVariants) return forced;
+    if (forced >= 0 && forced < variant_count()) return forced;
     (void)K;
-    return padded_area(kVariants[1], M, N) < padded_area(kVariants[0], M, N) ? 1 : 0;
+    return padded_area(variant_at(1), M, N) < padded_area(variant_at(0), M, N) ? 1 : 0;
 }
 
 struct DeviceState {
@@ -257,10 +232,11 @@ int device_state(DeviceState **out) {
             // keep up to 4 GiB of released workspace cached for reuse
             cuuint64_t keep = 4ull << 30;
             cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
-            for (const Variant &v : kVariants)
-                if ((e = v.set_attr()) != cudaSuccess) return cuda_fail(e);
-            if ((e = kExVariant.set_attr()) != cudaSuccess) return cuda_fail(e);
-            if ((e = kFusedVariant.set_attr()) != cudaSuccess) return cuda_fail(e);
+            for (int i = 0; i < variant_count(); ++i)
+                if ((e = variant_at(i).set_attr()) != cudaSuccess) return cuda_fail(e);
+            if ((e = ex_variant().set_attr()) != cudaSuccess) return cuda_fail(e);
+            if ((e = fused_variant().set_attr()) != cudaSuccess) return cuda_fail(e);
+            if ((e = abort_test_variant().set_attr()) != cudaSuccess) return cuda_fail(e);
             if ((e = cudaFuncSetAttribute(sg::t3::sgemm_3xtf32_pair_kernel,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           int(sg::t3::P_SMEM_BYTES))) != cudaSuccess)
@@ -423,9 +399,14 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
     const int M = g.M, N = g.N, K = g.K;
     const bool batched = g.batch > 1;
     const bool extended = batched || g.bias != nullptr || g.act != sg::ACT_NONE;
-    if (!extended && g_forced_variant.load() < 0 && small_problem(M, N, K, dev->sm_count))
+    const bool drop_test = !extended && g_drop_release.load() != 0;
+    if (!extended && !drop_test && g_forced_variant.load() < 0 &&
+        small_problem(M, N, K, dev->sm_count))
         return launch_small(g, stream, dev->sm_count);
-    const Variant &var = batched ? kExVariant : extended ? kFusedVariant : kVariants[pick_variant(M, N, K)];
+    const Variant &var = batched ? ex_variant()
+                         : extended ? fused_variant()
+                         : drop_test ? abort_test_variant()
+                                     : variant_at(pick_variant(M, N, K));
     // A and B enter as one plane per batch, or one plane for all batches when
     // their stride is 0
     const int a_planes = (g.batch > 1 && g.stride_a != 0) ? g.batch : 1;
@@ -918,14 +899,21 @@ int host_gemm(int M, int N, int K, float alpha, const float *A, int lda, const f
     return e == cudaSuccess ? SGEMM_OK : cuda_fail(e);
 }
 
+// Synchronises `stream`, then reads and clears the device error word of every
+// translation unit (each has its own copy, variant.cuh) on the current device.
 int read_and_clear_error_word(cudaStream_t stream) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e);
-    unsigned v = 0, zero = 0;
-    if ((e = cudaMemcpyFromSymbol(&v, sg::g_error_word, sizeof(v))) != cudaSuccess) return cuda_fail(e);
-    if (v && (e = cudaMemcpyToSymbol(sg::g_error_word, &zero, sizeof(zero))) != cudaSuccess)
-        return cuda_fail(e);
-    return v ? SGEMM_ERR_TIMEOUT : SGEMM_OK;
+    cudaError_t (*const units[])(unsigned *, bool) = {
+        &sgv::unit_error_word, sgv::extra_variants().error_word,
+        sgv::sweep_variants_a().error_word, sgv::sweep_variants_b().error_word};
+    unsigned any = 0;
+    for (auto word : units) {
+        unsigned v = 0;
+        if ((e = word(&v, true)) != cudaSuccess) return cuda_fail(e);
+        any |= v;
+    }
+    return any ? SGEMM_ERR_TIMEOUT : SGEMM_OK;
 }
 
 // ------------------------------------------------------------------ no-allocation path
@@ -972,9 +960,9 @@ int noalloc_state(NoAllocState **out) {
                     return cuda_fail(e != cudaSuccess ? e : cudaErrorNotSupported);
                 g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
             }
-            for (const Variant &v : kVariants)
-                if ((e = v.set_attr()) != cudaSuccess) return cuda_fail(e);
-            if ((e = kExVariant.set_attr()) != cudaSuccess) return cuda_fail(e);
+            for (int i = 0; i < variant_count(); ++i)
+                if ((e = variant_at(i).set_attr()) != cudaSuccess) return cuda_fail(e);
+            if ((e = ex_variant().set_attr()) != cudaSuccess) return cuda_fail(e);
             // In host code the array's name is only a host-side stand-in: the
             // kernels must be given its device address.
             void *ptr = nullptr;
@@ -1000,7 +988,7 @@ int sgemm_device_noalloc(int M, int N, int K, float alpha, const float *A, int l
     if (K == 0 || alpha == 0.0f) return launch_scale(stream, plain_call(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc),
                             dev->sm_count);
 
-    const Variant &var = kVariants[pick_variant(M, N, K)];
+    const Variant &var = variant_at(pick_variant(M, N, K));
     const long long ldat = round_up(M, 4);
     const bool b_direct = aligned16(B) && (ldb % 4 == 0);
     const long long ldbp = b_direct ? ldb : round_up(N, 4);
@@ -1039,7 +1027,7 @@ int sgemm_device_noalloc(int M, int N, int K, float alpha, const float *A, int l
     p.beta = beta;
     p.tiles_m = int((M + var.bm - 1) / var.bm);
     p.tiles_n = int((N + var.bn - 1) / var.bn);
-    p.group_m = 8;
+    p.group_m = var.group_m;
     p.c_vec4 = aligned16(C) ? 1 : 0;
     p.timeout_ns = g_timeout_ns.load();
     const long long tiles = (long long)p.tiles_m * p.tiles_n;
@@ -1171,19 +1159,25 @@ SGEMM_API int sgemm_profile_collect(double *main_ms, long long *main_launches, d
 SGEMM_API long long sgemm_kernel_launch_count(void) { return g_launches.load(); }
 
 SGEMM_API const char *sgemm_config_string(int M, int N, int K) {
-    return kVariants[pick_variant(M, N, K)].name;
+    return variant_at(pick_variant(M, N, K)).name;
 }
 
-SGEMM_API int sgemm_variant_count(void) { return kNumVariants; }
+SGEMM_API int sgemm_variant_count(void) { return variant_count(); }
 
 SGEMM_API const char *sgemm_variant_name(int id) {
-    if (id < 0 || id >= kNumVariants) return "";
-    return kVariants[id].name;
+    if (id < 0 || id >= variant_count()) return "";
+    return variant_at(id).name;
 }
 
 SGEMM_API int sgemm_set_variant(int id) {
-    if (id < -1 || id >= kNumVariants) return SGEMM_ERR_INVALID_ARG;
+    if (id < -1 || id >= variant_count()) return SGEMM_ERR_INVALID_ARG;
     g_forced_variant.store(id);
+    return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_debug_drop_release(int on) {
+    if (on != 0 && on != 1) return SGEMM_ERR_INVALID_ARG;
+    g_drop_release.store(on);
     return SGEMM_OK;
 }
 

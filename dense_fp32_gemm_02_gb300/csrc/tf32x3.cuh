@@ -276,7 +276,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             // after an abort: let the copies already issued land before exit
             if (*abort_flag) {
                 for (long long q = (issued > STAGES ? issued - STAGES : 0); q < issued; ++q)
-                    if (!mbar_wait(&full[q % STAGES], uint32_t((q / STAGES) & 1), p.timeout_ns)) {
+                    if (!mbar_wait(&full[q % STAGES], uint32_t((q / STAGES) & 1),
+                                   drain_limit_ns(p.timeout_ns))) {
                         atomicOr(&g_error_word, ERR_DRAIN_WAIT);
                         break;
                     }
@@ -334,7 +335,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!ok) {
                 // no MMA may still run when TMEM is freed
                 mma_commit(drain);
-                if (!mbar_wait(drain, 0u, p.timeout_ns)) atomicOr(&g_error_word, ERR_DRAIN_WAIT);
+                if (!mbar_wait(drain, 0u, drain_limit_ns(p.timeout_ns)))
+                    atomicOr(&g_error_word, ERR_DRAIN_WAIT);
             }
         }
     } else if (warp >= 4) {

@@ -112,6 +112,11 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
 __device__ __forceinline__ void st_cluster_flag(uint32_t addr, int v) {
     asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+__device__ __forceinline__ int ld_cluster_u32(uint32_t addr) {
+    int v;
+    asm volatile("ld.relaxed.cluster.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
 
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -195,6 +200,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     uint64_t *drain = acc_empty + 2;
     uint32_t *tmem_base = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base + 1);
+    volatile int *issued_slot = abort_flag + 1;   // stages this CTA's producer filled
 
     const uint32_t rank = cluster_rank();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -209,6 +215,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
+        *issued_slot = 0;
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc_pair(tmem_base, TMEM_COLS);
@@ -239,6 +246,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const uint32_t ring_s = smem_addr(ring);
             int stage = 0;
             uint32_t phase = 0;
+            int issued = 0;
             for (int j = 0; j < my_tiles && !*abort_flag; ++j) {
                 int tm, col0, ncols;
                 plan.item(p, j, tm, col0, ncols);
@@ -262,12 +270,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                                    brow);
                     tma_load_2d_pair(st + uint32_t(2 * P_A + P_B) * 4u, half ? &tmBl2 : &tmBl, fb,
                                    kb * BK, brow);
+                    ++issued;
                     if (++stage == P_STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
+            *issued_slot = issued;
         }
     } else if (warp == 1) {
         // ================================================================ MMA issuer (CTA 0)
@@ -321,7 +331,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             if (!ok) {
                 // no MMA may still run when either CTA frees its TMEM or exits
                 mma_commit_pair(drain);
-                if (!mbar_wait(drain, 0u, p.timeout_ns)) atomicOr(&g_error_word, ERR_DRAIN_WAIT);
+                if (!mbar_wait(drain, 0u, drain_limit_ns(p.timeout_ns)))
+                    atomicOr(&g_error_word, ERR_DRAIN_WAIT);
             }
         }
     } else if (warp >= 4) {
@@ -385,6 +396,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();   // CTA 0's MMAs and both CTAs' remote arrivals are done
+    // After an abort, copies of either producer may still be writing its CTA's
+    // ring, and they count on CTA 0's full barriers, which only CTA 0 can wait
+    // on.  Every abort was set in both CTAs before the barrier above, so both
+    // take this branch or neither.  CTA 0 completes the arrivals of stages
+    // that only one producer filled (the other, which never arrived, expects
+    // no bytes there), waits until the last P_STAGES fillings have landed, and
+    // the second cluster barrier keeps CTA 1 resident until then.
+    if (*abort_flag) {
+        if (rank == 0 && threadIdx.x == 0) {
+            const int mine = *issued_slot;
+            const int peer = ld_cluster_u32(map_to_rank(smem_addr((const void *)issued_slot), 1u));
+            const int lo = mine < peer ? mine : peer, hi = mine < peer ? peer : mine;
+            // a producer runs at most P_STAGES fillings ahead of the MMAs, which
+            // consume only stages both filled, so hi - lo <= P_STAGES
+            for (int q = lo; q < hi; ++q) mbar_arrive(&full[q % P_STAGES]);
+            for (int q = hi > P_STAGES ? hi - P_STAGES : 0; q < hi; ++q)
+                if (!mbar_wait_cluster(&full[q % P_STAGES], uint32_t((q / P_STAGES) & 1),
+                                       drain_limit_ns(p.timeout_ns))) {
+                    atomicOr(&g_error_word, ERR_DRAIN_WAIT);
+                    break;
+                }
+        }
+        cluster_sync_all();
+    }
     tc_fence_after();
     if (warp == 1) tmem_dealloc_pair(taddr, TMEM_COLS);
 }

@@ -216,6 +216,25 @@ int sgemm_set_wait_timeout_ns(unsigned long long ns);
 int sgemm_selftest_wait_timeout(unsigned long long ns, sgemm_stream_t stream);
 
 /*
+ * sgemm_debug_drop_release -- failure-detection test switch, off (0) by
+ * default.  With 1, later plain sgemm() calls (not sgemm_ex, sgemm_host,
+ * sgemm_noalloc or the 3xTF32 entry points) run a test build of the default
+ * persistent kernel, also for problems small enough for the direct kernel.  In
+ * it, consumer warp 0 of CTA 0 leaves out its release of the CTA's third
+ * k-slab, so the wait for that stage to be freed expires after the limit of
+ * sgemm_set_wait_timeout_ns (set a short one first: the call then takes about
+ * two limits) while no copy into it is in flight.  The kernel's own abort path
+ * runs: the expiry is recorded (sgemm_device_status returns SGEMM_ERR_TIMEOUT),
+ * CTA 0 writes nothing more to C, the output tiles it was computing (whole, or
+ * shared with other CTAs through stream-K pieces) stay unwritten, its copies
+ * in flight land before it exits, and every other tile is written as usual.
+ * CTA 0 must have at least five k-slabs of work for the expiry to happen.  No
+ * fault, trap or hang is involved; the context stays usable.  0 restores
+ * normal calls; anything but 0 or 1 gives SGEMM_ERR_INVALID_ARG.
+ */
+int sgemm_debug_drop_release(int on);
+
+/*
  * Kernel timing for benchmarks.  sgemm_profile_enable(1) makes later sgemm()
  * calls record CUDA events on their stream around their main GEMM kernel and
  * around their packing kernels.  sgemm_profile_collect() synchronises those

@@ -127,6 +127,11 @@ def test_variant_selection_validates(lib):
     assert lib.sgemm_set_variant(n - 1) == 0 and lib.sgemm_set_variant(-1) == 0
 
 
+def test_drop_release_switch_validates(lib):
+    assert lib.sgemm_debug_drop_release(2) == 1 and lib.sgemm_debug_drop_release(-1) == 1
+    assert lib.sgemm_debug_drop_release(1) == 0 and lib.sgemm_debug_drop_release(0) == 0
+
+
 def test_timeout_setter_validates(lib):
     lib.sgemm_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
     assert lib.sgemm_set_wait_timeout_ns(10) == 1
