@@ -40,6 +40,10 @@ PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "traffic.json")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 # nominal dense TF32 / BF16 tensor throughput of GB300 (1.1 / 2.25 PFLOP/s)
 TF32_PER_BF16 = 1.1 / 2.25
+# The TF32 MMA rate of one SM as a stand-alone probe measured it on GB300: one
+# tcgen05.mma kind::tf32 of M 128, N 256, K 8 every 128 cycles = 2048 MAC =
+# 4096 FLOP per clock per SM (profiles/sgemm_3xtf32_8192.md).
+TF32_MMA_FLOP_PER_SM_PER_CLK = 4096
 BF16_FALLBACK_TFLOPS = 1900.0
 HBM_FALLBACK_GBS = 6800.0
 
@@ -389,6 +393,23 @@ def tensor_peak_tf32():
     return bf16 * TF32_PER_BF16, src
 
 
+def probed_mma_fields(achieved_tflops, sms, sm_mhz=None):
+    """The 3xTF32 main kernel against the MMA unit's probed per-clock rate: at
+    the 2070 MHz maximum SM clock and, when known, at the clock measured during
+    its timed region.  The derived `peak` (bf16 burst x nominal ratio) sits
+    below the unit's rate, so `frac` there can read above 1; these cannot."""
+    peak = sms * TF32_MMA_FLOP_PER_SM_PER_CLK * SM_MAX_MHZ_FALLBACK * 1e6 / 1e12
+    out = {"probed_mma_peak": round(peak, 3),
+           "probed_mma_source": f"{sms} SMs x {TF32_MMA_FLOP_PER_SM_PER_CLK} TF32 FLOP/clk "
+                                f"(probed: one M128 N256 K8 MMA per 128 cycles) x 2070 MHz",
+           "frac_of_probed_mma": round(achieved_tflops / peak, 4) if achieved_tflops else None,
+           "frac_of_probed_mma_at_measured_clock": None}
+    if achieved_tflops and sm_mhz:
+        at = sms * TF32_MMA_FLOP_PER_SM_PER_CLK * sm_mhz * 1e6 / 1e12
+        out["frac_of_probed_mma_at_measured_clock"] = round(achieved_tflops / at, 4)
+    return out
+
+
 def dram_use(traffic, ms):
     """{dram_gbs, dram_frac}: one launch's DRAM bytes (the ncu figure) over its
     CUDA-event duration, and that rate against the measured copy bandwidth;
@@ -584,6 +605,8 @@ def run_ours(args):
         tf32x3["clocks"] = {"sm_mhz": tclk.get("sm_mhz"), "sm_max_mhz": tclk.get("sm_max_mhz"),
                             "reasons": tclk.get("reasons"), "samples": tclk.get("samples"),
                             "power_w_median": tclk.get("power_w_median")}
+        tf32x3["roofline"].update(probed_mma_fields(tf32x3["roofline"]["achieved"], sms,
+                                                    tclk.get("sm_mhz")))
 
     # ---- roofline of the main kernel
     main_ms = prof["main_ms"] / args.steps   # every compute launch of a step
@@ -621,6 +644,7 @@ def run_ours(args):
             "frac": round(mma_tflops / tpeak, 4) if mma_tflops else None,
             "traffic": load_traffic(w.name + ":tf32x3"),
             **dram_use(load_traffic(w.name + ":tf32x3"), main_ms), "peak_source": tsrc,
+            **probed_mma_fields(mma_tflops, sms, clk.get("sm_mhz")),
             "main_kernel_ms": round(main_ms, 4), "split_kernels_ms": round(pack_ms, 4),
             "algorithmic_flops_per_launch": 3.0 * w.flops,
         }

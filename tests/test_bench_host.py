@@ -143,3 +143,14 @@ def test_tensor_peak_comes_from_the_measured_bf16_figure_else_the_fallback(monke
     peak, src = bench.tensor_peak_tf32()
     assert peak == pytest.approx(2000.0 * bench.TF32_PER_BF16) and src.startswith("measured")
     assert bench.dram_use(7.0e9, 10.0)["dram_frac"] == pytest.approx(0.1)
+
+
+def test_probed_mma_fraction_uses_the_unit_rate_at_max_and_measured_clock():
+    import bench
+    # 152 SMs x 4096 TF32 FLOP/clk x 2070 MHz = 1288.8 TFLOP/s
+    f = bench.probed_mma_fields(1071.0, 152, 1960.0)
+    assert abs(f["probed_mma_peak"] - 152 * 4096 * 2070e6 / 1e12) < 1e-3
+    assert abs(f["frac_of_probed_mma"] - 1071.0 / 1288.8) < 1e-3
+    assert abs(f["frac_of_probed_mma_at_measured_clock"] - 1071.0 / (152 * 4096 * 1960e6 / 1e12)) < 1e-3
+    assert bench.probed_mma_fields(None, 152)["frac_of_probed_mma"] is None
+    assert bench.probed_mma_fields(1071.0, 152)["frac_of_probed_mma_at_measured_clock"] is None
