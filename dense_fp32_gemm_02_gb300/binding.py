@@ -10,17 +10,20 @@ from __future__ import annotations
 import ctypes
 import os
 
-from .build import LIB_PATH
+from .build import LIB_DEBUG_BOUNDS_PATH, LIB_PATH
 
-library_path = LIB_PATH
+# SGEMM_LIBRARY=debug_bounds loads the range-checked test build instead of the
+# library (a test switch; the library is always one of this package's builds)
+library_path = LIB_DEBUG_BOUNDS_PATH if os.environ.get("SGEMM_LIBRARY") == "debug_bounds" \
+    else LIB_PATH
 
-if not os.path.exists(LIB_PATH):
+if not os.path.exists(library_path):
     raise ImportError(
-        f"libsgemm.so is not built at {LIB_PATH}; run "
+        f"{os.path.basename(library_path)} is not built at {library_path}; run "
         "`python -c 'import __graft_entry__ as g; g.build()'` or "
         "`python -m dense_fp32_gemm_02_gb300.build`")
 
-lib = ctypes.CDLL(LIB_PATH)
+lib = ctypes.CDLL(library_path)
 
 _i, _f, _p = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
 _ull, _ll, _d = ctypes.c_ulonglong, ctypes.c_longlong, ctypes.c_double
@@ -69,6 +72,8 @@ lib.sgemm_set_3xtf32_kernel.argtypes = [_i]
 lib.sgemm_set_3xtf32_kernel.restype = _i
 lib.sgemm_debug_drop_release.argtypes = [_i]
 lib.sgemm_debug_drop_release.restype = _i
+lib.sgemm_debug_bounds_checks.argtypes = []
+lib.sgemm_debug_bounds_checks.restype = _i
 
 SGEMM_OK = 0
 SGEMM_ERR_INVALID_ARG = 1
@@ -77,6 +82,7 @@ SGEMM_ERR_CUDA = 3
 SGEMM_ERR_TIMEOUT = 4
 SGEMM_ERR_ALLOC = 5
 SGEMM_ERR_TOO_LARGE = 6
+SGEMM_ERR_BOUNDS = 7
 
 
 class SgemmError(RuntimeError):

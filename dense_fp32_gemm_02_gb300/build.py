@@ -19,6 +19,8 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libsgemm.so")
+# the range-checked build (-DSGEMM_DEBUG_BOUNDS): a test library, never the default
+LIB_DEBUG_BOUNDS_PATH = os.path.join(BUILD_DIR, "libsgemm_debug_bounds.so")
 HEADER = os.path.join(ROOT, "include", "sgemm.h")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -47,22 +49,27 @@ def sources():
     return sorted(units() + glob.glob(os.path.join(CSRC, "*.cuh")) + [HEADER])
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def is_stale(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return any(os.path.getmtime(s) > t for s in sources())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=None,
+          debug_bounds: bool = False) -> str:
     """Compile every translation unit to an object at the same time, then link
-    libsgemm.so (no relocatable device code: each unit's kernels are complete)."""
-    if not force and not is_stale():
-        return LIB_PATH
-    obj_dir = os.path.join(BUILD_DIR, f"obj{os.getpid()}")
+    libsgemm.so (no relocatable device code: each unit's kernels are complete).
+    debug_bounds=True builds the range-checked test library instead
+    (libsgemm_debug_bounds.so, -DSGEMM_DEBUG_BOUNDS)."""
+    lib_path = LIB_DEBUG_BOUNDS_PATH if debug_bounds else LIB_PATH
+    if not force and not is_stale(lib_path):
+        return lib_path
+    obj_dir = os.path.join(BUILD_DIR, f"obj{'_db' if debug_bounds else ''}{os.getpid()}")
     os.makedirs(obj_dir, exist_ok=True)
     nvcc = _nvcc()
-    flags = [*ARCH_FLAGS, *COMPILE_FLAGS, *(extra_flags or [])]
+    flags = [*ARCH_FLAGS, *COMPILE_FLAGS, *(extra_flags or []),
+             *(["-DSGEMM_DEBUG_BOUNDS"] if debug_bounds else [])]
     if verbose:
         flags.insert(0, "-Xptxas=-v")
 
@@ -81,11 +88,11 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     srcs = units()
     with ThreadPoolExecutor(max_workers=len(srcs)) as ex:
         objs = list(ex.map(compile_unit, srcs))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     subprocess.run([nvcc, *ARCH_FLAGS, *LINK_FLAGS, *objs, "-o", tmp], check=True)
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, lib_path)
     shutil.rmtree(obj_dir, ignore_errors=True)
-    return LIB_PATH
+    return lib_path
 
 
 if __name__ == "__main__":

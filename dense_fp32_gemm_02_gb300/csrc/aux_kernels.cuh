@@ -13,42 +13,50 @@
 namespace sg {
 
 // ------------------------------------------------------------------ pre-pass
-// At[k][m] = A[m][k] for one plane.  64x64 tiles through shared memory, 256
-// threads: each thread has 16 independent loads in flight (coalesced along k)
-// and then 16 stores (coalesced along m).
+// At[k][m] = A[m][k] for the 64x64 tile at (m0, k0), through shared memory,
+// 256 threads: each thread has 16 independent loads in flight (coalesced
+// along k) and then 16 stores (coalesced along m).
+__device__ __forceinline__ void transpose_tile(const float *__restrict__ A, long long lda, int M,
+                                               int K, float *__restrict__ At, long long ldat,
+                                               long long m0, long long k0,
+                                               float (&tile)[64][65]) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;   // 8 warps
+    float v[16];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const long long m = m0 + w * 8 + r;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const long long k = k0 + lane + 32 * h;
+            v[2 * r + h] = (m < M && k < K) ? __ldcs(A + m * lda + k) : 0.0f;
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) tile[w * 8 + r][lane + 32 * h] = v[2 * r + h];
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const long long k = k0 + w * 8 + r;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const long long m = m0 + lane + 32 * h;
+            if (k < K && m < M && SG_IN_RANGE(m < ldat))
+                At[k * ldat + m] = tile[lane + 32 * h][w * 8 + r];
+        }
+    }
+    __syncthreads();
+}
+
+// At[k][m] = A[m][k] for one plane: the block grid (x along k, y along m)
+// walks its 64x64 tiles.
 __device__ __forceinline__ void transpose_plane(const float *__restrict__ A, long long lda, int M,
                                                 int K, float *__restrict__ At, long long ldat) {
     __shared__ float tile[64][65];
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;   // 8 warps
-    for (long long m0 = (long long)blockIdx.y * 64; m0 < M; m0 += (long long)gridDim.y * 64) {
-        for (long long k0 = (long long)blockIdx.x * 64; k0 < K; k0 += (long long)gridDim.x * 64) {
-            float v[16];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const long long m = m0 + w * 8 + r;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const long long k = k0 + lane + 32 * h;
-                    v[2 * r + h] = (m < M && k < K) ? __ldcs(A + m * lda + k) : 0.0f;
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 8; ++r)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) tile[w * 8 + r][lane + 32 * h] = v[2 * r + h];
-            __syncthreads();
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const long long k = k0 + w * 8 + r;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const long long m = m0 + lane + 32 * h;
-                    if (k < K && m < M) At[k * ldat + m] = tile[lane + 32 * h][w * 8 + r];
-                }
-            }
-            __syncthreads();
-        }
-    }
+    for (long long m0 = (long long)blockIdx.y * 64; m0 < M; m0 += (long long)gridDim.y * 64)
+        for (long long k0 = (long long)blockIdx.x * 64; k0 < K; k0 += (long long)gridDim.x * 64)
+            transpose_tile(A, lda, M, K, At, ldat, m0, k0, tile);
 }
 
 // The pre-pass of a single GEMM.  Block (0,0) also zeroes `zero_count` ints at
@@ -87,8 +95,42 @@ __global__ void __launch_bounds__(256)
             float *dst = Bp + (long long)z * bp_plane + k * ldbp;
             for (long long n = (long long)blockIdx.x * blockDim.x + threadIdx.x; n < N;
                  n += (long long)gridDim.x * blockDim.x)
-                dst[n] = __ldcs(src + n);
+                if (SG_IN_RANGE(n < ldbp)) dst[n] = __ldcs(src + n);
         }
+    }
+}
+
+// The pre-pass of one GEMM whose B must be re-pitched, in one launch: blocks
+// [0, a_blocks) walk the 64x64 tiles of the A transpose, the others walk
+// strips of 16 rows x 256 columns of the B copy (a thread copies one column
+// of a strip: 16 loads in flight, coalesced along n; the rows of B need not
+// be 16-byte aligned, those of Bp are).  Block 0 also zeroes `zero_count`
+// ints at `zero` (the stream-K tile counters of the GEMM that follows).
+__global__ void __launch_bounds__(256)
+    pack_ab_kernel(const float *__restrict__ A, long long lda, int M, int K,
+                   float *__restrict__ At, long long ldat, const float *__restrict__ B,
+                   long long ldb, int N, float *__restrict__ Bp, long long ldbp, int a_blocks,
+                   int *zero, int zero_count) {
+    __shared__ float tile[64][65];
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < zero_count; i += blockDim.x) zero[i] = 0;
+    if (int(blockIdx.x) < a_blocks) {
+        const long long kt = (K + 63) / 64, tiles = kt * ((M + 63) / 64);
+        for (long long t = blockIdx.x; t < tiles; t += a_blocks)
+            transpose_tile(A, lda, M, K, At, ldat, (t / kt) * 64, (t % kt) * 64, tile);
+        return;
+    }
+    const long long nt = (N + 255) / 256, strips = nt * ((K + 15) / 16);
+    const long long b_blocks = gridDim.x - a_blocks;
+    for (long long t = blockIdx.x - a_blocks; t < strips; t += b_blocks) {
+        const long long k0 = (t / nt) * 16, n = (t % nt) * 256 + threadIdx.x;
+        if (n >= N) continue;
+        float v[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) v[r] = (k0 + r < K) ? __ldcs(B + (k0 + r) * ldb + n) : 0.0f;
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            if (k0 + r < K && SG_IN_RANGE(n < ldbp)) Bp[(k0 + r) * ldbp + n] = v[r];
     }
 }
 

@@ -40,12 +40,28 @@ enum : unsigned {
     ERR_EMPTY_WAIT = 2u,   // producer gave up waiting for a free stage
     ERR_DRAIN_WAIT = 4u,   // copies still in flight after an abort
     ERR_SELFTEST = 8u,     // the bounded-wait self test expired (expected)
+    ERR_BOUNDS = 16u,      // range-checked build: an index was out of range
 };
 
 // One word per device; every kernel of this library reports expiries here.
 // Internal linkage: each translation unit that includes this file has its own
 // copy, and the host reads and clears all of them (variant.cuh).
 static __device__ unsigned int g_error_word = 0;
+
+// Range checks of the range-checked build (compiled with -DSGEMM_DEBUG_BOUNDS,
+// the stand-in for a memory checker): SG_IN_RANGE(cond) is true when cond
+// holds; otherwise it records ERR_BOUNDS in the device error word and is
+// false, and the caller skips the access.  In the normal build it is `true`
+// and the checks cost nothing.
+#ifdef SGEMM_DEBUG_BOUNDS
+__device__ __forceinline__ bool sg_in_range(bool ok) {
+    if (!ok) atomicOr(&g_error_word, ERR_BOUNDS);
+    return ok;
+}
+#define SG_IN_RANGE(cond) ::sg::sg_in_range(bool(cond))
+#else
+#define SG_IN_RANGE(cond) true
+#endif
 
 // Limit of the waits that, after an abort, let this CTA's own copies (and
 // tensor-core operations) in flight complete before it exits.  Those always
@@ -101,8 +117,22 @@ struct TileConfig {
     static constexpr int A_STAGE = BK * BM;   // floats: K-rows of the transposed A tile
     static constexpr int B_STAGE = BK * BN;   // floats: K-rows of the B tile
     static constexpr uint32_t STAGE_BYTES = uint32_t(A_STAGE + B_STAGE) * 4u;
-    static constexpr size_t SMEM_BYTES =
+    static constexpr size_t RING_SMEM_BYTES =
         size_t(STAGES) * STAGE_BYTES + 2 * STAGES * sizeof(uint64_t) + 16 + 1024;
+    // Epilogue of C rows (StagedEpilogueConfig): direct 128-bit accesses from
+    // the registers (false), or every row through a staging area in shared
+    // memory, per consumer warp the four rows of WN columns it writes in one
+    // epilogue round (true).
+    static constexpr bool STAGED_EPI = false;
+    // A staged row is WN floats plus 16 of padding: the eight lanes of a
+    // quarter-warp write two rows in one 128-bit store, and the padding puts
+    // the second row 16 banks after the first, so they do not conflict.
+    static constexpr int EPI_ROW = WN + 16;
+    static constexpr int EPI_STAGE_FLOATS = LANES_M * EPI_ROW;
+    static constexpr size_t EPI_BYTES = size_t(CONSUMER_WARPS) * EPI_STAGE_FLOATS * 4;
+    static constexpr size_t SMEM_BYTES = RING_SMEM_BYTES;
+    // Epilogue rounds whose C_in loads are issued together (staged epilogue).
+    static constexpr int EPI_BATCH = 1;
     static constexpr int TILE_FLOATS = BM * BN;
     // EX: the kernel serves batched calls and the fused bias/activation
     // epilogue (see ExConfig); the plain kernel leaves that code out, which
@@ -152,6 +182,15 @@ struct FusedConfig : Base {
 template <class Base>
 struct AbortTestConfig : Base {
     static constexpr int DROP_RELEASE_SLAB = 2;
+};
+
+// The same tile configuration with the staged epilogue (store_tile_staged),
+// for C whose rows do not all start 16-byte aligned.
+template <class Base>
+struct StagedEpilogueConfig : Base {
+    static constexpr bool STAGED_EPI = true;
+    static constexpr size_t SMEM_BYTES = Base::RING_SMEM_BYTES + Base::EPI_BYTES;
+    static_assert(SMEM_BYTES <= 232448, "staging areas fit beside the ring");
 };
 
 struct MainParams {
@@ -423,6 +462,10 @@ __device__ __forceinline__ void store_tile(const float (&acc)[Cfg::TM][Cfg::TN],
             for (int t = 0; t < Cfg::TN / 4; ++t) {
                 const int col = col0 + t * 32;
                 const float *v = &acc[4 * s4 + r][4 * t];
+                // range-checked build: the four outputs lie in this tile
+                if (!SG_IN_RANGE(row >= tm * Cfg::BM && row < (tm + 1) * Cfg::BM &&
+                                 col >= tn * Cfg::BN && col + 3 < (tn + 1) * Cfg::BN))
+                    continue;
                 if (c_row_vec && col + 3 < p.N) {
                     float4 o;
                     if (beta != 0.0f) {
@@ -446,6 +489,102 @@ __device__ __forceinline__ void store_tile(const float (&acc)[Cfg::TM][Cfg::TN],
                             crow[col + e] = (beta != 0.0f) ? fmaf(alpha, v[e], c) : alpha * v[e];
                         }
                     }
+                }
+            }
+        }
+    }
+}
+
+// The epilogue for C whose rows do not all start 16-byte aligned (ldc % 4 !=
+// 0, or C itself not 16-byte aligned): C = alpha * acc + beta * C for this
+// thread's outputs of tile (tm, tn); C is not read when beta == 0; rows >= M
+// and columns >= N are not written.
+//
+// A thread's own outputs are four consecutive columns, 32 apart, of rows 16
+// apart, so 32-bit accesses straight from the registers would touch, per warp
+// access, four rows 16 bytes apart: four times the sectors they use.  Instead
+// the warp's outputs go through its staging area in shared memory (the
+// coalesced write-back through shared memory of "SGEMM CUDA kernel (Second
+// Half)", Part 9).  In round (s4, r) the warp holds four rows of C (one per
+// row group of lanes, 4 rows apart) of WN columns; the lanes write them to the
+// area, read them back row by row, and every warp access to C then covers 128
+// contiguous bytes of one row.  C_in is read the same way, EPI_BATCH rounds
+// at a time, after every line of the warp's part of C_in has been started
+// towards L2.
+template <class Cfg>
+__device__ __forceinline__ void store_tile_staged(const float (&acc)[Cfg::TM][Cfg::TN],
+                                                  const MainParams &p, int tm, int tn, int a_off,
+                                                  int b_off, uint32_t epi) {
+    constexpr int TM = Cfg::TM, TN = Cfg::TN, WN = Cfg::WN;
+    constexpr int RH = WN / 32;          // 32-column parts of a warp row
+    constexpr int RB = Cfg::EPI_BATCH;   // rounds whose C_in is loaded together
+    static_assert(4 * RH == TN, "a round holds TN values per lane");
+    static_assert(TM <= 32 && 4 % RB == 0, "rounds of a row group");
+    const int lane = threadIdx.x & 31;
+    const int rg = (a_off % Cfg::WM) >> 2, j = (b_off % WN) >> 2;   // lane row group, column group
+    const int roww = tm * Cfg::BM + a_off - 4 * rg;                  // the warp's first row
+    const int colw = tn * Cfg::BN + b_off - 4 * j;                   // and first column
+    const float alpha = p.alpha, beta = p.beta;
+    if (beta != 0.0f) {
+        // the warp's rows are roww .. roww + 4 * TM - 1: lane l starts row
+        // roww + l (and roww + l + 32, ...) towards L2, every line it touches
+#pragma unroll
+        for (int i = 0; i < (4 * TM + 31) / 32; ++i) {
+            const int row = roww + lane + 32 * i;
+            if (lane + 32 * i < 4 * TM && row < p.M) {
+                const float *crow = p.C + (long long)row * p.ldc;
+#pragma unroll
+                for (int h = 0; h <= RH; ++h) {
+                    const int col = min(colw + 32 * h, colw + WN - 1);
+                    if (col < p.N) prefetch_l2(crow + col);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < TM / RB; ++g) {
+        const int s4 = (g * RB) / 4, r0 = (g * RB) % 4;
+        float cin[RB][TN];
+        if (beta != 0.0f) {
+#pragma unroll
+            for (int rr = 0; rr < RB; ++rr)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int rq = roww + 4 * q + 16 * s4 + r0 + rr;
+                    const float *crow = p.C + (long long)rq * p.ldc;
+#pragma unroll
+                    for (int h = 0; h < RH; ++h) {
+                        const int col = colw + lane + 32 * h;
+                        cin[rr][RH * q + h] = (rq < p.M && col < p.N) ? __ldcs(crow + col) : 0.0f;
+                    }
+                }
+        }
+#pragma unroll
+        for (int rr = 0; rr < RB; ++rr) {
+            __syncwarp();   // the previous round's reads of the area are done
+#pragma unroll
+            for (int t = 0; t < TN / 4; ++t) {
+                const float *v = &acc[4 * s4 + r0 + rr][4 * t];
+                if (SG_IN_RANGE(rg * Cfg::EPI_ROW + 4 * j + 32 * t + 3 < Cfg::EPI_STAGE_FLOATS))
+                    sts128(epi + uint32_t(rg * Cfg::EPI_ROW + 4 * j + 32 * t) * 4u,
+                           make_float4(v[0], v[1], v[2], v[3]));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int rq = roww + 4 * q + 16 * s4 + r0 + rr;
+                float *crow = p.C + (long long)rq * p.ldc;
+#pragma unroll
+                for (int h = 0; h < RH; ++h) {
+                    const int col = colw + lane + 32 * h;
+                    if (!SG_IN_RANGE(q * Cfg::EPI_ROW + lane + 32 * h < Cfg::EPI_STAGE_FLOATS &&
+                                     rq >= tm * Cfg::BM && rq < (tm + 1) * Cfg::BM &&
+                                     col >= tn * Cfg::BN && col < (tn + 1) * Cfg::BN))
+                        continue;
+                    const float x = lds32(epi + uint32_t(q * Cfg::EPI_ROW + lane + 32 * h) * 4u);
+                    if (rq < p.M && col < p.N)
+                        __stcs(crow + col, (beta != 0.0f) ? fmaf(alpha, x, beta * cin[rr][RH * q + h])
+                                                          : alpha * x);
                 }
             }
         }
@@ -503,6 +642,10 @@ __device__ __forceinline__ void store_tile_ex(const float (&acc)[Cfg::TM][Cfg::T
             for (int t = 0; t < Cfg::TN / 4; ++t) {
                 const int col = col0 + t * 32;
                 const float *v = &acc[4 * s4 + r][4 * t];
+                // range-checked build: the four outputs lie in this tile
+                if (!SG_IN_RANGE(row >= tm * Cfg::BM && row < (tm + 1) * Cfg::BM &&
+                                 col >= tn * Cfg::BN && col + 3 < (tn + 1) * Cfg::BN))
+                    continue;
                 if (c_row_vec && col + 3 < p.N) {
                     float4 o;
                     if (beta != 0.0f) {
@@ -578,7 +721,8 @@ __device__ __forceinline__ void sum_pieces_row(float (&row)[Cfg::TN], const floa
             ++b1;
         }
         if (b0 < b1) {
-            const int slot = 2 * b + (b0 >= tile_start ? 0 : 1);
+            int slot = 2 * b + (b0 >= tile_start ? 0 : 1);
+            if (!SG_IN_RANGE(slot >= 0 && slot < 2 * int(gridDim.x))) slot = 0;
             const float4 *src = reinterpret_cast<const float4 *>(partials + (size_t)slot * Cfg::TILE_FLOATS);
 #pragma unroll
             for (int j4 = 0; j4 < Cfg::TN / 4; ++j4) {
@@ -616,7 +760,7 @@ __device__ __forceinline__ void block_stream_k_tiles(const MainParams &p, int k_
     const long long x0 = sk_start(blockIdx.x, p.sk_slabs, gridDim.x);
     const long long x1 = sk_start(blockIdx.x + 1, p.sk_slabs, gridDim.x);
     for (long long t = x0 / k_tiles; x0 < x1 && t <= (x1 - 1) / k_tiles; ++t)
-        atomicAdd(&p.counters[t], 1 << 24);
+        if (SG_IN_RANGE(t < p.sk_slabs / k_tiles)) atomicAdd(&p.counters[t], 1 << 24);
 }
 
 // ------------------------------------------------------------------ main kernel
@@ -628,7 +772,9 @@ struct Ring {
     uint32_t base;
     static constexpr uint32_t B_OFF = uint32_t(Cfg::STAGES * Cfg::A_STAGE) * 4u;
     static constexpr uint32_t BAR_OFF = B_OFF + uint32_t(Cfg::STAGES * Cfg::B_STAGE) * 4u;
-    static constexpr uint32_t BYTES = BAR_OFF + 16u * Cfg::STAGES + 16u;
+    static constexpr uint32_t EPI_OFF = BAR_OFF + 16u * Cfg::STAGES + 16u;
+    static constexpr uint32_t BYTES = EPI_OFF + (Cfg::STAGED_EPI ? uint32_t(Cfg::EPI_BYTES) : 0u);
+    static_assert(EPI_OFF % 16 == 0, "staging areas take 128-bit accesses");
 
     __device__ uint32_t a(int s) const { return base + uint32_t(s * Cfg::A_STAGE) * 4u; }
     __device__ uint32_t b(int s) const { return base + B_OFF + uint32_t(s * Cfg::B_STAGE) * 4u; }
@@ -637,6 +783,10 @@ struct Ring {
     __device__ uint32_t abort_flag() const { return base + BAR_OFF + 16u * Cfg::STAGES; }
     __device__ bool aborted() const { return ld_shared_flag(abort_flag()) != 0; }
     __device__ void set_abort() const { st_shared_flag(abort_flag(), 1); }
+    // epilogue staging area of consumer warp cw (StagedEpilogueConfig)
+    __device__ uint32_t epi(int cw) const {
+        return base + EPI_OFF + uint32_t(cw * Cfg::EPI_STAGE_FLOATS) * 4u;
+    }
 };
 
 // State of the TMA issuer: the next slab to copy is slab `slab` of segment
@@ -688,6 +838,15 @@ __device__ __forceinline__ bool issue_one(State &st, const Ring<Cfg> &ring,
         st.tn = tn;
     }
     const int s = st.stage;
+    // range-checked build: the copy's box starts on a 16-byte boundary (x a
+    // multiple of 4 floats), inside the k range, into a stage of the ring;
+    // otherwise nothing is copied and the CTA aborts as after an expiry
+    if (!SG_IN_RANGE(s >= 0 && s < Cfg::STAGES && st.slab >= 0 && st.slab < k_tiles &&
+                     (st.tm * Cfg::BM) % 4 == 0 && (st.tn * Cfg::BN) % 4 == 0 &&
+                     st.tm < p.tiles_m && st.tn < p.tiles_n)) {
+        ring.set_abort();
+        return false;
+    }
     // first use of a stage: parity 1 refers to the phase before the barrier's
     // first one and counts as complete
     if (!mbar_wait_at(ring.empty(s), st.phase ^ 1u, p.timeout_ns)) {
@@ -824,8 +983,19 @@ __device__ __forceinline__ void consumer_loop(const Ring<Cfg> &ring, const MainP
                     ring.set_abort();
                 }
             }
-            const uint32_t a_s = a_base + uint32_t(s * Cfg::A_STAGE) * 4u;
-            const uint32_t b_s = b_base + uint32_t(s * Cfg::B_STAGE) * 4u;
+            uint32_t a_s = a_base + uint32_t(s * Cfg::A_STAGE) * 4u;
+            uint32_t b_s = b_base + uint32_t(s * Cfg::B_STAGE) * 4u;
+            // range-checked build: every fragment this thread reads in the slab
+            // lies in stage s (otherwise read the stage's start instead)
+            if (!SG_IN_RANGE(
+                    (a_s & 15u) == 0 && (b_s & 15u) == 0 && a_s >= ring.a(s) && b_s >= ring.b(s) &&
+                    a_s + uint32_t((BK - 1) * BM + (TM / 4 - 1) * 16 + 4) * 4u <=
+                        ring.a(s) + uint32_t(Cfg::A_STAGE) * 4u &&
+                    b_s + uint32_t((BK - 1) * BN + (TN / 4 - 1) * 32 + 4) * 4u <=
+                        ring.b(s) + uint32_t(Cfg::B_STAGE) * 4u)) {
+                a_s = ring.a(s);
+                b_s = ring.b(s);
+            }
             // register double buffering of the fragments: the loads for k+1
             // are issued before the FMAs of k
             float fa[2][TM], fb[2][TN];
@@ -858,13 +1028,18 @@ __device__ __forceinline__ void consumer_loop(const Ring<Cfg> &ring, const MainP
         if (slot >= 0) {
             // ---- stream-K piece: publish the partial sums; the piece that
             // completes the tile's count adds all pieces in k order
-            write_partial<Cfg>(acc, p.partials + (size_t)slot * (BM * BN), ctid);
+            if (SG_IN_RANGE(slot >= 0 && slot < 2 * int(gridDim.x)))
+                write_partial<Cfg>(acc, p.partials + (size_t)slot * (BM * BN), ctid);
             __threadfence();
             named_barrier(BAR_CONSUMERS, Cfg::CONSUMER_THREADS);
             if (ctid == 0) {
                 const int rel_tile = int(fix.tile_start / k_tiles);
-                const int before = atomicAdd(&p.counters[rel_tile], 1);
-                fix.last = (before == fix.pieces - 1);
+                if (SG_IN_RANGE(rel_tile >= 0 && rel_tile < p.sk_slabs / k_tiles)) {
+                    const int before = atomicAdd(&p.counters[rel_tile], 1);
+                    fix.last = (before == fix.pieces - 1);
+                } else {
+                    fix.last = 0;
+                }
             }
             named_barrier(BAR_CONSUMERS, Cfg::CONSUMER_THREADS);
             finish = fix.last;
@@ -897,6 +1072,9 @@ __device__ __forceinline__ void consumer_loop(const Ring<Cfg> &ring, const MainP
             } else if constexpr (Cfg::EX) {
                 tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
                 store_tile_ex<Cfg>(acc, p, x, 0, tm, tn, a_off(), b_off());
+            } else if constexpr (Cfg::STAGED_EPI) {
+                tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                store_tile_staged<Cfg>(acc, p, tm, tn, a_off(), b_off(), ring.epi(cw));
             } else {
                 tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
                 store_tile<Cfg>(acc, p, tm, tn, a_off(), b_off());

@@ -78,6 +78,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
     return mbar_wait_at(smem_addr(bar), parity, timeout_ns);
 }
 
+// Shared-memory data access by 32-bit shared-window address (the memory
+// clobber keeps them in program order with the warp's other shared accesses).
+__device__ __forceinline__ void sts128(uint32_t addr, float4 v) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ float lds32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Volatile 32-bit shared-memory flag access by shared-window address.
 __device__ __forceinline__ int ld_shared_flag(uint32_t addr) {
     int v;

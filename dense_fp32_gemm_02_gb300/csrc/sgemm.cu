@@ -4,8 +4,8 @@
 //
 // Path of one sgemm() call (all on the caller's stream, no host sync):
 //   1. pack_a_transpose_kernel: A (M x K, any lda) -> At (K x roundup(M, 4))
-//   2. pack_b_copy_kernel, only when B's address or row pitch is not 16-byte
-//      aligned as the TMA requires
+//   2. B re-pitched, only when B's address or row pitch is not 16-byte aligned
+//      as the TMA requires: one pack_ab_kernel does steps 1 and 2 together
 //   3. sgemm_tma_ffma_kernel: persistent CTAs, TMA ring, FFMA micro-tiles,
 //      alpha/beta epilogue straight to C
 //   4. the workspace goes back to the pool, ordered after step 3.
@@ -19,6 +19,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <string>
 #include <utility>
 #include <vector>
 
@@ -110,6 +111,18 @@ std::atomic<int> g_t3_pair{-1};
 // 4097: 17 tile rows of 256 or 33 of 128).
 long long padded_area(const Variant &v, int M, int N) {
     return ((M + v.bm - 1LL) / v.bm) * v.bm * (((N + v.bn - 1LL) / v.bn) * v.bn);
+}
+
+// Stream-K is worth its fix-up (partial sums written and read back, a second
+// pass over them before the epilogue) only while whole tiles alone would
+// leave a noticeable share of the SMs' slots idle in their last wave.  Below
+// 1 % it is left out: 16384x16384x512 (8192 tiles of 256x128 in 54 waves of
+// 152, 0.2 % idle) measured 86.4 % of the FFMA peak with whole tiles only
+// against 86.1 % with the stream-K tail; 8192^3 (2048 tiles, 3.8 % idle)
+// keeps it.
+bool stream_k_pays(long long tiles, int sms) {
+    const long long waves = (tiles + sms - 1) / sms;
+    return double(waves * sms - tiles) >= 0.01 * double(waves * sms);
 }
 
 int pick_variant(int M, int N, int K) {
@@ -237,6 +250,9 @@ int device_state(DeviceState **out) {
             if ((e = ex_variant().set_attr()) != cudaSuccess) return cuda_fail(e);
             if ((e = fused_variant().set_attr()) != cudaSuccess) return cuda_fail(e);
             if ((e = abort_test_variant().set_attr()) != cudaSuccess) return cuda_fail(e);
+            for (int i = 0; i < sgv::staged_variants().count; ++i)
+                if ((e = sgv::staged_variants().entries[i].set_attr()) != cudaSuccess)
+                    return cuda_fail(e);
             if ((e = cudaFuncSetAttribute(sg::t3::sgemm_3xtf32_pair_kernel,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           int(sg::t3::P_SMEM_BYTES))) != cudaSuccess)
@@ -338,6 +354,22 @@ int checked_call(const GemmCall &g) {
     return SGEMM_OK;
 }
 
+// The pre-pass of one GEMM whose B must be re-pitched, in one launch
+// (pack_ab_kernel): up to 16 blocks per SM for each of the A transpose (64x64
+// tiles) and the B copy (16 x 256 strips), each part walking its own work.
+void launch_pack_ab(const float *A, long long lda, int M, int K, float *At, long long ldat,
+                    const float *B, long long ldb, int N, float *Bp, long long ldbp, int *zero,
+                    int zero_count, int sms, cudaStream_t stream) {
+    const long long cap = 16LL * sms;
+    const long long a_tiles = ((K + 63LL) / 64) * ((M + 63LL) / 64);
+    const long long b_strips = ((N + 255LL) / 256) * ((K + 15LL) / 16);
+    const int a_blocks = int(std::min(a_tiles, cap)), b_blocks = int(std::min(b_strips, cap));
+    sg::pack_ab_kernel<<<a_blocks + b_blocks, 256, 0, stream>>>(A, lda, M, K, At, ldat, B, ldb, N,
+                                                                Bp, ldbp, a_blocks, zero,
+                                                                zero_count);
+    g_launches.fetch_add(1);
+}
+
 int launch_scale(cudaStream_t stream, const GemmCall &g, int sms) {
     const long long total = (long long)g.M * g.N * g.batch;
     const int blocks = int(std::min<long long>((total + 255) / 256, (long long)sms * 8));
@@ -360,6 +392,24 @@ sg::ExParams ex_params(const GemmCall &g, int a_planes, int b_planes) {
     x.bias_vec4 = (g.bias && aligned16(g.bias) && g.stride_bias % 4 == 0) ? 1 : 0;
     x.act = g.act;
     return x;
+}
+
+// The kernel of a plain GEMM: the variant pick_variant() names, or the same
+// tile with the staged epilogue (store_tile_staged) when that pays: it is one
+// of the two default tiles, the rows of C do not all start 16-byte aligned,
+// C_in is read (beta != 0) and K is short (at most 2048: 32 slabs per tile).
+// There the staged epilogue's loads of C_in (128 contiguous bytes per warp
+// access, instead of four times the sectors they use) outweigh its main loop,
+// which runs about 2 % slower at the staged kernel's register allocation
+// (same box: 4097x3001x1023 with beta 1 0.430 ms against 0.458; with beta 0
+// 0.420 against 0.416; 4096x3001x4096 equal; 8192x8191x8192 15.84 against
+// 15.54).
+const Variant &plain_variant(int M, int N, int K, float beta, const float *C, int ldc) {
+    const int id = pick_variant(M, N, K);
+    const bool rows_aligned = aligned16(C) && ldc % 4 == 0;
+    if (id <= 1 && !rows_aligned && beta != 0.0f && K <= 2048)
+        return sgv::staged_variants().entries[id];
+    return variant_at(id);
 }
 
 // True when the default 256x128x64 tiling offers fewer slabs of work than
@@ -406,7 +456,7 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
     const Variant &var = batched ? ex_variant()
                          : extended ? fused_variant()
                          : drop_test ? abort_test_variant()
-                                     : variant_at(pick_variant(M, N, K));
+                                     : plain_variant(M, N, K, g.beta, g.C, g.ldc);
     // A and B enter as one plane per batch, or one plane for all batches when
     // their stride is 0
     const int a_planes = (g.batch > 1 && g.stride_a != 0) ? g.batch : 1;
@@ -416,9 +466,10 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
     const long long tiles_m = (M + var.bm - 1) / var.bm, tiles_n = (N + var.bn - 1) / var.bn;
     const long long tiles = tiles_m * tiles_n * g.batch;
     const long long k_tiles = (K + var.bk - 1) / var.bk;
-    const int grid = var.stream_k ? int(std::min<long long>(dev->sm_count, tiles * k_tiles))
-                                  : int(std::min<long long>(dev->sm_count, tiles));
-    const long long dp_tiles = var.stream_k ? (tiles / grid) * grid : tiles;
+    const bool sk = var.stream_k && stream_k_pays(tiles, dev->sm_count);
+    const int grid = sk ? int(std::min<long long>(dev->sm_count, tiles * k_tiles))
+                        : int(std::min<long long>(dev->sm_count, tiles));
+    const long long dp_tiles = sk ? (tiles / grid) * grid : tiles;
     const long long sk_tiles = tiles - dp_tiles;
     const long long sk_slabs = sk_tiles * k_tiles;
     if (tiles > (1LL << 30)) return SGEMM_ERR_TOO_LARGE;
@@ -451,7 +502,10 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
 
     {
         ProfScope prof(stream, false);
-        if (a_planes == 1) {
+        if (a_planes == 1 && b_planes == 1 && !b_direct) {
+            launch_pack_ab(g.A, g.lda, M, K, At, ldat, g.B, g.ldb, N, Bp, ldbp, counters,
+                           int(sk_tiles), dev->sm_count, stream);
+        } else if (a_planes == 1) {
             dim3 pgrid(unsigned(std::min<long long>((K + 63) / 64, 1LL << 20)),
                        unsigned(std::min<long long>((M + 63) / 64, 65535)));
             sg::pack_a_transpose_kernel<<<pgrid, 256, 0, stream>>>(g.A, g.lda, M, K, At, ldat,
@@ -468,7 +522,7 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
                 z0 == 0 ? int(sk_tiles) : 0);
             g_launches.fetch_add(1);
         }
-        if (!b_direct) {
+        if (!b_direct && !(a_planes == 1 && b_planes == 1)) {
             dim3 bgrid(unsigned(std::min<long long>((N + 255) / 256, 64)),
                        unsigned(std::min<long long>(K, 65535)),
                        unsigned(std::min(b_planes, 65535)));
@@ -476,8 +530,7 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
                                                               ldbp, bp_plane, b_planes);
             g_launches.fetch_add(1);
         }
-    }
-    e = cudaGetLastError();
+    }    e = cudaGetLastError();
     if (e != cudaSuccess) {
         cudaFreeAsync(ws, stream);
         return cuda_fail(e);
@@ -906,13 +959,15 @@ int read_and_clear_error_word(cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e);
     cudaError_t (*const units[])(unsigned *, bool) = {
         &sgv::unit_error_word, sgv::extra_variants().error_word,
-        sgv::sweep_variants_a().error_word, sgv::sweep_variants_b().error_word};
+        sgv::staged_variants().error_word, sgv::sweep_variants_a().error_word,
+        sgv::sweep_variants_b().error_word};
     unsigned any = 0;
     for (auto word : units) {
         unsigned v = 0;
         if ((e = word(&v, true)) != cudaSuccess) return cuda_fail(e);
         any |= v;
     }
+    if (any & sg::ERR_BOUNDS) return SGEMM_ERR_BOUNDS;
     return any ? SGEMM_ERR_TIMEOUT : SGEMM_OK;
 }
 
@@ -962,7 +1017,9 @@ int noalloc_state(NoAllocState **out) {
             }
             for (int i = 0; i < variant_count(); ++i)
                 if ((e = variant_at(i).set_attr()) != cudaSuccess) return cuda_fail(e);
-            if ((e = ex_variant().set_attr()) != cudaSuccess) return cuda_fail(e);
+            for (int i = 0; i < sgv::staged_variants().count; ++i)
+                if ((e = sgv::staged_variants().entries[i].set_attr()) != cudaSuccess)
+                    return cuda_fail(e);
             // In host code the array's name is only a host-side stand-in: the
             // kernels must be given its device address.
             void *ptr = nullptr;
@@ -988,7 +1045,7 @@ int sgemm_device_noalloc(int M, int N, int K, float alpha, const float *A, int l
     if (K == 0 || alpha == 0.0f) return launch_scale(stream, plain_call(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc),
                             dev->sm_count);
 
-    const Variant &var = variant_at(pick_variant(M, N, K));
+    const Variant &var = plain_variant(M, N, K, beta, C, ldc);
     const long long ldat = round_up(M, 4);
     const bool b_direct = aligned16(B) && (ldb % 4 == 0);
     const long long ldbp = b_direct ? ldb : round_up(N, 4);
@@ -999,14 +1056,13 @@ int sgemm_device_noalloc(int M, int N, int K, float alpha, const float *A, int l
     float *At = dev->scratch;
     float *Bp = b_direct ? const_cast<float *>(B) : dev->scratch + at_floats;
 
-    dim3 grid(unsigned(std::min<long long>((K + 63) / 64, 1LL << 20)),
-              unsigned(std::min<long long>((M + 63) / 64, 65535)));
-    sg::pack_a_transpose_kernel<<<grid, 256, 0, stream>>>(A, lda, M, K, At, ldat, nullptr, 0);
-    g_launches.fetch_add(1);
     if (!b_direct) {
-        dim3 bgrid(unsigned(std::min<long long>((N + 255) / 256, 64)),
-                   unsigned(std::min<long long>(K, 65535)));
-        sg::pack_b_copy_kernel<<<bgrid, 256, 0, stream>>>(B, ldb, 0, K, N, Bp, ldbp, 0, 1);
+        launch_pack_ab(A, lda, M, K, At, ldat, B, ldb, N, Bp, ldbp, nullptr, 0, dev->sm_count,
+                       stream);
+    } else {
+        dim3 grid(unsigned(std::min<long long>((K + 63) / 64, 1LL << 20)),
+                  unsigned(std::min<long long>((M + 63) / 64, 65535)));
+        sg::pack_a_transpose_kernel<<<grid, 256, 0, stream>>>(A, lda, M, K, At, ldat, nullptr, 0);
         g_launches.fetch_add(1);
     }
     cudaError_t e = cudaGetLastError();
@@ -1084,6 +1140,7 @@ SGEMM_API const char *sgemm_status_string(int status) {
         case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT: a bounded in-kernel wait expired";
         case SGEMM_ERR_ALLOC: return "SGEMM_ERR_ALLOC: workspace allocation failed";
         case SGEMM_ERR_TOO_LARGE: return "SGEMM_ERR_TOO_LARGE: the problem needs more scratch than the fixed array of sgemm_noalloc holds";
+        case SGEMM_ERR_BOUNDS: return "SGEMM_ERR_BOUNDS: the range-checked build found an index out of range (the access was skipped)";
         default: return "unknown sgemm status";
     }
 }
@@ -1159,7 +1216,20 @@ SGEMM_API int sgemm_profile_collect(double *main_ms, long long *main_launches, d
 SGEMM_API long long sgemm_kernel_launch_count(void) { return g_launches.load(); }
 
 SGEMM_API const char *sgemm_config_string(int M, int N, int K) {
-    return variant_at(pick_variant(M, N, K)).name;
+    const Variant &v = variant_at(pick_variant(M, N, K));
+    if (!v.stream_k || M <= 0 || N <= 0) return v.name;
+    // with a device, say when the work split leaves the stream-K tail out
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();   // the failure just caused here (no device) is not kept
+        return v.name;
+    }
+    const long long tiles = ((M + v.bm - 1LL) / v.bm) * ((N + v.bn - 1LL) / v.bn);
+    if (sms <= 0 || stream_k_pays(tiles, sms)) return v.name;
+    thread_local std::string text;
+    text = std::string(v.name) + " (whole tiles only on this device)";
+    return text.c_str();
 }
 
 SGEMM_API int sgemm_variant_count(void) { return variant_count(); }
@@ -1173,6 +1243,14 @@ SGEMM_API int sgemm_set_variant(int id) {
     if (id < -1 || id >= variant_count()) return SGEMM_ERR_INVALID_ARG;
     g_forced_variant.store(id);
     return SGEMM_OK;
+}
+
+SGEMM_API int sgemm_debug_bounds_checks(void) {
+#ifdef SGEMM_DEBUG_BOUNDS
+    return 1;
+#else
+    return 0;
+#endif
 }
 
 SGEMM_API int sgemm_debug_drop_release(int on) {

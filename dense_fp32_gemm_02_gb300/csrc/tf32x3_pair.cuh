@@ -361,6 +361,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             for (int c = 0; c < ncols / 32; ++c) {
                 float v[32];
                 __syncwarp();   // tcgen05.ld is warp-collective; buf reuse
+                // range-checked build: the 32 columns lie in this accumulator
+                if (!SG_IN_RANGE(a * ACC_COLS + c * 32 + 32 <= TMEM_COLS && c * 32 + 32 <= ACC_COLS))
+                    break;
                 tmem_load32(src + uint32_t(c * 32), v);
                 if (c == ncols / 32 - 1) {
                     // all of this accumulator is in registers: hand it back to CTA 0
@@ -382,7 +385,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 if (col_ok) {
 #pragma unroll
                     for (int r = 0; r < 32; ++r) {
-                        if (row0 + r < p.M) {
+                        if (row0 + r < p.M &&
+                            SG_IN_RANGE(row0 + r >= tm * P_BM && row0 + r < (tm + 1) * P_BM &&
+                                        col >= col0 && col < col0 + ncols)) {
                             const float x = buf[r * 33 + lane];
                             p.C[(long long)(row0 + r) * p.ldc + col] =
                                 (beta != 0.0f) ? fmaf(alpha, x, beta * cin[r]) : alpha * x;

@@ -5,7 +5,8 @@
 // The library is built from several translation units compiled in parallel:
 // sgemm.cu (host code, the default configurations, the 3xTF32 kernels),
 // extra_variants.cu (the batched and fused-epilogue kernels, the
-// failure-detection test kernel) and sweep_variants_a.cu /
+// failure-detection test kernel), staged_variants.cu (the default tiles with
+// the staged epilogue) and sweep_variants_a.cu /
 // sweep_variants_b.cu (configurations kept for tile-configuration sweeps).  They are linked without relocatable device
 // code, so each unit has its own copy of the device error word (kernels.cuh);
 // every table carries the function that reads and clears its unit's copy.
@@ -72,5 +73,9 @@ VariantTable sweep_variants_b();
 // test kernel, at these indices.
 enum { EXTRA_BATCHED = 0, EXTRA_FUSED = 1, EXTRA_DROP_RELEASE = 2 };
 VariantTable extra_variants();
+
+// staged_variants.cu: variants 0 and 1 (in that order) with the staged
+// epilogue, for C whose rows do not all start 16-byte aligned.
+VariantTable staged_variants();
 
 }  // namespace sgv

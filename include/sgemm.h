@@ -47,7 +47,9 @@ typedef enum {
     SGEMM_ERR_CUDA = 3,               /* a CUDA runtime/driver call failed; see sgemm_last_cuda_error() */
     SGEMM_ERR_TIMEOUT = 4,            /* a bounded in-kernel wait expired (reported by sgemm_device_status) */
     SGEMM_ERR_ALLOC = 5,              /* device or pinned workspace allocation failed */
-    SGEMM_ERR_TOO_LARGE = 6           /* sgemm_noalloc: the problem does not fit its fixed scratch */
+    SGEMM_ERR_TOO_LARGE = 6,          /* sgemm_noalloc: the problem does not fit its fixed scratch */
+    SGEMM_ERR_BOUNDS = 7              /* range-checked build only: an index was out of range
+                                         (reported by sgemm_device_status) */
 } sgemm_status;
 
 /*
@@ -191,8 +193,9 @@ int sgemm_last_cuda_error(void);
  * sgemm_device_status -- synchronises `stream`, then reads and clears the
  * library's device-side error word for the current device.  Returns SGEMM_OK,
  * or SGEMM_ERR_TIMEOUT if a kernel gave up a bounded wait (it then wrote no
- * result for the affected tiles), or SGEMM_ERR_CUDA if the synchronisation
- * itself failed.
+ * result for the affected tiles), or SGEMM_ERR_BOUNDS (range-checked build
+ * only, sgemm_debug_bounds_checks) if a kernel found an index out of range, or
+ * SGEMM_ERR_CUDA if the synchronisation itself failed.
  */
 int sgemm_device_status(sgemm_stream_t stream);
 
@@ -214,6 +217,20 @@ int sgemm_set_wait_timeout_ns(unsigned long long ns);
  * outcome), and the error word is left cleared.
  */
 int sgemm_selftest_wait_timeout(unsigned long long ns, sgemm_stream_t stream);
+
+/*
+ * sgemm_debug_bounds_checks -- 1 when this library is the range-checked build
+ * (compiled with -DSGEMM_DEBUG_BOUNDS: libsgemm_debug_bounds.so), 0 otherwise.
+ * In that build every kernel checks the indices of its shared-memory,
+ * global-memory, tensor-memory and TMA accesses against the ranges they must
+ * lie in (the fragments of a slab inside its ring stage, the outputs of a tile
+ * inside the tile, stream-K slots and counters inside their arrays, pre-pass
+ * writes inside the row pitch, ...).  An index out of range is not used: the
+ * access is skipped and sgemm_device_status() reports SGEMM_ERR_BOUNDS.  It is
+ * the library's own stand-in for a memory checker, for tests; it runs slower
+ * and is never the library the package loads by default.
+ */
+int sgemm_debug_bounds_checks(void);
 
 /*
  * sgemm_debug_drop_release -- failure-detection test switch, off (0) by
@@ -250,7 +267,11 @@ long long sgemm_kernel_launch_count(void);
 
 /*
  * sgemm_config_string -- the kernel configuration sgemm() would pick for the
- * given shape (tile sizes, stages, micro-kernel), as static text.  No GPU work.
+ * given shape (tile sizes, stages, micro-kernel, work split), as text that
+ * stays valid until the calling thread's next call.  With a CUDA device
+ * current, it also says when the work split on that device leaves out the
+ * stream-K tail (whole tiles alone would leave under 1 % of the SMs' slots
+ * idle).  No GPU work.
  */
 const char *sgemm_config_string(int M, int N, int K);
 

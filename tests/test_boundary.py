@@ -127,6 +127,12 @@ def test_variant_selection_validates(lib):
     assert lib.sgemm_set_variant(n - 1) == 0 and lib.sgemm_set_variant(-1) == 0
 
 
+def test_default_library_is_not_the_range_checked_build(lib):
+    assert lib.sgemm_debug_bounds_checks() == 0
+    lib.sgemm_status_string.restype = ctypes.c_char_p
+    assert b"SGEMM_ERR_BOUNDS" in lib.sgemm_status_string(7)
+
+
 def test_drop_release_switch_validates(lib):
     assert lib.sgemm_debug_drop_release(2) == 1 and lib.sgemm_debug_drop_release(-1) == 1
     assert lib.sgemm_debug_drop_release(1) == 0 and lib.sgemm_debug_drop_release(0) == 0

@@ -74,6 +74,34 @@ def test_leading_dimensions_and_alignment(pads, offsets, kernel):
         assert np.isnan(full[:, N:]).all(), "C padding columns were written"
 
 
+@pytest.mark.parametrize("variant", [0, 1])
+@pytest.mark.parametrize("ldc_pad,c_off", [(0, 0), (2, 1), (3, 3), (4, 2)])
+def test_staged_epilogue_rows_not_16_byte_aligned(variant, ldc_pad, c_off):
+    """Rows of C that do not all start 16-byte aligned (odd row pitch, or a
+    base 4 or 12 bytes past a 16-byte boundary), with beta != 0 and a short K,
+    take the staged epilogue on both tile orientations: the whole C within the
+    bound, the padding columns beyond N untouched, and integer inputs bit-exact."""
+    from dense_fp32_gemm_02_gb300 import binding
+    M, N, K = 515, 1003, 300
+    binding.set_variant(variant)
+    try:
+        for dist, exact in (("upm1", False), ("int4", True)):
+            A, B, C = make_inputs(M, N, K, dist, dist, "int4" if exact else "normal",
+                                  seed=variant * 10 + ldc_pad, ldc=N + ldc_pad)
+            ref, bound = oracle.sgemm(A, B, C, 1.5, 0.5)
+            dC = run_gpu(A, B, C, 1.5, 0.5, offsets=(0, 0, c_off))
+            got = dC.cpu().numpy()
+            if exact:
+                assert np.array_equal(got, ref), (variant, ldc_pad, c_off)
+            else:
+                assert_within_bound(got, ref, bound, f"variant {variant} ldc+{ldc_pad} off {c_off}")
+            if ldc_pad:
+                full = dC.as_strided((M, N + ldc_pad), (N + ldc_pad, 1)).cpu().numpy()
+                assert np.isnan(full[:, N:]).all(), "C padding columns were written"
+    finally:
+        binding.set_variant(-1)
+
+
 def test_edge_rows_and_columns_not_written_outside_block(kernel):
     """Guard band: C is a window inside a NaN-filled buffer; nothing outside the
     M x N window may change."""
