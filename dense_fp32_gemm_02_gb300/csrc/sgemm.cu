@@ -120,6 +120,8 @@ long long padded_area(const Variant &v, int M, int N) {
 // 152, 0.2 % idle) measured 86.4 % of the FFMA peak with whole tiles only
 // against 86.1 % with the stream-K tail; 8192^3 (2048 tiles, 3.8 % idle)
 // keeps it.
+constexpr long long kAllStreamKSlabs = 64;
+
 bool stream_k_pays(long long tiles, int sms) {
     const long long waves = (tiles + sms - 1) / sms;
     return double(waves * sms - tiles) >= 0.01 * double(waves * sms);
@@ -501,7 +503,15 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
     const bool sk = var.stream_k && stream_k_pays(tiles, dev->sm_count);
     const int grid = sk ? int(std::min<long long>(dev->sm_count, tiles * k_tiles))
                         : int(std::min<long long>(dev->sm_count, tiles));
-    const long long dp_tiles = sk ? (tiles / grid) * grid : tiles;
+    // With long k ranges (kAllStreamKSlabs slabs per tile or more) every tile
+    // goes through stream-K: each CTA takes an equal contiguous run of slabs,
+    // so the CTAs reach tile boundaries, and the epilogue's burst of C
+    // traffic that comes with them, at different times instead of all at
+    // once.  Same box: 8192^3 15.494 -> 15.445 ms, 4096^3 1.9575 -> 1.9545;
+    // shorter k ranges lost (4097x3001x1023 0.4312 -> 0.4343, 4864x4096x1024
+    // 0.6069 -> 0.6110, 16384x16384x512 3.954 -> 4.010) and keep whole-tile
+    // waves with the stream-K tail.
+    const long long dp_tiles = !sk ? tiles : (k_tiles >= kAllStreamKSlabs ? 0 : (tiles / grid) * grid);
     const long long sk_tiles = tiles - dp_tiles;
     const long long sk_slabs = sk_tiles * k_tiles;
     if (tiles > (1LL << 30)) return SGEMM_ERR_TOO_LARGE;
