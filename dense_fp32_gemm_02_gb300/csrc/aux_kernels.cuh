@@ -172,21 +172,24 @@ __global__ void __launch_bounds__(256)
 // (any leading dimension or alignment), no pre-pass, no workspace, one launch.
 // 256 threads in a 16x16 grid, (TS/16) x (TS/16) outputs each; k in steps of
 // 32 through shared memory (A stored transposed, as in the pages' tiled
-// kernel), the next step's operands loaded into registers meanwhile.  Every output sums its k terms in ascending order with fused
-// multiply-adds, so the result is deterministic.
+// kernel), the next step's operands loaded into registers meanwhile.  Every
+// output sums its k terms in ascending order with fused multiply-adds, so the
+// result is deterministic.
 constexpr int SMALL_BK = 32;
+
+// This thread's TS/16 x TS/16 outputs of the tile at blockIdx.(y, x), summed
+// over k in [kb, ke) (acc starts at zero).
 template <int TS>
-__global__ void __launch_bounds__(256)
-    sgemm_small_kernel(int M, int N, int K, float alpha, const float *__restrict__ A,
-                       long long lda, const float *__restrict__ B, long long ldb, float beta,
-                       float *__restrict__ C, long long ldc) {
+__device__ __forceinline__ void small_tile_sum(float (&acc)[TS / 16][TS / 16], int M, int N,
+                                               const float *__restrict__ A, long long lda,
+                                               const float *__restrict__ B, long long ldb,
+                                               int kb, int ke) {
     constexpr int T = TS / 16;                       // outputs per thread along each side
     constexpr int LOADS = TS * SMALL_BK / 256;       // elements of A (and of B) per thread
     __shared__ float As[SMALL_BK][TS + 4];           // As[k][m]
     __shared__ float Bs[SMALL_BK][TS + 4];           // Bs[k][n]
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const long long row0 = (long long)blockIdx.y * TS, col0 = (long long)blockIdx.x * TS;
-    float acc[T][T];
 #pragma unroll
     for (int i = 0; i < T; ++i)
 #pragma unroll
@@ -201,14 +204,14 @@ __global__ void __launch_bounds__(256)
             const int e = threadIdx.x + q * 256;
             const long long gr = row0 + e / SMALL_BK;
             const int gk = k0 + e % SMALL_BK;
-            ra[q] = (gr < M && gk < K) ? A[gr * lda + gk] : 0.0f;
+            ra[q] = (gr < M && gk < ke) ? A[gr * lda + gk] : 0.0f;
             const long long gc = col0 + e % TS;
             const int gkb = k0 + e / TS;
-            rb[q] = (gkb < K && gc < N) ? B[(long long)gkb * ldb + gc] : 0.0f;
+            rb[q] = (gkb < ke && gc < N) ? B[(long long)gkb * ldb + gc] : 0.0f;
         }
     };
-    fetch(0);
-    for (int k0 = 0; k0 < K; k0 += SMALL_BK) {
+    fetch(kb);
+    for (int k0 = kb; k0 < ke; k0 += SMALL_BK) {
 #pragma unroll
         for (int q = 0; q < LOADS; ++q) {
             const int e = threadIdx.x + q * 256;
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(256)
             Bs[e / TS][e % TS] = rb[q];
         }
         __syncthreads();
-        if (k0 + SMALL_BK < K) fetch(k0 + SMALL_BK);
+        if (k0 + SMALL_BK < ke) fetch(k0 + SMALL_BK);
 #pragma unroll
         for (int kk = 0; kk < SMALL_BK; ++kk) {
             float a[T], b[T];
@@ -231,6 +234,16 @@ __global__ void __launch_bounds__(256)
         }
         __syncthreads();
     }
+}
+
+// alpha/beta update of this thread's outputs of the tile at blockIdx.(y, x)
+template <int TS>
+__device__ __forceinline__ void small_tile_store(const float (&acc)[TS / 16][TS / 16], int M, int N,
+                                                 float alpha, float beta, float *__restrict__ C,
+                                                 long long ldc) {
+    constexpr int T = TS / 16;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const long long row0 = (long long)blockIdx.y * TS, col0 = (long long)blockIdx.x * TS;
 #pragma unroll
     for (int i = 0; i < T; ++i) {
         const long long r = row0 + ty * T + i;
@@ -243,6 +256,60 @@ __global__ void __launch_bounds__(256)
             *out = (beta != 0.0f) ? fmaf(alpha, acc[i][j], beta * *out) : alpha * acc[i][j];
         }
     }
+}
+
+template <int TS>
+__global__ void __launch_bounds__(256)
+    sgemm_small_kernel(int M, int N, int K, float alpha, const float *__restrict__ A,
+                       long long lda, const float *__restrict__ B, long long ldb, float beta,
+                       float *__restrict__ C, long long ldc) {
+    float acc[TS / 16][TS / 16];
+    small_tile_sum<TS>(acc, M, N, A, lda, B, ldb, 0, K);
+    small_tile_store<TS>(acc, M, N, alpha, beta, C, ldc);
+}
+
+// The small-problem kernel with the k range split over the CTAs of a
+// thread-block cluster of 1 x 1 x S (S = gridDim.z, at most 8): a tile's S
+// CTAs sum k in [z * kchunk, (z + 1) * kchunk) each, so a problem of few
+// tiles keeps S times as many SMs busy and each CTA walks 1/S of the k
+// steps.  CTAs 1 .. S-1 leave their partial sums in their shared memory; CTA
+// 0 adds them to its own in the order z = 1, 2, ... through distributed
+// shared memory and runs the alpha/beta update, so the result does not depend
+// on which CTA finishes first.  A second cluster barrier keeps every CTA's
+// shared memory until CTA 0 has read it.
+template <int TS>
+__global__ void __launch_bounds__(256)
+    sgemm_small_splitk_kernel(int M, int N, int K, int kchunk, float alpha,
+                              const float *__restrict__ A, long long lda,
+                              const float *__restrict__ B, long long ldb, float beta,
+                              float *__restrict__ C, long long ldc) {
+    constexpr int T = TS / 16;
+    __shared__ float part[T * T][256];   // [output][thread]: a warp's accesses are contiguous
+    const int z = int(cluster_ctarank());
+    const int kb = z * kchunk, ke = min(K, kb + kchunk);
+    float acc[T][T];
+    small_tile_sum<TS>(acc, M, N, A, lda, B, ldb, kb, ke);
+    if (z != 0) {
+#pragma unroll
+        for (int i = 0; i < T; ++i)
+#pragma unroll
+            for (int j = 0; j < T; ++j) part[i * T + j][threadIdx.x] = acc[i][j];
+    }
+    cluster_barrier();   // the partial sums are visible to CTA 0
+    if (z == 0) {
+        const uint32_t mine = smem_addr(&part[0][threadIdx.x]);
+        for (int r = 1; r < int(gridDim.z); ++r) {
+            if (!SG_IN_RANGE(r < 8)) break;
+            const uint32_t peer = dsmem_map(mine, uint32_t(r));
+#pragma unroll
+            for (int i = 0; i < T; ++i)
+#pragma unroll
+                for (int j = 0; j < T; ++j)
+                    acc[i][j] += dsmem_ld_f32(peer + uint32_t((i * T + j) * 256) * 4u);
+        }
+        small_tile_store<TS>(acc, M, N, alpha, beta, C, ldc);
+    }
+    cluster_barrier();   // no CTA leaves while CTA 0 may still read its shared memory
 }
 
 // One thread waits on a barrier that nothing completes; the bounded wait must

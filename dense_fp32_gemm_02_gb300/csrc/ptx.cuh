@@ -91,6 +91,30 @@ __device__ __forceinline__ float lds32(uint32_t addr) {
     return v;
 }
 
+// Thread-block clusters: this CTA's rank, a full barrier of the cluster
+// (release / acquire: shared-memory writes before it are visible to every CTA
+// of the cluster after it), the cluster-window address of the same shared
+// variable in CTA `rank`, and a 32-bit load through such an address.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Volatile 32-bit shared-memory flag access by shared-window address.
 __device__ __forceinline__ int ld_shared_flag(uint32_t addr) {
     int v;

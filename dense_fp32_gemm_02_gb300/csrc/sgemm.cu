@@ -120,8 +120,6 @@ long long padded_area(const Variant &v, int M, int N) {
 // 152, 0.2 % idle) measured 86.4 % of the FFMA peak with whole tiles only
 // against 86.1 % with the stream-K tail; 8192^3 (2048 tiles, 3.8 % idle)
 // keeps it.
-constexpr long long kAllStreamKSlabs = 64;
-
 bool stream_k_pays(long long tiles, int sms) {
     const long long waves = (tiles + sms - 1) / sms;
     return double(waves * sms - tiles) >= 0.01 * double(waves * sms);
@@ -455,9 +453,39 @@ bool small_problem(int M, int N, int K, int sms) {
 
 int launch_small(const GemmCall &g, cudaStream_t stream, int sms) {
     const long long t64 = ((g.M + 63LL) / 64) * ((g.N + 63LL) / 64);
+    const long long t32 = ((g.M + 31LL) / 32) * ((g.N + 31LL) / 32);
     ProfCall prof(stream);
     prof.main_begin();
-    if (t64 < sms) {
+    // With 32x32 tiles that fill at most half the SMs, the k range of a tile
+    // is split over the CTAs of a cluster (S <= 8, at least two k steps of 32
+    // each): 256^3 runs 64 tiles x 4 CTAs instead of 64 CTAs walking all of K.
+    int S = 1, kchunk = g.K;
+    if (t64 < sms && 2 * t32 <= sms) {
+        const int by_sms = int(std::min<long long>(8, (2LL * sms) / t32));
+        const int by_k = (g.K + 2 * sg::SMALL_BK - 1) / (2 * sg::SMALL_BK);
+        S = std::max(1, std::min(by_sms, by_k));
+        if (S > 1) {
+            kchunk = int(round_up((g.K + S - 1) / S, sg::SMALL_BK));
+            S = (g.K + kchunk - 1) / kchunk;
+        }
+    }
+    if (S > 1) {
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3(unsigned((g.N + 31) / 32), unsigned((g.M + 31) / 32), unsigned(S));
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 1;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = unsigned(S);
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        cudaLaunchKernelEx(&cfg, sg::sgemm_small_splitk_kernel<32>, g.M, g.N, g.K, kchunk, g.alpha,
+                           g.A, (long long)g.lda, g.B, (long long)g.ldb, g.beta, g.C,
+                           (long long)g.ldc);
+    } else if (t64 < sms) {
         dim3 grid(unsigned((g.N + 31) / 32), unsigned((g.M + 31) / 32));
         sg::sgemm_small_kernel<32><<<grid, 256, 0, stream>>>(g.M, g.N, g.K, g.alpha, g.A, g.lda, g.B,
                                                             g.ldb, g.beta, g.C, g.ldc);
@@ -503,15 +531,7 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
     const bool sk = var.stream_k && stream_k_pays(tiles, dev->sm_count);
     const int grid = sk ? int(std::min<long long>(dev->sm_count, tiles * k_tiles))
                         : int(std::min<long long>(dev->sm_count, tiles));
-    // With long k ranges (kAllStreamKSlabs slabs per tile or more) every tile
-    // goes through stream-K: each CTA takes an equal contiguous run of slabs,
-    // so the CTAs reach tile boundaries, and the epilogue's burst of C
-    // traffic that comes with them, at different times instead of all at
-    // once.  Same box: 8192^3 15.494 -> 15.445 ms, 4096^3 1.9575 -> 1.9545;
-    // shorter k ranges lost (4097x3001x1023 0.4312 -> 0.4343, 4864x4096x1024
-    // 0.6069 -> 0.6110, 16384x16384x512 3.954 -> 4.010) and keep whole-tile
-    // waves with the stream-K tail.
-    const long long dp_tiles = !sk ? tiles : (k_tiles >= kAllStreamKSlabs ? 0 : (tiles / grid) * grid);
+    const long long dp_tiles = sk ? (tiles / grid) * grid : tiles;
     const long long sk_tiles = tiles - dp_tiles;
     const long long sk_slabs = sk_tiles * k_tiles;
     if (tiles > (1LL << 30)) return SGEMM_ERR_TOO_LARGE;

@@ -48,21 +48,6 @@ constexpr uint32_t P_IDESC = (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(P_BN
                              (uint32_t(P_BM >> 4) << 24);
 constexpr uint32_t P_IDESC_HALF = (P_IDESC & ~(0x3Fu << 17)) | (uint32_t((P_BN / 2) >> 3) << 17);
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// The shared::cluster address of the same shared variable in CTA `rank`.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-                 ::: "memory");
-}
 // Arrive (with an expected byte count) on a barrier of either CTA of the pair.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
@@ -202,7 +187,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base + 1);
     volatile int *issued_slot = abort_flag + 1;   // stages this CTA's producer filled
 
-    const uint32_t rank = cluster_rank();
+    const uint32_t rank = cluster_ctarank();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < P_STAGES; ++s) {
@@ -220,10 +205,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
     if (warp == 1) tmem_alloc_pair(tmem_base, TMEM_COLS);
     tc_fence_before();
-    cluster_sync_all();   // both CTAs' barriers, flags and TMEM exist before any remote use
+    cluster_barrier();   // both CTAs' barriers, flags and TMEM exist before any remote use
     tc_fence_after();
     const uint32_t taddr = *tmem_base;
-    const uint32_t peer_abort = map_to_rank(smem_addr((const void *)abort_flag), rank ^ 1u);
+    const uint32_t peer_abort = dsmem_map(smem_addr((const void *)abort_flag), rank ^ 1u);
     auto set_abort = [&] {
         *abort_flag = 1;
         st_cluster_flag(peer_abort, 1);
@@ -262,7 +247,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         break;
                     }
                     const uint32_t st = ring_s + uint32_t(stage * P_STAGE_FLOATS) * 4u;
-                    const uint32_t fb = map_to_rank(smem_addr(&full[stage]), 0u);
+                    const uint32_t fb = dsmem_map(smem_addr(&full[stage]), 0u);
                     mbar_arrive_expect_tx_cluster(fb, half ? P_STAGE_BYTES_HALF : P_STAGE_BYTES);
                     tma_load_2d_pair(st, &tmAh, fb, kb * BK, arow);
                     tma_load_2d_pair(st + uint32_t(P_A) * 4u, &tmAl, fb, kb * BK, arow);
@@ -369,7 +354,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     // all of this accumulator is in registers: hand it back to CTA 0
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_addr(&acc_empty[a]), 0u));
+                    if (lane == 0) mbar_arrive_cluster(dsmem_map(smem_addr(&acc_empty[a]), 0u));
                 }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) buf[lane * 33 + i] = v[i];
@@ -400,7 +385,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
-    cluster_sync_all();   // CTA 0's MMAs and both CTAs' remote arrivals are done
+    cluster_barrier();   // CTA 0's MMAs and both CTAs' remote arrivals are done
     // After an abort, copies of either producer may still be writing its CTA's
     // ring, and they count on CTA 0's full barriers, which only CTA 0 can wait
     // on.  Every abort was set in both CTAs before the barrier above, so both
@@ -411,7 +396,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (*abort_flag) {
         if (rank == 0 && threadIdx.x == 0) {
             const int mine = *issued_slot;
-            const int peer = ld_cluster_u32(map_to_rank(smem_addr((const void *)issued_slot), 1u));
+            const int peer = ld_cluster_u32(dsmem_map(smem_addr((const void *)issued_slot), 1u));
             const int lo = mine < peer ? mine : peer, hi = mine < peer ? peer : mine;
             // a producer runs at most P_STAGES fillings ahead of the MMAs, which
             // consume only stages both filled, so hi - lo <= P_STAGES
@@ -423,7 +408,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     break;
                 }
         }
-        cluster_sync_all();
+        cluster_barrier();
     }
     tc_fence_after();
     if (warp == 1) tmem_dealloc_pair(taddr, TMEM_COLS);

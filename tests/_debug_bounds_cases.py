@@ -78,8 +78,10 @@ def main():
     plain(4097, 3001, 1023, 1.0, 1.0, "ragged 4097x3001x1023")
     # stream-K: one output tile split over every CTA
     plain(200, 100, 16384, 1.0, 0.5, "stream-K 200x100x16384", exact=True)
-    # whole tiles only (last wave nearly full): 16384 x 2048 x 128
-    plain(16384, 2048, 128, 1.0, 0.0, "whole tiles 16384x2048x128")
+    # whole tiles only: 19 x 8 = 152 tiles of 256x128, one full wave, no stream-K
+    plain(4864, 1024, 256, 1.0, 0.0, "whole tiles 4864x1024x256")
+    # every tile by stream-K (64 slabs per tile): 128 tiles over all CTAs
+    plain(2048, 2048, 4096, 1.5, 0.5, "all stream-K 2048x2048x4096", exact=True)
     # 3xTF32, both main kernels
     for pair in (False, True):
         binding.set_3xtf32_kernel(pair)
