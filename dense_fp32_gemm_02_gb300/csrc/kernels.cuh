@@ -142,6 +142,9 @@ struct TileConfig {
     // Failure-detection test instantiation only (AbortTestConfig): the CTA
     // slab at which consumer warp 0 of CTA 0 leaves out its release; -1 here.
     static constexpr int DROP_RELEASE_SLAB = -1;
+    // CTAs resident per SM (TwoPerSMConfig: 2, each with half the registers
+    // and at most half the shared memory)
+    static constexpr int CTAS_PER_SM = 1;
 
     static_assert(WM * WARPS_M == BM && WN * WARPS_N == BN, "warp grid must cover the tile");
     static_assert(TM % 4 == 0 && TN % 4 == 0, "thread tile is made of 4x4 sub-tiles");
@@ -191,6 +194,17 @@ struct StagedEpilogueConfig : Base {
     static constexpr bool STAGED_EPI = true;
     static constexpr size_t SMEM_BYTES = Base::RING_SMEM_BYTES + Base::EPI_BYTES;
     static_assert(SMEM_BYTES <= 232448, "staging areas fit beside the ring");
+};
+
+// The same tile configuration with two CTAs resident per SM: the two run
+// their tiles independently, so one CTA's epilogue overlaps the other's main
+// loop.  The configuration must fit twice in an SM (registers: THREADS x 128
+// at most half the register file; shared memory: at most half of 227 KB).
+template <class Base>
+struct TwoPerSMConfig : Base {
+    static constexpr int CTAS_PER_SM = 2;
+    static_assert(Base::SMEM_BYTES <= 232448 / 2 - 1024, "two CTAs fit an SM's shared memory");
+    static_assert(Base::THREADS <= 256, "two CTAs fit an SM's register file at 128 registers");
 };
 
 struct MainParams {
@@ -1109,7 +1123,7 @@ __device__ __forceinline__ void consumer_loop(const Ring<Cfg> &ring, const MainP
 // consumer still passes the consumer barriers, and at the end the issuing
 // thread waits for the copies it issued (drain_limit_ns).
 template <class Cfg>
-__global__ void __launch_bounds__(Cfg::THREADS, 1)
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::CTAS_PER_SM)
     sgemm_tma_ffma_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB, const MainParams p,
                           const ExParams x) {

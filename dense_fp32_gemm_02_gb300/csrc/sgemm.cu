@@ -69,18 +69,21 @@ const Variant kMainVariants[] = {
 };
 
 // All variants in variant-number order: 0, 1 and 3 from this file, 2 and 4-6
-// from sweep_variants_a.cu, 7-11 from sweep_variants_b.cu.
+// from sweep_variants_a.cu, 7-11 from sweep_variants_b.cu, 12-13 from
+// sweep_variants_c.cu.
 struct VariantIndex {
     const Variant *v[32];
     int n = 0;
     VariantIndex() {
         const sgv::VariantTable a = sgv::sweep_variants_a(), b = sgv::sweep_variants_b();
+        const sgv::VariantTable c = sgv::sweep_variants_c();
         v[n++] = &kMainVariants[0];
         v[n++] = &kMainVariants[1];
         v[n++] = &a.entries[0];
         v[n++] = &kMainVariants[2];
         for (int i = 1; i < a.count; ++i) v[n++] = &a.entries[i];
         for (int i = 0; i < b.count; ++i) v[n++] = &b.entries[i];
+        for (int i = 0; i < c.count; ++i) v[n++] = &c.entries[i];
     }
 };
 const VariantIndex &variant_index() {
@@ -528,9 +531,10 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
     const long long tiles_m = (M + var.bm - 1) / var.bm, tiles_n = (N + var.bn - 1) / var.bn;
     const long long tiles = tiles_m * tiles_n * g.batch;
     const long long k_tiles = (K + var.bk - 1) / var.bk;
-    const bool sk = var.stream_k && stream_k_pays(tiles, dev->sm_count);
-    const int grid = sk ? int(std::min<long long>(dev->sm_count, tiles * k_tiles))
-                        : int(std::min<long long>(dev->sm_count, tiles));
+    const int slots = dev->sm_count * var.ctas_per_sm;   // persistent CTAs
+    const bool sk = var.stream_k && stream_k_pays(tiles, slots);
+    const int grid = sk ? int(std::min<long long>(slots, tiles * k_tiles))
+                        : int(std::min<long long>(slots, tiles));
     const long long dp_tiles = sk ? (tiles / grid) * grid : tiles;
     const long long sk_tiles = tiles - dp_tiles;
     const long long sk_slabs = sk_tiles * k_tiles;
@@ -1021,7 +1025,7 @@ int read_and_clear_error_word(cudaStream_t stream) {
     cudaError_t (*const units[])(unsigned *, bool) = {
         &sgv::unit_error_word, sgv::extra_variants().error_word,
         sgv::staged_variants().error_word, sgv::sweep_variants_a().error_word,
-        sgv::sweep_variants_b().error_word};
+        sgv::sweep_variants_b().error_word, sgv::sweep_variants_c().error_word};
     unsigned any = 0;
     for (auto word : units) {
         unsigned v = 0;
@@ -1148,7 +1152,7 @@ int sgemm_device_noalloc(int M, int N, int K, float alpha, const float *A, int l
     p.c_vec4 = aligned16(C) ? 1 : 0;
     p.timeout_ns = g_timeout_ns.load();
     const long long tiles = (long long)p.tiles_m * p.tiles_n;
-    const int grid_main = int(std::min<long long>(tiles, dev->sm_count));
+    const int grid_main = int(std::min<long long>(tiles, (long long)dev->sm_count * var.ctas_per_sm));
     p.dp_tiles = int(tiles);     // whole tiles only: no partial-sum scratch needed
     p.sk_slabs = 0;
     p.partials = nullptr;

@@ -24,6 +24,7 @@ struct Variant {
     int bm, bn, bk;
     bool stream_k;
     int group_m;
+    int ctas_per_sm;   // resident CTAs per SM: the persistent grid is ctas_per_sm x SMs
     cudaError_t (*set_attr)();
     void (*launch)(int grid, cudaStream_t s, const CUtensorMap &a, const CUtensorMap &b,
                    const sg::MainParams &p, const sg::ExParams &x);
@@ -43,8 +44,8 @@ void launch_t(int grid, cudaStream_t s, const CUtensorMap &a, const CUtensorMap 
 
 template <class Cfg>
 constexpr Variant make_variant(const char *name, bool stream_k, int group_m = 8) {
-    return Variant{name, Cfg::BM, Cfg::BN, Cfg::BK, stream_k, group_m, &set_attr_t<Cfg>,
-                   &launch_t<Cfg>};
+    return Variant{name,      Cfg::BM,          Cfg::BN,          Cfg::BK, stream_k, group_m,
+                   Cfg::CTAS_PER_SM, &set_attr_t<Cfg>, &launch_t<Cfg>};
 }
 
 // Reads this translation unit's device error word into *v (current device),
@@ -67,6 +68,7 @@ struct VariantTable {
 
 VariantTable sweep_variants_a();
 VariantTable sweep_variants_b();
+VariantTable sweep_variants_c();
 
 // extra_variants.cu: the default tile for batched calls with the fused
 // epilogue, for one GEMM with the fused epilogue, and the failure-detection
