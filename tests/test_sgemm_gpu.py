@@ -102,6 +102,19 @@ def test_staged_epilogue_rows_not_16_byte_aligned(variant, ldc_pad, c_off):
         binding.set_variant(-1)
 
 
+def test_config_string_reports_the_work_split_on_this_device():
+    """With a device current, the configuration text says when the work split
+    leaves the stream-K tail out: 16384x16384x512 is 8192 tiles of 256x128, 54
+    waves of 152 with 0.2 % of the slots idle; 8192^3 (2048 tiles, 3.8 % idle)
+    keeps the tail."""
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the split of these shapes assumes 152 SMs")
+    assert "whole tiles only" in binding.config_string(16384, 16384, 512)
+    assert "whole tiles only" not in binding.config_string(8192, 8192, 8192)
+
+
 def test_edge_rows_and_columns_not_written_outside_block(kernel):
     """Guard band: C is a window inside a NaN-filled buffer; nothing outside the
     M x N window may change."""
