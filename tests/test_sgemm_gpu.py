@@ -102,6 +102,34 @@ def test_staged_epilogue_rows_not_16_byte_aligned(variant, ldc_pad, c_off):
         binding.set_variant(-1)
 
 
+@pytest.mark.parametrize("M,N,K", [
+    (64, 64, 128),      # 4 tiles of 32x32: split in two (two k steps each)
+    (33, 95, 200),      # 12 tiles, ragged: split in four
+    (256, 256, 256),    # the 256^3 workload: 64 tiles x 4 CTAs
+    (7, 5, 1000),       # one tile: split in eight
+    (100, 130, 4099),   # 20 tiles, K not a multiple of 32: split in eight
+])
+def test_small_problem_k_split_over_clusters(M, N, K):
+    """Small problems whose 32x32 tiles fill at most half the SMs split the k
+    range over a cluster's CTAs, CTA 0 adding the others' partial sums in a
+    fixed order: integer inputs bit-exact (any order is exact), random inputs
+    within the bound, misaligned operands and padded pitches included, and
+    bitwise the same on a second call."""
+    from dense_fp32_gemm_02_gb300 import binding
+    binding.set_variant(-1)
+    A, B, C = make_inputs(M, N, K, "int4", "int4", "int4", seed=M + N + K, lda=K + 3, ldc=N + 1)
+    ref, _ = oracle.sgemm(A, B, C, 1.5, 0.5)
+    got = run_gpu(A, B, C, 1.5, 0.5, offsets=(1, 2, 3)).cpu().numpy()
+    assert np.array_equal(got, ref), (M, N, K)
+    A, B, C = make_inputs(M, N, K, "upm1", "normal", "normal", seed=M * N + K)
+    ref, bound = oracle.sgemm(A, B, C, -0.75, 1.25)
+    first = run_gpu(A, B, C, -0.75, 1.25).cpu().numpy()
+    second = run_gpu(A, B, C, -0.75, 1.25).cpu().numpy()
+    assert_within_bound(first, ref, bound, f"split-K {M}x{N}x{K}")
+    assert np.array_equal(first, second), "split-K result changed between calls"
+    assert binding.device_status() == binding.SGEMM_OK
+
+
 def test_config_string_reports_the_work_split_on_this_device():
     """With a device current, the configuration text says when the work split
     leaves the stream-K tail out: 16384x16384x512 is 8192 tiles of 256x128, 54
