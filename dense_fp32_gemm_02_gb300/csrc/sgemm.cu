@@ -823,12 +823,12 @@ struct EventSet {
 };
 
 // Row blocks of the host-buffer pipeline: a first block of kEdgeRows rows (the
-// first multiply waits only for its own operands), a last one of kEdgeRows (the
+// first multiply waits only for its own operands), a last one of kLastRows (the
 // copy back after the last multiply is short) and blocks of about kMidRows rows
 // between them (fewer launches); `uniform`: equal blocks of at least kEdgeRows
 // rows, at most 8.  One block when M < 2 * kEdgeRows or when nothing is
 // multiplied.  Returns (first row, rows) per block.
-constexpr int kEdgeRows = 1024, kMidRows = 2048;
+constexpr int kEdgeRows = 1024, kMidRows = 2048, kLastRows = 512;
 std::vector<std::pair<int, int>> host_row_blocks(int M, bool multiply, bool uniform) {
     std::vector<std::pair<int, int>> b;
     if (!multiply || M < 2 * kEdgeRows) {
@@ -847,14 +847,17 @@ std::vector<std::pair<int, int>> host_row_blocks(int M, bool multiply, bool unif
         b.emplace_back(kEdgeRows, rest);
         return b;
     }
-    const int mid = rest - kEdgeRows;
+    const int mid = rest - kLastRows;
     const int nmid = (mid + kMidRows - 1) / kMidRows;
+    // block starts on multiples of 128 rows, so only the last block can leave
+    // a partly filled tile row
     for (int i = 0; i < nmid; ++i) {
-        const int r0 = kEdgeRows + int((long long)mid * i / nmid);
-        const int r1 = kEdgeRows + int((long long)mid * (i + 1) / nmid);
+        const int r0 = kEdgeRows + int((long long)mid * i / nmid) / 128 * 128;
+        const int r1 = i + 1 == nmid ? M - kLastRows
+                                     : kEdgeRows + int((long long)mid * (i + 1) / nmid) / 128 * 128;
         b.emplace_back(r0, r1 - r0);
     }
-    b.emplace_back(M - kEdgeRows, kEdgeRows);
+    b.emplace_back(M - kLastRows, kLastRows);
     return b;
 }
 
@@ -883,9 +886,28 @@ int host_gemm(int M, int N, int K, float alpha, const float *A, int lda, const f
     const std::vector<std::pair<int, int>> blocks = host_row_blocks(M, need_ab, tensor);
     int max_rows = 0;
     for (const auto &b : blocks) max_rows = std::max(max_rows, b.second);
-    // block 0 in k-chunks when K is long enough for the copies of B to matter
-    const int kchunks = (need_ab && K >= 4096) ? 4 : 1;
-    const int kc = need_ab ? int(round_up((K + kchunks - 1) / kchunks, 64)) : 0;
+    // Block 0 in k-chunks when K is long enough for the copies of B to matter.
+    // 3xTF32: four equal chunks.  FFMA: a first chunk of K/8 (the first
+    // multiply waits only for it) and chunks growing by half after it: a
+    // chunk's multiply takes longer than the copy of the next one (at 8192^3
+    // 0.28 us against 0.18 us of host link per k), so the copies stay ahead.
+    // K = 8192: 1024, 1536, 2304, 3328.
+    std::vector<std::pair<int, int>> chunks;   // (k0, kn)
+    if (need_ab && K >= 4096 && !tensor) {
+        int k0 = 0, kn = int(round_up((K + 7) / 8, 64));
+        while (k0 < K) {
+            if (K - k0 - kn < kn / 2) kn = K - k0;   // no short last chunk
+            chunks.emplace_back(k0, kn);
+            k0 += kn;
+            kn = int(round_up(kn + kn / 2, 64));
+        }
+    } else if (need_ab && K >= 4096) {
+        const int kc = int(round_up((K + 3) / 4, 64));
+        for (int k0 = 0; k0 < K; k0 += kc) chunks.emplace_back(k0, std::min(kc, K - k0));
+    } else if (need_ab) {
+        chunks.emplace_back(0, K);
+    }
+    const int kchunks = int(chunks.size());
     // The 3xTF32 path is bound by the host link, not by its first multiply:
     // it keeps equal row blocks and C_in in front of B (the deferred add and
     // the unequal blocks measured 0.4-1.3 % slower there, 2.2 % faster on the
@@ -950,8 +972,7 @@ int host_gemm(int M, int N, int K, float alpha, const float *A, int lda, const f
         if (bi == 0 && need_ab) {
             // block 0: copy order A_0 chunk, (C_0 unless deferred), B chunk, ...
             for (int c = 0; c < kchunks; ++c) {
-                const int k0 = c * kc, kn = std::min(kc, K - k0);
-                if (kn <= 0) break;
+                const int k0 = chunks[c].first, kn = chunks[c].second;
                 cudaEvent_t chunk = evs.make();
                 if (!chunk) return fail(SGEMM_ERR_CUDA);
                 e = cudaMemcpy2DAsync(dA + k0, size_t(K) * 4, A + k0, size_t(lda) * 4,

@@ -123,15 +123,16 @@ int sgemm_ex(int M, int N, int K, float alpha,
  *
  * A, B, C are host pointers (page-locked memory gives the fastest copies, but
  * pageable memory is accepted).  The call works through row blocks of A and C
- * (M >= 2048: a first and a last block of 1024 rows, blocks of about 2048 rows
- * between them; one block otherwise): block i is copied in on a host-to-device
- * copy stream, multiplied on `stream` while block i+1 is copied in, and copied
- * back into C (respecting ldc) on a device-to-host copy stream while block i+1
- * is multiplied.  When K >= 4096, block 0 and B are copied in four k-chunks
- * (columns of A, rows of B) and block 0 is multiplied chunk by chunk as they
+ * (M >= 2048: a first block of 1024 rows, a last one of 512, blocks of about
+ * 2048 rows between them; one block otherwise): block i is copied in on a
+ * host-to-device copy stream, multiplied on `stream` while block i+1 is
+ * copied in, and copied back into C (respecting ldc) on a device-to-host copy
+ * stream while block i+1 is multiplied.  When K >= 4096, block 0 and B are
+ * copied in k-chunks (columns of A, rows of B: the first K/8 deep, each next
+ * one half again as deep) and block 0 is multiplied chunk by chunk as they
  * land, the first chunk with beta = 0 and the others accumulating into its C
  * rows; beta * C_in is added to block 0 after its C_in has been copied in
- * behind the chunks.  So the first GEMM waits for a quarter of B and of A's
+ * behind the chunks.  So the first GEMM waits for an eighth of B and of A's
  * first block only.  Device buffers come from the library pool; the two copy
  * streams are the library's own (one pair per device).  `stream` is
  * synchronised before returning, so C holds the result on return.  Results

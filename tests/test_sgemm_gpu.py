@@ -348,10 +348,10 @@ def test_stream_k_split_matches_oracle(M, N, K, kernel):
 @pytest.mark.parametrize("tensor_cores", [False, True])
 @pytest.mark.parametrize("pinned", [True, False])
 def test_host_entry_point_pipelined_over_row_blocks(tensor_cores, pinned):
-    """M = 4100 splits into four row blocks (copy in, multiply, copy back
-    overlap): 1024, 1026, 1026 and 1024 rows on the FFMA path, four of 1025 on
-    the 3xTF32 path; padded leading dimensions and beta != 0; checked against
-    the oracle on rows at every block boundary of both and on columns."""
+    """M = 4100 splits into row blocks (copy in, multiply, copy back overlap):
+    1024, 1280, 1284 and 512 rows on the FFMA path, four of 1025 on the 3xTF32
+    path; padded leading dimensions and beta != 0; checked against the oracle
+    on rows at every block boundary of both and on columns."""
     import torch
     from dense_fp32_gemm_02_gb300 import binding
     M, N, K = 4100, 777, 515
@@ -365,7 +365,8 @@ def test_host_entry_point_pipelined_over_row_blocks(tensor_cores, pinned):
         tB = torch.from_numpy(B.base.copy()).pin_memory()[:, :N]
         cbuf = cbuf.pin_memory()
     binding.sgemm_host(tA, tB, cbuf[:, :N], 1.25, -0.5, tensor_cores=tensor_cores)
-    rows = np.array([0, 1, 1023, 1024, 2049, 2050, 3075, 3076, 4099], np.int64)
+    rows = np.array([0, 1, 1023, 1024, 1025, 2049, 2050, 2303, 2304, 3075, 3076, 3587, 3588, 4099],
+                    np.int64)
     cols = np.array([0, 5, 300, 776], np.int64)
     got = cbuf.numpy()
     ref, bound = oracle.sgemm_rows(A, B, C, 1.25, -0.5, rows)
@@ -378,13 +379,14 @@ def test_host_entry_point_pipelined_over_row_blocks(tensor_cores, pinned):
 
 @pytest.mark.parametrize("tensor_cores", [False, True])
 def test_host_entry_point_first_block_in_k_chunks(tensor_cores):
-    """K >= 4096: block 0 is multiplied in four k-chunks of A and B (1088,
-    1088, 1088 and 836 here, the last not a multiple of the tile depth) as
-    they arrive, accumulating into its rows of C.  FFMA path: blocks of 1024
-    and 1076 rows, the first chunk with beta = 0 and beta * C_in added once
-    C_in has arrived; 3xTF32 path: two blocks of 1050 rows, C_in copied in
-    front.  The other block takes the whole of K.  beta != 0 and padded
-    leading dimensions; oracle on rows at both plans' boundaries and on
+    """K >= 4096: block 0 is multiplied in k-chunks of A and B as they
+    arrive, accumulating into its rows of C.  FFMA path: chunks of 576, 896,
+    1344 and 1284 (K/8 first, each next one half again as long, the last not a
+    multiple of the tile depth), blocks of 1024 and 1076 rows, the first chunk
+    with beta = 0 and beta * C_in added once C_in has arrived; 3xTF32 path:
+    four chunks of 1088, 1088, 1088 and 836, two blocks of 1050 rows, C_in
+    copied in front.  The other block takes the whole of K.  beta != 0 and
+    padded leading dimensions; oracle on rows at both plans' boundaries and on
     columns."""
     import torch
     from dense_fp32_gemm_02_gb300 import binding
