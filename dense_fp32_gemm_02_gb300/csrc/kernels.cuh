@@ -139,6 +139,8 @@ struct TileConfig {
     // keeps its main loop under the register cap.
     static constexpr bool EX = false;
     static constexpr bool BATCH = false;
+    // TallBatchConfig: a batch run as one tall GEMM (B's rows offset per batch)
+    static constexpr bool TALL = false;
     // Failure-detection test instantiation only (AbortTestConfig): the CTA
     // slab at which consumer warp 0 of CTA 0 leaves out its release; -1 here.
     static constexpr int DROP_RELEASE_SLAB = -1;
@@ -174,6 +176,20 @@ template <class Base>
 struct FusedConfig : Base {
     static constexpr bool EX = true;
     static constexpr bool BATCH = false;
+};
+
+// The same tile configuration for a batch of GEMMs run as one tall GEMM: the
+// batches' transposed A side by side (K x batch*M), their C one under the
+// other (batch*M x N, batch b at row b*M), their B one under the other (batch
+// b's rows at b*K).  Every batch holds whole tiles (M a multiple of BM, K of
+// BK) and the raster groups are one batch's tile rows (group_m = M/BM), so a
+// tile's raster group is its batch, and only the copies of B depend on it:
+// their k coordinate starts at that batch's first row of B.  The rest is the
+// plain kernel, with its epilogue and its 123 registers (the batched kernel,
+// ExConfig, needs 128 and runs its main loop 2 % slower).
+template <class Base>
+struct TallBatchConfig : Base {
+    static constexpr bool TALL = true;
 };
 
 // The same tile configuration with one release left out on purpose: consumer
@@ -232,6 +248,8 @@ struct ExParams {
     // starts at C + b * stride_c; its A and B are plane b of the 3-D tensor
     // maps (plane 0 for every batch when a_planes / b_planes is 1).
     int batch;
+    // TallBatchConfig: rows of B per batch (0 when every batch shares one B)
+    int tall_b_rows;
     long long stride_c;
     int a_planes, b_planes;
     // Fused epilogue: C = act(alpha*acc + beta*C + bias[col]); bias may be null
@@ -827,6 +845,17 @@ struct IssueStateEx : IssueState {
     int tb;
 };
 
+// The issuer state of the tall-batch kernel: also the first row of B of the
+// current tile's batch.
+struct IssueStateTall : IssueState {
+    int b_row0;
+};
+
+template <class Cfg>
+using IssueStateOf = typename std::conditional<
+    Cfg::BATCH, IssueStateEx,
+    typename std::conditional<Cfg::TALL, IssueStateTall, IssueState>::type>::type;
+
 // Issue the copies of the next slab.  Returns false when there is none left or
 // the wait for the stage to be released expired (abort).
 template <class Cfg, class State>
@@ -847,6 +876,8 @@ __device__ __forceinline__ bool issue_one(State &st, const Ring<Cfg> &ring,
             st.tb = tb;
         } else {
             tile_coords(sg.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            // the raster group (tile_coords) is the batch
+            if constexpr (Cfg::TALL) st.b_row0 = (sg.tile / (p.group_m * p.tiles_n)) * x.tall_b_rows;
         }
         st.tm = tm;
         st.tn = tn;
@@ -875,6 +906,10 @@ __device__ __forceinline__ bool issue_one(State &st, const Ring<Cfg> &ring,
                        x.a_planes > 1 ? st.tb : 0);
         tma_load_3d_at(ring.b(s), tmB, ring.full(s), st.tn * Cfg::BN, st.slab * Cfg::BK,
                        x.b_planes > 1 ? st.tb : 0);
+    } else if constexpr (Cfg::TALL) {
+        tma_load_2d_at(ring.a(s), tmA, ring.full(s), st.tm * Cfg::BM, st.slab * Cfg::BK);
+        tma_load_2d_at(ring.b(s), tmB, ring.full(s), st.tn * Cfg::BN,
+                       st.b_row0 + st.slab * Cfg::BK);
     } else {
         tma_load_2d_at(ring.a(s), tmA, ring.full(s), st.tm * Cfg::BM, st.slab * Cfg::BK);
         tma_load_2d_at(ring.b(s), tmB, ring.full(s), st.tn * Cfg::BN, st.slab * Cfg::BK);
@@ -1137,7 +1172,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::CTAS_PER_SM)
     __shared__ FixInfo fix;
     // issuer state in shared memory (ISSUE_THREAD0, ISSUE_LAST_WARP): keeping
     // it out of registers leaves them to the accumulators
-    __shared__ typename std::conditional<Cfg::BATCH, IssueStateEx, IssueState>::type ist;
+    __shared__ IssueStateOf<Cfg> ist;
     __shared__ int released[STAGES];   // ISSUE_LAST_WARP: warps done with a stage
 
     const int warp = threadIdx.x >> 5;
@@ -1164,7 +1199,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::CTAS_PER_SM)
             // ======================================================== producer
             regs_decrease<Cfg::PRODUCER_REGS>();
             if (warp != 0) return;
-            typename std::conditional<Cfg::BATCH, IssueStateEx, IssueState>::type st;
+            IssueStateOf<Cfg> st;
             st.init(p);
             if (lane == 0) {
                 tma_prefetch_desc(&tmA);

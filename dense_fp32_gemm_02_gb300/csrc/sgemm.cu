@@ -101,6 +101,9 @@ const Variant &variant_at(int id) { return *variant_index().v[id]; }
 const Variant &ex_variant() { return sgv::extra_variants().entries[sgv::EXTRA_BATCHED]; }
 const Variant &fused_variant() { return sgv::extra_variants().entries[sgv::EXTRA_FUSED]; }
 const Variant &abort_test_variant() { return sgv::extra_variants().entries[sgv::EXTRA_DROP_RELEASE]; }
+// A batch that tall_batch_call() accepts runs as one tall GEMM through the
+// plain kernel's epilogue (tall_variants.cu).
+const Variant &tall_variant() { return sgv::tall_variants().entries[0]; }
 std::atomic<int> g_forced_variant{-1};
 std::atomic<int> g_drop_release{0};
 // 3xTF32 main kernel: -1 = chosen per shape (t3_use_pair), 0 = the single-CTA
@@ -283,6 +286,7 @@ int device_state(DeviceState **out) {
             if ((e = ex_variant().set_attr()) != cudaSuccess) return cuda_fail(e);
             if ((e = fused_variant().set_attr()) != cudaSuccess) return cuda_fail(e);
             if ((e = abort_test_variant().set_attr()) != cudaSuccess) return cuda_fail(e);
+            if ((e = tall_variant().set_attr()) != cudaSuccess) return cuda_fail(e);
             for (int i = 0; i < sgv::staged_variants().count; ++i)
                 if ((e = sgv::staged_variants().entries[i].set_attr()) != cudaSuccess)
                     return cuda_fail(e);
@@ -424,6 +428,7 @@ sg::ExParams ex_params(const GemmCall &g, int a_planes, int b_planes) {
     x.stride_bias = g.stride_bias;
     x.bias_vec4 = (g.bias && aligned16(g.bias) && g.stride_bias % 4 == 0) ? 1 : 0;
     x.act = g.act;
+    x.tall_b_rows = 0;
     return x;
 }
 
@@ -443,6 +448,27 @@ const Variant &plain_variant(int M, int N, int K, float beta, const float *C, in
     if (id <= 1 && !rows_aligned && beta != 0.0f && K <= 2048)
         return sgv::staged_variants().entries[id];
     return variant_at(id);
+}
+
+// True when a strided batch can run as one tall GEMM (TallBatchConfig): no
+// bias or activation, one A per batch, every batch whole tiles of the default
+// 256x128x64 tile (M a multiple of 256, K of 64) and at most 16 tile rows (the
+// raster groups are the batches, and a group of 16 rows is twice the default
+// 8), the batches of C one under the other (stride_c = M * ldc), and B either
+// shared (stride_b = 0), its batches one under the other (stride_b = K * ldb),
+// or re-pitched anyway (rows that break the TMA's 16-byte rule).  Batch b's
+// rows of C are then rows b*M .. b*M+M-1 of one (batch*M) x N matrix, its
+// transposed A columns b*M .. of one K x (batch*M) matrix, and its B rows
+// b*K .. of one (batch*K) x N matrix.  The batched kernel (ExConfig) takes the
+// rest: its 3-D tensor maps read B with any plane pitch, but its main loop
+// runs 2 % slower (same box: 64 x 1024^3 2.026 ms against 1.989).
+bool tall_batch_call(const GemmCall &g) {
+    if (g.batch <= 1 || g.bias != nullptr || g.act != sg::ACT_NONE || g.stride_a == 0) return false;
+    if (g.M % 256 != 0 || g.M > 16 * 256 || g.K % 64 != 0) return false;
+    if (g.stride_c != (long long)g.M * g.ldc) return false;
+    if ((long long)g.batch * g.M > INT32_MAX || (long long)g.batch * g.K > INT32_MAX) return false;
+    const bool b_tma = aligned16(g.B) && g.ldb % 4 == 0;
+    return !b_tma || g.stride_b == 0 || g.stride_b == (long long)g.K * g.ldb;
 }
 
 // True when the default 256x128x64 tiling offers fewer slabs of work than
@@ -518,7 +544,9 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
     if (!extended && !drop_test && g_forced_variant.load() < 0 &&
         small_problem(M, N, K, dev->sm_count))
         return launch_small(g, stream, dev->sm_count);
-    const Variant &var = batched ? ex_variant()
+    const bool tall = tall_batch_call(g);
+    const Variant &var = tall ? tall_variant()
+                         : batched ? ex_variant()
                          : extended ? fused_variant()
                          : drop_test ? abort_test_variant()
                                      : plain_variant(M, N, K, g.beta, g.C, g.ldc);
@@ -526,10 +554,14 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
     // their stride is 0
     const int a_planes = (g.batch > 1 && g.stride_a != 0) ? g.batch : 1;
     const int b_planes = (g.batch > 1 && g.stride_b != 0) ? g.batch : 1;
+    // the rows and batches the kernel walks: a tall batch is one GEMM of
+    // batch * M rows
+    const long long m_rows = tall ? (long long)g.batch * M : M;
+    const int k_batch = tall ? 1 : g.batch;
     // ---- work split: whole-tile waves, then the leftover tiles' k-slabs spread
     // evenly over all CTAs (stream-K) so the last wave is not partly idle
-    const long long tiles_m = (M + var.bm - 1) / var.bm, tiles_n = (N + var.bn - 1) / var.bn;
-    const long long tiles = tiles_m * tiles_n * g.batch;
+    const long long tiles_m = (m_rows + var.bm - 1) / var.bm, tiles_n = (N + var.bn - 1) / var.bn;
+    const long long tiles = tiles_m * tiles_n * k_batch;
     const long long k_tiles = (K + var.bk - 1) / var.bk;
     const int slots = dev->sm_count * var.ctas_per_sm;   // persistent CTAs
     const bool sk = var.stream_k && stream_k_pays(tiles, slots);
@@ -541,17 +573,23 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
     if (tiles > (1LL << 30)) return SGEMM_ERR_TOO_LARGE;
 
     // ---- workspace: transposed A, a re-pitched B if needed, stream-K partial
-    // sums and tile counters
-    const long long ldat = round_up(M, 4);
-    const long long at_plane = round_up((long long)K * ldat, 64);   // 256-byte aligned planes
+    // sums and tile counters.  A transposed: one K x ldat plane per batch
+    // (256-byte aligned planes), or for a tall batch one K x (batch*M) matrix
+    // with batch b's columns at b*M.
+    const long long ldat = tall ? m_rows : round_up(M, 4);
+    const long long at_plane = tall ? M : round_up((long long)K * ldat, 64);
     // B is read in place when the TMA can address it: 16-byte base and row
     // pitch, and (several planes) a 16-byte plane pitch that is at least a
     // whole matrix
     const bool b_direct = aligned16(g.B) && (g.ldb % 4 == 0) &&
                           (b_planes == 1 || (g.stride_b % 4 == 0 && g.stride_b >= (long long)K * g.ldb));
+    // (a tall batch's re-pitched B planes lie one under the other)
     const long long ldbp = b_direct ? g.ldb : round_up(N, 4);
-    const long long bp_plane = b_direct ? g.stride_b : round_up((long long)K * ldbp, 64);
-    const size_t at_bytes = size_t(at_plane) * a_planes * 4;
+    const long long bp_plane = b_direct ? g.stride_b
+                               : tall   ? (long long)K * ldbp
+                                        : round_up((long long)K * ldbp, 64);
+    const size_t at_bytes = tall ? size_t(round_up((long long)K * ldat, 64)) * 4
+                                 : size_t(at_plane) * a_planes * 4;
     const size_t bp_bytes = b_direct ? 0 : size_t(bp_plane) * b_planes * 4;
     const size_t part_bytes = sk_slabs ? size_t(2) * grid * var.bm * var.bn * 4 : 0;
     const size_t cnt_bytes = size_t(sk_tiles) * 4;
@@ -597,15 +635,21 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
                                                               ldbp, bp_plane, b_planes);
             g_launches.fetch_add(1);
         }
-    }    e = cudaGetLastError();
+    }
+    e = cudaGetLastError();
     if (e != cudaSuccess) {
         cudaFreeAsync(ws, stream);
         return cuda_fail(e);
     }
 
-    // the batched kernel takes 3-D tensor maps, the others 2-D maps
+    // the batched kernel takes 3-D tensor maps, the others 2-D maps (a tall
+    // batch's B: batch*K rows, or K when every batch shares it)
     CUtensorMap tmA, tmB;
-    if (batched) {
+    if (tall) {
+        const long long b_rows = b_planes > 1 ? (long long)g.batch * K : K;
+        if ((st = encode_2d(&tmA, At, m_rows, K, ldat, var.bm, var.bk)) == SGEMM_OK)
+            st = encode_2d(&tmB, Bp, N, b_rows, ldbp, var.bn, var.bk);
+    } else if (batched) {
         if ((st = encode_3d(&tmA, At, M, K, a_planes, ldat, at_plane, var.bm, var.bk)) == SGEMM_OK)
             st = encode_3d(&tmB, Bp, N, K, b_planes, ldbp, b_planes > 1 ? bp_plane : K * ldbp,
                            var.bn, var.bk);
@@ -621,21 +665,28 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
     sg::MainParams p;
     p.C = g.C;
     p.ldc = g.ldc;
-    p.M = M;
+    p.M = int(m_rows);
     p.N = N;
     p.K = K;
     p.alpha = g.alpha;
     p.beta = g.beta;
     p.tiles_m = int(tiles_m);
     p.tiles_n = int(tiles_n);
-    p.group_m = var.group_m;
+    // a tall batch's raster groups are its batches (TallBatchConfig)
+    p.group_m = tall ? M / var.bm : var.group_m;
     p.c_vec4 = aligned16(g.C) ? 1 : 0;
     p.timeout_ns = g_timeout_ns.load();
     p.dp_tiles = int(dp_tiles);
     p.sk_slabs = sk_slabs;
     p.partials = partials;
     p.counters = counters;
-    const sg::ExParams x = ex_params(g, a_planes, b_planes);
+    sg::ExParams x = ex_params(g, a_planes, b_planes);
+    if (tall) {
+        x.batch = 1;
+        x.a_planes = 1;
+        x.b_planes = 1;
+        x.tall_b_rows = b_planes > 1 ? K : 0;
+    }
     prof.main_begin();
     var.launch(grid, stream, tmA, tmB, p, x);
     prof.main_end();
@@ -1046,7 +1097,8 @@ int read_and_clear_error_word(cudaStream_t stream) {
     cudaError_t (*const units[])(unsigned *, bool) = {
         &sgv::unit_error_word, sgv::extra_variants().error_word,
         sgv::staged_variants().error_word, sgv::sweep_variants_a().error_word,
-        sgv::sweep_variants_b().error_word, sgv::sweep_variants_c().error_word};
+        sgv::sweep_variants_b().error_word, sgv::sweep_variants_c().error_word,
+        sgv::tall_variants().error_word};
     unsigned any = 0;
     for (auto word : units) {
         unsigned v = 0;

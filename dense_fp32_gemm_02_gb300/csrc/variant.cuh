@@ -6,8 +6,9 @@
 // sgemm.cu (host code, the default configurations, the 3xTF32 kernels),
 // extra_variants.cu (the batched and fused-epilogue kernels, the
 // failure-detection test kernel), staged_variants.cu (the default tiles with
-// the staged epilogue) and sweep_variants_a.cu /
-// sweep_variants_b.cu (configurations kept for tile-configuration sweeps).  They are linked without relocatable device
+// the staged epilogue), tall_variants.cu (a batch run as one tall GEMM) and
+// sweep_variants_a.cu / sweep_variants_b.cu / sweep_variants_c.cu
+// (configurations kept for tile-configuration sweeps).  They are linked without relocatable device
 // code, so each unit has its own copy of the device error word (kernels.cuh);
 // every table carries the function that reads and clears its unit's copy.
 #pragma once
@@ -79,5 +80,9 @@ VariantTable extra_variants();
 // staged_variants.cu: variants 0 and 1 (in that order) with the staged
 // epilogue, for C whose rows do not all start 16-byte aligned.
 VariantTable staged_variants();
+
+// tall_variants.cu: the default tile for a batch run as one tall GEMM
+// (TallBatchConfig).
+VariantTable tall_variants();
 
 }  // namespace sgv

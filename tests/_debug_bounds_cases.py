@@ -113,6 +113,24 @@ def main():
         ref, bound = oracle.sgemm_batched(As[:nb], Bs[:nb], Cs[:nb], 1.25, 0.5, bs[:nb], act)
         for b in range(nb):
             assert_within_bound(dC[b].cpu().numpy(), ref[b], bound[b], f"sgemm_ex {act} {b}")
+    # batches run as one tall GEMM: contiguous B (48 tiles, all by stream-K),
+    # and B re-pitched (rows of 203 floats) under a C with a padded pitch
+    for batch, M, N, K, ldc in ((3, 512, 1000, 512, 1000), (2, 768, 203, 192, 207)):
+        As, Bs, Cs = [], [], []
+        for b in range(batch):
+            A, B, C = make_inputs(M, N, K, "int4", "int4", "int4", seed=300 + b)
+            As.append(A), Bs.append(B), Cs.append(C)
+        dA = torch.stack([torch.from_numpy(a) for a in As]).cuda()
+        dB = torch.stack([torch.from_numpy(b) for b in Bs]).cuda()
+        full = torch.zeros((batch, M, ldc), device="cuda")
+        full[:, :, :N] = torch.stack([torch.from_numpy(c) for c in Cs]).cuda()
+        dC = full[:, :, :N]
+        binding.sgemm_ex_into(dA, dB, dC, 1.5, 0.5)
+        torch.cuda.synchronize()
+        status_ok(f"tall batch {batch}x{M}x{N}x{K}")
+        ref, _ = oracle.sgemm_batched(As, Bs, Cs, 1.5, 0.5, None, "none")
+        for b in range(batch):
+            assert np.array_equal(dC[b].cpu().numpy(), ref[b]), f"tall batch {b}"
     # host buffers (row blocks and k-chunks)
     A, B, C = make_inputs(2100, 300, 4100, "int4", "int4", "int4", seed=5)
     ref, _ = oracle.sgemm(A, B, C, 1.5, 0.5)
