@@ -106,6 +106,14 @@ typedef enum {
  * for sgemm(); the workspace holds one transposed A per batch (one when
  * stride_a == 0).
  *
+ * A batch with no bias and no activation, its own A per batch, M a multiple of
+ * 256 up to 4096, K a multiple of 64 and stride_c == M * ldc (batches of C one
+ * under the other) runs as one (batch*M) x N GEMM on the plain kernel; B is
+ * then read in place when shared or when stride_b == K * ldb, and re-pitched
+ * that way when its rows break the 16-byte rule.  Other batches run the
+ * batched kernel.  Either way the result meets sgemm()'s tolerance and is
+ * bitwise the same from call to call.
+ *
  * Errors: SGEMM_ERR_INVALID_ARG for a negative size, batch or stride, an
  * unknown `act`, a bias pointer not 4-byte aligned, overlapping batches of C,
  * or any condition sgemm() rejects; batch == 0 (like M == 0 or N == 0) is a
