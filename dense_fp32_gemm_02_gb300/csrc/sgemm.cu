@@ -131,11 +131,28 @@ bool stream_k_pays(long long tiles, int sms) {
     return double(waves * sms - tiles) >= 0.01 * double(waves * sms);
 }
 
-int pick_variant(int M, int N, int K) {
+// Few tiles: when the chosen orientation of the default tile makes fewer
+// tiles than a quarter of the SMs, stream-K splits every tile over more than
+// four CTAs, and the CTA that completes a tile reads back all its pieces
+// (128 KB each) before the epilogue.  The 128x128x48 tile of variant 9 (four
+// stages fed by a producer warpgroup) makes twice the tiles with half-size
+// pieces.  Same box, pre-pass + main kernel: 1024^3 0.066 ms against 0.073,
+// 768^3 0.049 against 0.065, 1024x1024x4096 0.164 against 0.172,
+// 128x4096x4096 0.101 against 0.115, 512x512x2048 0.065 against 0.084,
+// 128x3001x1023 0.068 against 0.070; 256x3001x1023 (24 tiles, no padding in
+// M for the 256-row tile) 0.073 against 0.071 is the one loss seen.  48 tiles
+// and more stay on the default tile (512x3001x1023: 0.090 against 0.095).
+// `sms` 0 (no device known) leaves this rule out.
+constexpr int kFewTilesVariant = 9;
+
+int pick_variant(int M, int N, int K, int sms) {
     const int forced = g_forced_variant.load();
     if (forced >= 0 && forced < variant_count()) return forced;
     (void)K;
-    return padded_area(variant_at(1), M, N) < padded_area(variant_at(0), M, N) ? 1 : 0;
+    const int id = padded_area(variant_at(1), M, N) < padded_area(variant_at(0), M, N) ? 1 : 0;
+    const Variant &v = variant_at(id);
+    const long long tiles = ((M + v.bm - 1LL) / v.bm) * ((N + v.bn - 1LL) / v.bn);
+    return (sms > 0 && 4 * tiles < sms) ? kFewTilesVariant : id;
 }
 
 struct DeviceState {
@@ -442,8 +459,8 @@ sg::ExParams ex_params(const GemmCall &g, int a_planes, int b_planes) {
 // (same box: 4097x3001x1023 with beta 1 0.430 ms against 0.458; with beta 0
 // 0.420 against 0.416; 4096x3001x4096 equal; 8192x8191x8192 15.84 against
 // 15.54).
-const Variant &plain_variant(int M, int N, int K, float beta, const float *C, int ldc) {
-    const int id = pick_variant(M, N, K);
+const Variant &plain_variant(int M, int N, int K, float beta, const float *C, int ldc, int sms) {
+    const int id = pick_variant(M, N, K, sms);
     const bool rows_aligned = aligned16(C) && ldc % 4 == 0;
     if (id <= 1 && !rows_aligned && beta != 0.0f && K <= 2048)
         return sgv::staged_variants().entries[id];
@@ -549,7 +566,7 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
                          : batched ? ex_variant()
                          : extended ? fused_variant()
                          : drop_test ? abort_test_variant()
-                                     : plain_variant(M, N, K, g.beta, g.C, g.ldc);
+                                     : plain_variant(M, N, K, g.beta, g.C, g.ldc, dev->sm_count);
     // A and B enter as one plane per batch, or one plane for all batches when
     // their stride is 0
     const int a_planes = (g.batch > 1 && g.stride_a != 0) ? g.batch : 1;
@@ -1180,10 +1197,11 @@ int sgemm_device_noalloc(int M, int N, int K, float alpha, const float *A, int l
     NoAllocState *dev = nullptr;
     if ((st = noalloc_state(&dev)) != SGEMM_OK) return st;
 
-    if (K == 0 || alpha == 0.0f) return launch_scale(stream, plain_call(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc),
+    if (K == 0 || alpha == 0.0f)
+        return launch_scale(stream, plain_call(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc),
                             dev->sm_count);
 
-    const Variant &var = plain_variant(M, N, K, beta, C, ldc);
+    const Variant &var = plain_variant(M, N, K, beta, C, ldc, dev->sm_count);
     const long long ldat = round_up(M, 4);
     const bool b_direct = aligned16(B) && (ldb % 4 == 0);
     const long long ldbp = b_direct ? ldb : round_up(N, 4);
@@ -1354,15 +1372,16 @@ SGEMM_API int sgemm_profile_collect(double *main_ms, long long *main_launches, d
 SGEMM_API long long sgemm_kernel_launch_count(void) { return g_launches.load(); }
 
 SGEMM_API const char *sgemm_config_string(int M, int N, int K) {
-    const Variant &v = variant_at(pick_variant(M, N, K));
-    if (!v.stream_k || M <= 0 || N <= 0) return v.name;
-    // with a device, say when the work split leaves the stream-K tail out
+    // with a device, its SM count picks the tile for few-tile shapes, and the
+    // text says when the work split leaves the stream-K tail out
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         cudaGetLastError();   // the failure just caused here (no device) is not kept
-        return v.name;
+        sms = 0;
     }
+    const Variant &v = variant_at(pick_variant(M, N, K, sms));
+    if (!v.stream_k || M <= 0 || N <= 0) return v.name;
     const long long tiles = ((M + v.bm - 1LL) / v.bm) * ((N + v.bn - 1LL) / v.bn);
     if (sms <= 0 || stream_k_pays(tiles, sms)) return v.name;
     thread_local std::string text;

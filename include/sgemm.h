@@ -21,7 +21,7 @@
  *  - Elements of C outside the M x N block (columns N..ldc-1) are never written.
  *  - Pointers must be 4-byte aligned; no other alignment is required.
  *  - C must not overlap A or B (not checked).
- *  - Summation order is fixed per build and shape: results are bitwise
+ *  - Summation order is fixed per build, shape and GPU model: results are bitwise
  *    reproducible run to run.  On the FFMA path each element's k terms are
  *    accumulated by fp32 fused multiply-adds over k ascending; where the work
  *    split cuts a tile along k (stream-K), the pieces' partial sums are added in

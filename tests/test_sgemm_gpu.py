@@ -130,6 +130,34 @@ def test_small_problem_k_split_over_clusters(M, N, K):
     assert binding.device_status() == binding.SGEMM_OK
 
 
+# Shapes whose chosen orientation of the default tile makes fewer tiles than a
+# quarter of the SMs run the 128x128x48 tile (variant 9): twice the tiles, so
+# stream-K cuts each into half as many pieces.  All of these are above the
+# small-problem kernel's threshold.
+FEW_TILE_SHAPES = [(1024, 1024, 1024), (768, 768, 768), (1, 3001, 1023), (256, 3001, 1023),
+                   (512, 512, 2048), (130, 700, 4000)]
+
+
+@pytest.mark.parametrize("M,N,K", FEW_TILE_SHAPES)
+def test_few_tile_shapes_take_the_128x128_tile_and_match_oracle(M, N, K):
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    binding.set_variant(-1)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = min(-(-M // 256) * -(-N // 128), -(-M // 128) * -(-N // 256))
+    name = binding.config_string(M, N, K)
+    if 4 * tiles < sms:
+        assert "tile=128x128x48" in name, name
+    A, B, C = make_inputs(M, N, K, "int4", "int4", "int4", seed=M + 7 * N + K)
+    ref, _ = oracle.sgemm(A, B, C, 1.5, 0.5)
+    got = run_gpu(A, B, C, 1.5, 0.5).cpu().numpy()
+    assert np.array_equal(got, ref), (M, N, K)
+    A, B, C = make_inputs(M, N, K, "upm1", "upm1", "normal", seed=M + 7 * N + K + 1)
+    ref, bound = oracle.sgemm(A, B, C, -0.75, 1.25)
+    got = run_gpu(A, B, C, -0.75, 1.25).cpu().numpy()
+    assert_within_bound(got, ref, bound, f"few tiles {M}x{N}x{K}")
+
+
 def test_config_string_reports_the_work_split_on_this_device():
     """With a device current, the configuration text says when the work split
     leaves the stream-K tail out: 16384x16384x512 is 8192 tiles of 256x128, 54
