@@ -62,6 +62,8 @@ lib.sgemm_kernel_launch_count.argtypes = []
 lib.sgemm_kernel_launch_count.restype = _ll
 lib.sgemm_config_string.argtypes = [_i, _i, _i]
 lib.sgemm_config_string.restype = ctypes.c_char_p
+lib.sgemm_last_kernel.argtypes = []
+lib.sgemm_last_kernel.restype = ctypes.c_char_p
 lib.sgemm_variant_count.argtypes = []
 lib.sgemm_variant_count.restype = _i
 lib.sgemm_variant_name.argtypes = [_i]
@@ -312,6 +314,11 @@ def kernel_launch_count() -> int:
 
 def config_string(M: int, N: int, K: int) -> str:
     return lib.sgemm_config_string(M, N, K).decode()
+
+
+def last_kernel() -> str:
+    """Configuration of the last main kernel this thread's calls launched."""
+    return lib.sgemm_last_kernel().decode()
 
 
 def variants() -> list:

@@ -38,6 +38,15 @@ constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
 constexpr int kMaxDevices = 64;
 
 thread_local int t_last_cuda_error = 0;
+// Configuration text of the last main kernel this thread's calls launched
+// (sgemm_last_kernel): a variant's name or one of the fixed texts below.
+thread_local const char *t_last_kernel = "";
+constexpr const char *kSmallKernel32 = "direct small-problem kernel, 32x32 tiles";
+constexpr const char *kSmallKernel64 = "direct small-problem kernel, 64x64 tiles";
+constexpr const char *kSmallSplitK = "direct small-problem kernel, 32x32 tiles, k split over a cluster";
+constexpr const char *kScaleOnly = "scale only (C = beta * C)";
+constexpr const char *kT3Pair = "3xtf32 tcgen05 cta_group::2, 256x256 pair tiles";
+constexpr const char *kT3Single = "3xtf32 tcgen05, 128x256 tiles";
 
 // ------------------------------------------------------------------ kernel variants
 // Every variant is the same persistent TMA/FFMA kernel with other tile sizes or
@@ -430,6 +439,7 @@ int launch_scale(cudaStream_t stream, const GemmCall &g, int sms) {
     sg::scale_c_kernel<<<blocks, 256, 0, stream>>>(g.C, g.ldc, g.stride_c, g.M, g.N, g.batch,
                                                    g.beta, g.bias, g.stride_bias, g.act);
     g_launches.fetch_add(1);
+    t_last_kernel = kScaleOnly;
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? SGEMM_OK : cuda_fail(e);
 }
@@ -528,15 +538,18 @@ int launch_small(const GemmCall &g, cudaStream_t stream, int sms) {
         attr.val.clusterDim.z = unsigned(S);
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
+        t_last_kernel = kSmallSplitK;
         cudaLaunchKernelEx(&cfg, sg::sgemm_small_splitk_kernel<32>, g.M, g.N, g.K, kchunk, g.alpha,
                            g.A, (long long)g.lda, g.B, (long long)g.ldb, g.beta, g.C,
                            (long long)g.ldc);
     } else if (t64 < sms) {
         dim3 grid(unsigned((g.N + 31) / 32), unsigned((g.M + 31) / 32));
+        t_last_kernel = kSmallKernel32;
         sg::sgemm_small_kernel<32><<<grid, 256, 0, stream>>>(g.M, g.N, g.K, g.alpha, g.A, g.lda, g.B,
                                                             g.ldb, g.beta, g.C, g.ldc);
     } else {
         dim3 grid(unsigned((g.N + 63) / 64), unsigned((g.M + 63) / 64));
+        t_last_kernel = kSmallKernel64;
         sg::sgemm_small_kernel<64><<<grid, 256, 0, stream>>>(g.M, g.N, g.K, g.alpha, g.A, g.lda, g.B,
                                                             g.ldb, g.beta, g.C, g.ldc);
     }
@@ -706,6 +719,7 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
     }
     prof.main_begin();
     var.launch(grid, stream, tmA, tmB, p, x);
+    t_last_kernel = var.name;
     prof.main_end();
     g_launches.fetch_add(1);
     e = cudaGetLastError();
@@ -807,10 +821,12 @@ int t3_run(int M, int N, int K, float alpha, const float *A, int lda, const floa
         const unsigned pairs = unsigned(std::min<long long>(tiles, sm_count / 2));
         t3::sgemm_3xtf32_pair_kernel<<<2 * pairs, t3::THREADS, t3::P_SMEM_BYTES, stream>>>(
             mAh, mAl, mBh, mBl, mBh2, mBl2, p);
+        t_last_kernel = kT3Pair;
     } else {
         const unsigned grid = unsigned(std::min<long long>(tiles, sm_count));
         t3::sgemm_3xtf32_kernel<<<grid, t3::THREADS, t3::SMEM_BYTES, stream>>>(
             mAh, mAl, mBh, mBl, mBh2, mBl2, p);
+        t_last_kernel = kT3Single;
     }
     prof.main_end();
     g_launches.fetch_add(1);
@@ -1248,6 +1264,7 @@ int sgemm_device_noalloc(int M, int N, int K, float alpha, const float *A, int l
     p.sk_slabs = 0;
     p.partials = nullptr;
     p.counters = nullptr;
+    t_last_kernel = var.name;
     var.launch(grid_main, stream, tmA, tmB, p,
                ex_params(plain_call(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc), 1, 1));
     g_launches.fetch_add(1);
@@ -1304,6 +1321,8 @@ SGEMM_API const char *sgemm_status_string(int status) {
 SGEMM_API int sgemm_version(void) { return kVersion; }
 
 SGEMM_API int sgemm_last_cuda_error(void) { return t_last_cuda_error; }
+
+SGEMM_API const char *sgemm_last_kernel(void) { return t_last_kernel; }
 
 SGEMM_API int sgemm_device_status(sgemm_stream_t stream) {
     DeviceState *dev = nullptr;

@@ -199,6 +199,18 @@ int sgemm_version(void);
 int sgemm_last_cuda_error(void);
 
 /*
+ * sgemm_last_kernel -- the configuration of the last main kernel that a call
+ * from the calling thread launched (any entry point), as static text that stays
+ * valid for the life of the process: a kernel variant's name (as
+ * sgemm_variant_name gives it; the batched, fused, tall-batch and
+ * staged-epilogue kernels have their own), the direct small-problem kernel,
+ * one of the two 3xTF32 kernels, or the scale-only kernel of alpha == 0 or
+ * K == 0.  "" before the thread's first launch.  Set when the launch is
+ * enqueued, not when it completes.  No GPU work.
+ */
+const char *sgemm_last_kernel(void);
+
+/*
  * sgemm_device_status -- synchronises `stream`, then reads and clears the
  * library's device-side error word for the current device.  Returns SGEMM_OK,
  * or SGEMM_ERR_TIMEOUT if a kernel gave up a bounded wait (it then wrote no

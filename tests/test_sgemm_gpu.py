@@ -453,3 +453,42 @@ def test_host_entry_point_k_chunks_with_beta_zero_never_read_c(tensor_cores):
     got = hC.numpy()
     assert not np.isnan(got).any()
     assert_within_bound(got[rows], ref, bound, "beta = 0 chunked host rows")
+
+
+def test_last_kernel_names_the_kernel_each_call_ran():
+    """sgemm_last_kernel reports the main kernel of the thread's last call: the
+    small-problem kernel, the few-tiles tile, the default tile, the tall-batch
+    and batched kernels of sgemm_ex, a 3xTF32 kernel, the scale-only kernel."""
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    binding.set_variant(-1)
+    dev = "cuda"
+
+    def run(M, N, K, alpha=1.0):
+        A = torch.ones((M, K), device=dev)
+        B = torch.ones((K, N), device=dev)
+        C = torch.zeros((M, N), device=dev)
+        binding.sgemm_into(A, B, C, alpha, 0.0)
+        torch.cuda.synchronize()
+        return binding.last_kernel()
+
+    assert run(256, 256, 256).startswith("direct small-problem kernel")
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert "tile=128x128x48" in run(1024, 1024, 1024)
+    assert "tile=256x128x64" in run(4096, 4096, 256)
+    assert run(300, 300, 300, alpha=0.0) == "scale only (C = beta * C)"
+    A3 = torch.ones((4, 512, 128), device=dev)
+    B3 = torch.ones((4, 128, 256), device=dev)
+    C3 = torch.zeros((4, 512, 256), device=dev)
+    binding.sgemm_ex_into(A3, B3, C3, 1.0, 0.0)
+    assert "tall_batch" in binding.last_kernel()
+    binding.sgemm_ex_into(A3, B3, C3, 1.0, 0.0, act="relu")
+    assert "batched+epilogue" in binding.last_kernel()
+    A = torch.ones((1024, 512), device=dev)
+    B = torch.ones((512, 1024), device=dev)
+    C = torch.zeros((1024, 1024), device=dev)
+    binding.sgemm_3xtf32_into(A, B, C, 1.0, 0.0)
+    torch.cuda.synchronize()
+    assert binding.last_kernel().startswith("3xtf32")
+    assert torch.all(C == 512.0)
+    assert torch.all(C3 == 128.0)
