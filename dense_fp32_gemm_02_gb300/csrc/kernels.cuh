@@ -527,6 +527,32 @@ __device__ __forceinline__ void store_tile(const float (&acc)[Cfg::TM][Cfg::TN],
     }
 }
 
+// The lines of C_in that the staged epilogue reads for this thread's warp
+// (rows roww .. roww + 4 * TM - 1 of its WN columns) started towards L2: lane
+// l takes row roww + l (and roww + l + 32, ...).  Issued when the warp starts
+// a tile, so the epilogue's first round finds them in L2 too.
+template <class Cfg>
+__device__ __forceinline__ void prefetch_c_tile_rows(const MainParams &p, int tm, int tn, int a_off,
+                                                     int b_off) {
+    constexpr int TM = Cfg::TM, WN = Cfg::WN, RH = WN / 32;
+    const int lane = threadIdx.x & 31;
+    const int rg = (a_off % Cfg::WM) >> 2, j = (b_off % WN) >> 2;
+    const int roww = tm * Cfg::BM + a_off - 4 * rg;
+    const int colw = tn * Cfg::BN + b_off - 4 * j;
+#pragma unroll
+    for (int i = 0; i < (4 * TM + 31) / 32; ++i) {
+        const int row = roww + lane + 32 * i;
+        if (lane + 32 * i < 4 * TM && row < p.M) {
+            const float *crow = p.C + (long long)row * p.ldc;
+#pragma unroll
+            for (int h = 0; h <= RH; ++h) {
+                const int col = min(colw + 32 * h, colw + WN - 1);
+                if (col < p.N) prefetch_l2(crow + col);
+            }
+        }
+    }
+}
+
 // The epilogue for C whose rows do not all start 16-byte aligned (ldc % 4 !=
 // 0, or C itself not 16-byte aligned): C = alpha * acc + beta * C for this
 // thread's outputs of tile (tm, tn); C is not read when beta == 0; rows >= M
@@ -541,8 +567,8 @@ __device__ __forceinline__ void store_tile(const float (&acc)[Cfg::TM][Cfg::TN],
 // row group of lanes, 4 rows apart) of WN columns; the lanes write them to the
 // area, read them back row by row, and every warp access to C then covers 128
 // contiguous bytes of one row.  C_in is read the same way, EPI_BATCH rounds
-// at a time, after every line of the warp's part of C_in has been started
-// towards L2.
+// at a time; every line of the warp's part of C_in was started towards L2
+// when the warp began the tile (prefetch_c_tile_rows).
 template <class Cfg>
 __device__ __forceinline__ void store_tile_staged(const float (&acc)[Cfg::TM][Cfg::TN],
                                                   const MainParams &p, int tm, int tn, int a_off,
@@ -557,22 +583,8 @@ __device__ __forceinline__ void store_tile_staged(const float (&acc)[Cfg::TM][Cf
     const int roww = tm * Cfg::BM + a_off - 4 * rg;                  // the warp's first row
     const int colw = tn * Cfg::BN + b_off - 4 * j;                   // and first column
     const float alpha = p.alpha, beta = p.beta;
-    if (beta != 0.0f) {
-        // the warp's rows are roww .. roww + 4 * TM - 1: lane l starts row
-        // roww + l (and roww + l + 32, ...) towards L2, every line it touches
-#pragma unroll
-        for (int i = 0; i < (4 * TM + 31) / 32; ++i) {
-            const int row = roww + lane + 32 * i;
-            if (lane + 32 * i < 4 * TM && row < p.M) {
-                const float *crow = p.C + (long long)row * p.ldc;
-#pragma unroll
-                for (int h = 0; h <= RH; ++h) {
-                    const int col = min(colw + 32 * h, colw + WN - 1);
-                    if (col < p.N) prefetch_l2(crow + col);
-                }
-            }
-        }
-    }
+    // (C_in's lines were started towards L2 when the warp began the tile:
+    // prefetch_c_tile_rows)
 #pragma unroll
     for (int g = 0; g < TM / RB; ++g) {
         const int s4 = (g * RB) / 4, r0 = (g * RB) % 4;
@@ -1005,6 +1017,16 @@ __device__ __forceinline__ void consumer_loop(const Ring<Cfg> &ring, const MainP
                     pieces +=
                         sk_start(b, p.sk_slabs, gridDim.x) < sk_start(b + 1, p.sk_slabs, gridDim.x);
                 fix.pieces = pieces;
+            }
+        }
+
+        if constexpr (Cfg::STAGED_EPI) {
+            if (p.beta != 0.0f) {
+                Segment seg;
+                segment_at(p, k_tiles, si, seg);
+                int tm, tn;
+                tile_coords(seg.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                prefetch_c_tile_rows<Cfg>(p, tm, tn, a_off(), b_off());
             }
         }
 
