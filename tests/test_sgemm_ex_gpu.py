@@ -234,3 +234,31 @@ def test_full_size_workload_sampled_rows(name):
         got = dC[b][torch.from_numpy(rows).cuda()].cpu().numpy()
         assert_within_bound(got, ref, bound, f"{name} batch {b}")
     assert torch.isfinite(dC).all()
+
+
+def test_batch_count_past_the_grid_limit():
+    """70,000 batches: past the 65,535 blocks a launch may have along z, so
+    the per-batch A transpose runs in two launches and the per-batch B copy
+    (rows of 5 floats, re-pitched) walks its batches in a grid-stride loop.
+    Integer inputs; up to 129 batches, those next to each launch's z range among
+    them, checked bit for bit against the oracle."""
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    batch, M, N, K = 70000, 3, 5, 7
+    rng = np.random.default_rng(31)
+    A = rng.integers(-4, 5, (batch, M, K)).astype(np.float32)
+    B = rng.integers(-4, 5, (batch, K, N)).astype(np.float32)
+    C = rng.integers(-4, 5, (batch, M, N)).astype(np.float32)
+    dA, dB, dC = (torch.from_numpy(x).cuda() for x in (A, B, C))
+    binding.sgemm_ex_into(dA, dB, dC, 1.5, 0.5)
+    torch.cuda.synchronize()
+    assert binding.device_status() == binding.SGEMM_OK
+    got = dC.cpu().numpy()
+    # the batches on both sides of each launch's z range, the first and the
+    # last, and a seeded sample of the rest (one oracle call per batch)
+    picks = sorted({0, 1, 65533, 65534, 65535, 65536, 65537, batch - 2, batch - 1}
+                   | set(rng.choice(batch, 120, replace=False).tolist()))
+    ref, _ = oracle.sgemm_batched([A[b] for b in picks], [B[b] for b in picks],
+                                  [C[b] for b in picks], 1.5, 0.5, None, "none", threads=1,
+                                  with_bound=False)
+    assert np.array_equal(got[picks], ref)
