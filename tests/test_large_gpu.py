@@ -81,3 +81,32 @@ def test_a_past_2_to_the_31_elements(cuda_device):
     ref, _ = oracle.sgemm(A_rows, B, None, 1.0, 0.0)
     got = dC[torch.from_numpy(rows).cuda()].cpu().numpy()
     assert np.array_equal(got, ref), "sampled rows differ from the oracle"
+
+
+@pytest.mark.parametrize("kind", ["tall", "batched"])
+def test_batched_output_past_2_to_the_31_elements(cuda_device, kind):
+    """12 batches of 4096 x 49152 (C 2.42e9 elements, 9.7 GB in all; element
+    2^31 lies in row 2730 of batch 10, and batch 11 starts past it).  Without an
+    activation the batch runs as one tall GEMM of 49152 rows; with ReLU it runs
+    the batched kernel.  Sampled rows (row 2730 among them) of the first, the
+    tenth and the last batch, bit-exact."""
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    batch, M, N, K = 12, 4096, 49152, 64
+    assert batch * M * N > 2 ** 31
+    dA = torch.stack([_device_pattern(M, K, 7 + b, 3, M) for b in range(batch)])
+    dB = torch.stack([_device_pattern(K, N, 5, 11 + b, K) for b in range(batch)])
+    dC = torch.full((batch, M, N), float("nan"), dtype=torch.float32, device="cuda")
+    act = "none" if kind == "tall" else "relu"
+    binding.sgemm_ex_into(dA, dB, dC, 1.5, 0.0, act=act)
+    torch.cuda.synchronize()
+    assert binding.device_status() == binding.SGEMM_OK
+    assert ("tall_batch" in binding.last_kernel()) == (kind == "tall")
+    rows = np.array([0, 1, 2730, 4095], np.int64)
+    for b in (0, 10, batch - 1):
+        A = _host_pattern(np.arange(M), K, 7 + b, 3)
+        B = _host_pattern(np.arange(K), N, 5, 11 + b)
+        ref, _ = oracle.sgemm_ex_rows(A, B, None, 1.5, 0.0, None, act, rows)
+        got = dC[b][torch.from_numpy(rows).cuda()].cpu().numpy()
+        assert np.array_equal(got, ref), f"{kind}: batch {b} sampled rows differ from the oracle"
+    del dC
