@@ -312,6 +312,117 @@ __global__ void __launch_bounds__(256)
     cluster_barrier();   // no CTA leaves while CTA 0 may still read its shared memory
 }
 
+// ------------------------------------------------------------------ skinny M
+// GEMMs with at most SKINNY_ROWS rows of A and C.  Every element of B is used
+// by M <= 32 FMAs only, so the work is bound by reading B once from HBM (at
+// M = 1 it is a vector-matrix product), not by the FMA units the tiled
+// kernels are built for.  Block (x, y) owns columns x * 256 * COLS + t + 256 q
+// (q < COLS) for thread t, so every warp load of B covers 128 contiguous
+// bytes of one row without any alignment rule, and the k range
+// [y * kchunk, min(K, (y + 1) * kchunk)): the grid's y dimension splits K so
+// that a few column blocks still fill every SM.  A's rows of each 128-deep
+// sub-range sit in shared memory, k-major, read by all threads at once (four
+// rows per 128-bit read).  MINB: blocks per SM the register allocation leaves
+// room for; UNR: k steps unrolled.  Each element sums its k terms in ascending order by fp32 FMAs;
+// with one k range the block applies alpha / beta and writes C, otherwise it
+// writes its partial sums to P (range y at P + y * M * N, row-major M x N)
+// and skinny_reduce_kernel adds the ranges in y order.
+constexpr int SKINNY_ROWS = 32;
+constexpr int SKINNY_THREADS = 256;
+constexpr int SKINNY_KSUB = 128;     // k values of A staged in shared memory at a time
+
+template <int MR, int COLS, int MINB, int UNR>
+__global__ void __launch_bounds__(SKINNY_THREADS, MINB)
+    sgemm_skinny_kernel(int M, int N, int K, int kchunk, float alpha, const float *__restrict__ A,
+                        long long lda, const float *__restrict__ B, long long ldb, float beta,
+                        float *__restrict__ C, long long ldc, float *__restrict__ P) {
+    // A's sub-range k-major: the MR values of one k are contiguous (128-bit reads)
+    __shared__ __align__(16) float As[SKINNY_KSUB][MR];
+    const int t = threadIdx.x;
+    const long long col0 = (long long)blockIdx.x * (SKINNY_THREADS * COLS) + t;
+    const int kb = int(blockIdx.y) * kchunk, ke = min(K, kb + kchunk);
+    float acc[MR][COLS];
+#pragma unroll
+    for (int i = 0; i < MR; ++i)
+#pragma unroll
+        for (int q = 0; q < COLS; ++q) acc[i][q] = 0.0f;
+    for (int k0 = kb; k0 < ke; k0 += SKINNY_KSUB) {
+        const int kn = min(SKINNY_KSUB, ke - k0);
+        __syncthreads();   // the previous sub-range's reads of As are done
+        for (int e = t; e < MR * SKINNY_KSUB; e += SKINNY_THREADS) {
+            const int i = e % MR, kk = e / MR;
+            As[kk][i] = (i < M && kk < kn) ? A[(long long)i * lda + k0 + kk] : 0.0f;
+        }
+        __syncthreads();
+        // UNR k steps in flight: UNR x COLS loads of B per thread
+#pragma unroll UNR
+        for (int kk = 0; kk < kn; ++kk) {
+            const float *brow = B + (long long)(k0 + kk) * ldb;
+            float b[COLS];
+#pragma unroll
+            for (int q = 0; q < COLS; ++q) {
+                const long long col = col0 + q * SKINNY_THREADS;
+                b[q] = col < N ? __ldcs(brow + col) : 0.0f;
+            }
+            if constexpr (MR % 4 == 0) {
+#pragma unroll
+                for (int i = 0; i < MR; i += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(&As[kk][i]);
+#pragma unroll
+                    for (int q = 0; q < COLS; ++q) {
+                        acc[i][q] = fmaf(a4.x, b[q], acc[i][q]);
+                        acc[i + 1][q] = fmaf(a4.y, b[q], acc[i + 1][q]);
+                        acc[i + 2][q] = fmaf(a4.z, b[q], acc[i + 2][q]);
+                        acc[i + 3][q] = fmaf(a4.w, b[q], acc[i + 3][q]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < MR; ++i) {
+                    const float a = As[kk][i];
+#pragma unroll
+                    for (int q = 0; q < COLS; ++q) acc[i][q] = fmaf(a, b[q], acc[i][q]);
+                }
+            }
+        }
+    }
+    const bool split = gridDim.y > 1;
+#pragma unroll
+    for (int i = 0; i < MR; ++i) {
+        if (i >= M) break;
+#pragma unroll
+        for (int q = 0; q < COLS; ++q) {
+            const long long col = col0 + q * SKINNY_THREADS;
+            if (col >= N) continue;
+            if (split) {
+                // range-checked build: the partial sum lies in P's S x M x N floats
+                const long long pi = ((long long)blockIdx.y * M + i) * N + col;
+                if (SG_IN_RANGE(pi < (long long)gridDim.y * M * N)) P[pi] = acc[i][q];
+            } else {
+                float *out = C + (long long)i * ldc + col;
+                *out = (beta != 0.0f) ? fmaf(alpha, acc[i][q], beta * *out) : alpha * acc[i][q];
+            }
+        }
+    }
+}
+
+// C[i][j] = alpha * (P_0 + P_1 + ... + P_{S-1})[i][j] + beta * C[i][j], the
+// ranges added in order (C not read when beta == 0).
+__global__ void __launch_bounds__(256)
+    skinny_reduce_kernel(int M, int N, int S, const float *__restrict__ P, float alpha, float beta,
+                         float *__restrict__ C, long long ldc) {
+    const long long total = (long long)M * N;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const long long i = e / N, j = e - i * N;
+        if (!SG_IN_RANGE(i < M && j < N)) continue;
+        float sum = P[e];
+        for (int y = 1; y < S; ++y) sum += P[(long long)y * total + e];
+        float *out = C + i * ldc + j;
+        *out = (beta != 0.0f) ? fmaf(alpha, sum, beta * *out) : alpha * sum;
+    }
+}
+
 // One thread waits on a barrier that nothing completes; the bounded wait must
 // expire, record ERR_SELFTEST and return.
 __global__ void wait_timeout_selftest_kernel(unsigned long long timeout_ns) {

@@ -45,6 +45,7 @@ constexpr const char *kSmallKernel32 = "direct small-problem kernel, 32x32 tiles
 constexpr const char *kSmallKernel64 = "direct small-problem kernel, 64x64 tiles";
 constexpr const char *kSmallSplitK = "direct small-problem kernel, 32x32 tiles, k split over a cluster";
 constexpr const char *kScaleOnly = "scale only (C = beta * C)";
+constexpr const char *kSkinny = "skinny-M kernel (B read once, k split over the grid)";
 constexpr const char *kT3Pair = "3xtf32 tcgen05 cta_group::2, 256x256 pair tiles";
 constexpr const char *kT3Single = "3xtf32 tcgen05, 128x256 tiles";
 
@@ -153,6 +154,15 @@ bool stream_k_pays(long long tiles, int sms) {
 // and more stay on the default tile (512x3001x1023: 0.090 against 0.095).
 // `sms` 0 (no device known) leaves this rule out.
 constexpr int kFewTilesVariant = 9;
+
+// Rows up to which a GEMM that is not a small problem takes the skinny-M
+// kernel (launch_skinny) instead of the persistent one.  Same box, main kernel
+// against the 128x128 tile the few-tiles rule would give: 1 x 8192 x 8192
+// 0.052 ms against 0.279, 16 x 8192 x 8192 0.104 against 0.276, 32 x 8192 x
+// 8192 0.216 against 0.278, 16 x 16384 x 2048 0.061 against 0.149, 32 x 3001
+// x 1023 0.029 against 0.055.  At 32 rows the margin at 8192^2 x 8192 is down
+// to 22 %, so the persistent kernel keeps 33 rows and more.
+constexpr int kSkinnyRows = sg::SKINNY_ROWS;
 
 int pick_variant(int M, int N, int K, int sms) {
     const int forced = g_forced_variant.load();
@@ -559,6 +569,71 @@ int launch_small(const GemmCall &g, cudaStream_t stream, int sms) {
     return e == cudaSuccess ? SGEMM_OK : cuda_fail(e);
 }
 
+// One instantiation of the skinny kernel: rows, columns per thread, blocks per
+// SM (the register budget: 65536 / (256 x MINB) per thread) and k steps
+// unrolled.  Chosen per row count by a sweep of 25 instantiations over
+// 4096^2 x 4096, 8192^2 x 8192, 16384 x 2048 x N and 3001 x 1023 x N shapes
+// (same box): M = 1 runs at 4.2-5.1 TB/s of B at the larger shapes.
+struct SkinnyConfig {
+    int rows, cols;
+    void (*kernel)(int, int, int, int, float, const float *, long long, const float *, long long,
+                   float, float *, long long, float *);
+};
+template <int MR, int COLS, int MINB, int UNR>
+constexpr SkinnyConfig skinny_config() {
+    return {MR, COLS, &sg::sgemm_skinny_kernel<MR, COLS, MINB, UNR>};
+}
+constexpr SkinnyConfig kSkinnyConfigs[] = {
+    skinny_config<1, 4, 4, 8>(), skinny_config<2, 4, 4, 4>(), skinny_config<4, 2, 4, 8>(),
+    skinny_config<8, 2, 4, 8>(), skinny_config<16, 2, 2, 8>(), skinny_config<32, 2, 1, 8>(),
+};
+// k-range split: about this many blocks per SM
+constexpr int kSkinnyBlocksPerSM = 4;
+
+// GEMMs of at most SKINNY_ROWS rows that are not small problems: B streamed
+// once by sgemm_skinny_kernel, the k range split so that about
+// kSkinnyBlocksPerSM blocks per SM run (whole 128-deep sub-ranges), partial
+// sums added in order by skinny_reduce_kernel.
+int launch_skinny(const GemmCall &g, cudaStream_t stream, DeviceState *dev) {
+    const int M = g.M, N = g.N, K = g.K;
+    const SkinnyConfig *cfg = &kSkinnyConfigs[0];
+    while (cfg->rows < M) ++cfg;
+    const long long block_cols = (long long)sg::SKINNY_THREADS * cfg->cols;
+    const long long col_blocks = (N + block_cols - 1) / block_cols;
+    const long long subs = (K + sg::SKINNY_KSUB - 1LL) / sg::SKINNY_KSUB;
+    const long long want = (long long)kSkinnyBlocksPerSM * dev->sm_count;
+    long long S = std::max(1LL, std::min(subs, (want + col_blocks - 1) / col_blocks));
+    const int kchunk = int(((subs + S - 1) / S) * sg::SKINNY_KSUB);
+    S = (K + kchunk - 1LL) / kchunk;
+    if (col_blocks > 0x7fffffffLL || S > 65535) return SGEMM_ERR_TOO_LARGE;
+    float *P = nullptr;
+    if (S > 1) {
+        cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&P),
+                                                size_t(S) * M * N * 4, dev->pool, stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    ProfCall prof(stream);
+    prof.main_begin();
+    const dim3 grid(static_cast<unsigned>(col_blocks), static_cast<unsigned>(S));
+    cfg->kernel<<<grid, sg::SKINNY_THREADS, 0, stream>>>(M, N, K, kchunk, g.alpha, g.A, g.lda, g.B,
+                                                         g.ldb, g.beta, g.C, g.ldc, P);
+    g_launches.fetch_add(1);
+    t_last_kernel = kSkinny;
+    if (S > 1) {
+        const long long total = (long long)M * N;
+        const int blocks = int(std::min<long long>((total + 255) / 256, (long long)dev->sm_count * 8));
+        sg::skinny_reduce_kernel<<<blocks, 256, 0, stream>>>(M, N, int(S), P, g.alpha, g.beta,
+                                                             g.C, g.ldc);
+        g_launches.fetch_add(1);
+    }
+    prof.main_end();
+    cudaError_t e = cudaGetLastError();
+    cudaError_t ef = S > 1 ? cudaFreeAsync(P, stream) : cudaSuccess;
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (ef != cudaSuccess) return cuda_fail(ef);
+    return SGEMM_OK;
+}
+
 int gemm_device(const GemmCall &g, cudaStream_t stream) {
     int st = checked_call(g);
     if (st != SGEMM_OK || g.M == 0 || g.N == 0 || g.batch == 0) return st;
@@ -571,9 +646,10 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
     const bool batched = g.batch > 1;
     const bool extended = batched || g.bias != nullptr || g.act != sg::ACT_NONE;
     const bool drop_test = !extended && g_drop_release.load() != 0;
-    if (!extended && !drop_test && g_forced_variant.load() < 0 &&
-        small_problem(M, N, K, dev->sm_count))
-        return launch_small(g, stream, dev->sm_count);
+    if (!extended && !drop_test && g_forced_variant.load() < 0) {
+        if (small_problem(M, N, K, dev->sm_count)) return launch_small(g, stream, dev->sm_count);
+        if (M <= kSkinnyRows) return launch_skinny(g, stream, dev);
+    }
     const bool tall = tall_batch_call(g);
     const Variant &var = tall ? tall_variant()
                          : batched ? ex_variant()

@@ -113,6 +113,11 @@ def main():
         ref, bound = oracle.sgemm_batched(As[:nb], Bs[:nb], Cs[:nb], 1.25, 0.5, bs[:nb], act)
         for b in range(nb):
             assert_within_bound(dC[b].cpu().numpy(), ref[b], bound[b], f"sgemm_ex {act} {b}")
+    # skinny rows: k split over the grid (partial sums), and one k range per
+    # block (N wide enough for every SM); odd pitches and misaligned pointers
+    plain(5, 3001, 1023, 1.5, 0.5, "skinny 5x3001x1023", exact=True, offsets=(1, 3, 2))
+    plain(32, 2049, 777, 1.5, 0.5, "skinny 32x2049x777", exact=True)
+    plain(4, 320000, 64, 1.5, 0.5, "skinny one k range", exact=True)
     # batches run as one tall GEMM: contiguous B (48 tiles, all by stream-K),
     # and B re-pitched (rows of 203 floats) under a C with a padded pitch
     for batch, M, N, K, ldc in ((3, 512, 1000, 512, 1000), (2, 768, 203, 192, 207)):

@@ -492,3 +492,70 @@ def test_last_kernel_names_the_kernel_each_call_ran():
     assert binding.last_kernel().startswith("3xtf32")
     assert torch.all(C == 512.0)
     assert torch.all(C3 == 128.0)
+
+
+# GEMMs of at most 32 rows (above the small-problem threshold) run the
+# skinny-M kernel: B streamed once, the k range split over the grid and the
+# partial sums added in order.  17 rows is just past the 16-row configuration;
+# 33 rows is past the skinny range and runs the persistent kernel.
+SKINNY_M = [1, 2, 3, 4, 5, 8, 9, 16, 17, 31, 32, 33]
+SKINNY_NK = [(3001, 1023), (1000, 5000), (300, 4100)]
+
+
+@pytest.mark.parametrize("N,K", SKINNY_NK)
+def test_skinny_rows_bit_exact_on_integer_inputs(N, K):
+    from dense_fp32_gemm_02_gb300 import binding
+    binding.set_variant(-1)
+    for M in SKINNY_M:
+        A, B, C = make_inputs(M, N, K, "int4", "int4", "int4", seed=41 + M + N)
+        ref, _ = oracle.sgemm(A, B, C, 1.5, 0.5)
+        got = run_gpu(A, B, C, 1.5, 0.5).cpu().numpy()
+        assert np.array_equal(got, ref), (M, N, K)
+        assert ("skinny" in binding.last_kernel()) == (M <= 32), (M, binding.last_kernel())
+
+
+@pytest.mark.parametrize("M", [1, 7, 16, 32])
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (-0.75, 1.25)])
+def test_skinny_rows_random_parity(M, alpha, beta):
+    N, K = 2500, 3000
+    A, B, C = make_inputs(M, N, K, "upm1", "normal", "normal", seed=42 + M)
+    ref, bound = oracle.sgemm(A, B, C if beta != 0 else None, alpha, beta)
+    got = run_gpu(A, B, C if beta != 0 else None, alpha, beta).cpu().numpy()
+    assert_within_bound(got, ref, bound, f"skinny {M}x{N}x{K} a={alpha} b={beta}")
+
+
+@pytest.mark.parametrize("offsets,ldc_pad", [((1, 3, 2), 0), ((0, 0, 0), 5), ((3, 1, 0), 3)])
+def test_skinny_rows_misaligned_and_padded(offsets, ldc_pad):
+    """Pointers off 16-byte boundaries, odd pitches and a padded C: the skinny
+    kernel has no alignment rule, and C's padding columns stay untouched."""
+    import torch
+    from _helpers import to_device
+    from dense_fp32_gemm_02_gb300 import binding
+    M, N, K = 6, 2049, 1537
+    A, B, C = make_inputs(M, N, K, "int4", "int4", "int4", seed=43)
+    ref, _ = oracle.sgemm(A, B, C, 1.5, 0.5)
+    dA = to_device(A, offset_elems=offsets[0])
+    dB = to_device(B, offset_elems=offsets[1])
+    full = torch.full((M, N + ldc_pad + offsets[2]), 777.0, device="cuda")
+    full[:, offsets[2]:offsets[2] + N] = torch.from_numpy(C).cuda()
+    dC = full[:, offsets[2]:offsets[2] + N]
+    binding.sgemm_into(dA, dB, dC, 1.5, 0.5)
+    torch.cuda.synchronize()
+    assert "skinny" in binding.last_kernel()
+    assert np.array_equal(dC.cpu().numpy(), ref)
+    rest = torch.cat([full[:, :offsets[2]], full[:, offsets[2] + N:]], dim=1)
+    assert bool((rest == 777.0).all()), "columns outside C written"
+
+
+def test_skinny_rows_one_k_range_and_nan_c():
+    """N wide enough that every SM gets column blocks without splitting K: the
+    blocks write C themselves (no partial sums); beta 0 leaves NaN in C_in
+    unread."""
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    M, N, K = 4, 320000, 100
+    A, B, _ = make_inputs(M, N, K, "int4", "int4", "int4", seed=44)
+    ref, _ = oracle.sgemm(A, B, None, 2.0, 0.0)
+    got = run_gpu(A, B, None, 2.0, 0.0).cpu().numpy()
+    assert "skinny" in binding.last_kernel()
+    assert np.array_equal(got, ref)
