@@ -406,6 +406,82 @@ __global__ void __launch_bounds__(SKINNY_THREADS, MINB)
     }
 }
 
+// ------------------------------------------------------------------ skinny N
+// GEMMs with at most SKINNY_COLS_MAX columns of B and C (at N = 1 a
+// matrix-vector product): A, M x K, is the operand read once from HBM, and a
+// tiled kernel would pad N up to its 128-column tile and transpose all of A
+// first.  Block (x, y) owns rows x * 256 .. x * 256 + 255, one per thread, and
+// the k range [y * kchunk, min(K, (y + 1) * kchunk)).  Per 32-deep step the
+// block stages its rows of A in shared memory (each warp reads one row's 128
+// contiguous bytes; no alignment rule) and B's 32 x N values k-major, then
+// each thread adds its row's 32 terms to its NR accumulators in k order, B
+// read four columns at a time (the same address for every thread).  Output
+// as in sgemm_skinny_kernel: alpha / beta into C with one k range, partial
+// sums to P (range y at P + y * M * N) otherwise.
+constexpr int SKINNY_COLS_MAX = 32;
+constexpr int SKINNY_N_ROWS = 256;   // rows per block, one per thread
+constexpr int SKINNY_N_KC = 32;      // k values per staged step
+
+template <int NR>
+__global__ void __launch_bounds__(SKINNY_N_ROWS)
+    sgemm_skinny_n_kernel(int M, int N, int K, int kchunk, float alpha, const float *__restrict__ A,
+                          long long lda, const float *__restrict__ B, long long ldb, float beta,
+                          float *__restrict__ C, long long ldc, float *__restrict__ P) {
+    static_assert(NR % 4 == 0, "B is read four columns at a time");
+    __shared__ float As[SKINNY_N_ROWS][SKINNY_N_KC + 1];        // +1: rows in distinct banks
+    __shared__ __align__(16) float Bs[SKINNY_N_KC][NR];
+    const int t = threadIdx.x;
+    const long long row0 = (long long)blockIdx.x * SKINNY_N_ROWS;
+    const int kb = int(blockIdx.y) * kchunk, ke = min(K, kb + kchunk);
+    float acc[NR];
+#pragma unroll
+    for (int j = 0; j < NR; ++j) acc[j] = 0.0f;
+    for (int k0 = kb; k0 < ke; k0 += SKINNY_N_KC) {
+        const int kn = min(SKINNY_N_KC, ke - k0);
+        __syncthreads();   // the previous step's reads of As and Bs are done
+        // warp w loads rows w, w + 8, ...: lane l takes column k0 + l (all 32
+        // loads of a thread in flight at once)
+#pragma unroll
+        for (int r = t / 32; r < SKINNY_N_ROWS; r += SKINNY_N_ROWS / 32) {
+            const int kk = t % 32;
+            const long long row = row0 + r;
+            As[r][kk] = (row < M && kk < kn) ? __ldcs(A + row * lda + k0 + kk) : 0.0f;
+        }
+        for (int e = t; e < SKINNY_N_KC * NR; e += SKINNY_N_ROWS) {
+            const int kk = e / NR, j = e % NR;
+            Bs[kk][j] = (kk < kn && j < N) ? B[(long long)(k0 + kk) * ldb + j] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < SKINNY_N_KC; ++kk) {
+            const float a = As[t][kk];
+#pragma unroll
+            for (int j = 0; j < NR; j += 4) {
+                const float4 b4 = *reinterpret_cast<const float4 *>(&Bs[kk][j]);
+                acc[j] = fmaf(a, b4.x, acc[j]);
+                acc[j + 1] = fmaf(a, b4.y, acc[j + 1]);
+                acc[j + 2] = fmaf(a, b4.z, acc[j + 2]);
+                acc[j + 3] = fmaf(a, b4.w, acc[j + 3]);
+            }
+        }
+    }
+    const long long row = row0 + t;
+    if (row >= M) return;
+    const bool split = gridDim.y > 1;
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+        if (j >= N) break;
+        if (split) {
+            // range-checked build: the partial sum lies in P's S x M x N floats
+            const long long pi = ((long long)blockIdx.y * M + row) * N + j;
+            if (SG_IN_RANGE(pi < (long long)gridDim.y * M * N)) P[pi] = acc[j];
+        } else {
+            float *out = C + row * ldc + j;
+            *out = (beta != 0.0f) ? fmaf(alpha, acc[j], beta * *out) : alpha * acc[j];
+        }
+    }
+}
+
 // C[i][j] = alpha * (P_0 + P_1 + ... + P_{S-1})[i][j] + beta * C[i][j], the
 // ranges added in order (C not read when beta == 0).
 __global__ void __launch_bounds__(256)

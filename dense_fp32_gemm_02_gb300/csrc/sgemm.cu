@@ -46,6 +46,7 @@ constexpr const char *kSmallKernel64 = "direct small-problem kernel, 64x64 tiles
 constexpr const char *kSmallSplitK = "direct small-problem kernel, 32x32 tiles, k split over a cluster";
 constexpr const char *kScaleOnly = "scale only (C = beta * C)";
 constexpr const char *kSkinny = "skinny-M kernel (B read once, k split over the grid)";
+constexpr const char *kSkinnyN = "skinny-N kernel (A read once, k split over the grid)";
 constexpr const char *kT3Pair = "3xtf32 tcgen05 cta_group::2, 256x256 pair tiles";
 constexpr const char *kT3Single = "3xtf32 tcgen05, 128x256 tiles";
 
@@ -163,6 +164,8 @@ constexpr int kFewTilesVariant = 9;
 // x 1023 0.029 against 0.055.  At 32 rows the margin at 8192^2 x 8192 is down
 // to 22 %, so the persistent kernel keeps 33 rows and more.
 constexpr int kSkinnyRows = sg::SKINNY_ROWS;
+// Columns up to which such a GEMM takes the skinny-N kernel (launch_skinny_n).
+constexpr int kSkinnyCols = sg::SKINNY_COLS_MAX;
 
 int pick_variant(int M, int N, int K, int sms) {
     const int forced = g_forced_variant.load();
@@ -517,24 +520,39 @@ bool small_problem(int M, int N, int K, int sms) {
     return tiles * ((K + 63LL) / 64) < sms;
 }
 
-int launch_small(const GemmCall &g, cudaStream_t stream, int sms) {
-    const long long t64 = ((g.M + 63LL) / 64) * ((g.N + 63LL) / 64);
-    const long long t32 = ((g.M + 31LL) / 32) * ((g.N + 31LL) / 32);
-    ProfCall prof(stream);
-    prof.main_begin();
-    // With 32x32 tiles that fill at most half the SMs, the k range of a tile
-    // is split over the CTAs of a cluster (S <= 8, at least two k steps of 32
-    // each): 256^3 runs 64 tiles x 4 CTAs instead of 64 CTAs walking all of K.
-    int S = 1, kchunk = g.K;
+// The small-problem kernel's configuration: 64x64 tiles when they fill at
+// least the SMs, else 32x32 tiles; with 32x32 tiles that fill at most half
+// the SMs, the k range of a tile is split over the CTAs of a cluster (S <= 8,
+// at least two k steps of 32 each): 256^3 runs 64 tiles x 4 CTAs instead of
+// 64 CTAs walking all of K.
+struct SmallSplit {
+    int tile, S, kchunk;
+};
+SmallSplit small_split(int M, int N, int K, int sms) {
+    const long long t64 = ((M + 63LL) / 64) * ((N + 63LL) / 64);
+    const long long t32 = ((M + 31LL) / 32) * ((N + 31LL) / 32);
+    SmallSplit r{t64 < sms ? 32 : 64, 1, K};
     if (t64 < sms && 2 * t32 <= sms) {
         const int by_sms = int(std::min<long long>(8, (2LL * sms) / t32));
-        const int by_k = (g.K + 2 * sg::SMALL_BK - 1) / (2 * sg::SMALL_BK);
-        S = std::max(1, std::min(by_sms, by_k));
-        if (S > 1) {
-            kchunk = int(round_up((g.K + S - 1) / S, sg::SMALL_BK));
-            S = (g.K + kchunk - 1) / kchunk;
+        const int by_k = (K + 2 * sg::SMALL_BK - 1) / (2 * sg::SMALL_BK);
+        r.S = std::max(1, std::min(by_sms, by_k));
+        if (r.S > 1) {
+            r.kchunk = int(round_up((K + r.S - 1) / r.S, sg::SMALL_BK));
+            r.S = (K + r.kchunk - 1) / r.kchunk;
         }
     }
+    return r;
+}
+
+const char *small_kernel_text(const SmallSplit &sp) {
+    return sp.S > 1 ? kSmallSplitK : sp.tile == 32 ? kSmallKernel32 : kSmallKernel64;
+}
+
+int launch_small(const GemmCall &g, cudaStream_t stream, int sms) {
+    ProfCall prof(stream);
+    prof.main_begin();
+    const SmallSplit sp = small_split(g.M, g.N, g.K, sms);
+    const int S = sp.S, kchunk = sp.kchunk;
     if (S > 1) {
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof(cfg));
@@ -552,7 +570,7 @@ int launch_small(const GemmCall &g, cudaStream_t stream, int sms) {
         cudaLaunchKernelEx(&cfg, sg::sgemm_small_splitk_kernel<32>, g.M, g.N, g.K, kchunk, g.alpha,
                            g.A, (long long)g.lda, g.B, (long long)g.ldb, g.beta, g.C,
                            (long long)g.ldc);
-    } else if (t64 < sms) {
+    } else if (sp.tile == 32) {
         dim3 grid(unsigned((g.N + 31) / 32), unsigned((g.M + 31) / 32));
         t_last_kernel = kSmallKernel32;
         sg::sgemm_small_kernel<32><<<grid, 256, 0, stream>>>(g.M, g.N, g.K, g.alpha, g.A, g.lda, g.B,
@@ -634,6 +652,51 @@ int launch_skinny(const GemmCall &g, cudaStream_t stream, DeviceState *dev) {
     return SGEMM_OK;
 }
 
+// GEMMs of at most SKINNY_COLS_MAX columns that are not small problems (nor
+// skinny in M): A streamed once by sgemm_skinny_n_kernel, 256 rows per block,
+// the k range split so that about kSkinnyBlocksPerSM blocks per SM run, partial
+// sums added in order by skinny_reduce_kernel.
+int launch_skinny_n(const GemmCall &g, cudaStream_t stream, DeviceState *dev) {
+    const int M = g.M, N = g.N, K = g.K;
+    const long long row_blocks = (M + sg::SKINNY_N_ROWS - 1LL) / sg::SKINNY_N_ROWS;
+    const long long steps = (K + sg::SKINNY_N_KC - 1LL) / sg::SKINNY_N_KC;
+    const long long want = (long long)kSkinnyBlocksPerSM * dev->sm_count;
+    long long S = std::max(1LL, std::min(steps, (want + row_blocks - 1) / row_blocks));
+    const int kchunk = int(((steps + S - 1) / S) * sg::SKINNY_N_KC);
+    S = (K + kchunk - 1LL) / kchunk;
+    if (row_blocks > 0x7fffffffLL || S > 65535) return SGEMM_ERR_TOO_LARGE;
+    float *P = nullptr;
+    if (S > 1) {
+        cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&P),
+                                                size_t(S) * M * N * 4, dev->pool, stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    ProfCall prof(stream);
+    prof.main_begin();
+    const dim3 grid(static_cast<unsigned>(row_blocks), static_cast<unsigned>(S));
+    auto kernel = N <= 4 ? &sg::sgemm_skinny_n_kernel<4>
+                  : N <= 8 ? &sg::sgemm_skinny_n_kernel<8>
+                  : N <= 16 ? &sg::sgemm_skinny_n_kernel<16>
+                            : &sg::sgemm_skinny_n_kernel<32>;
+    kernel<<<grid, sg::SKINNY_N_ROWS, 0, stream>>>(M, N, K, kchunk, g.alpha, g.A, g.lda, g.B, g.ldb,
+                                                  g.beta, g.C, g.ldc, P);
+    g_launches.fetch_add(1);
+    t_last_kernel = kSkinnyN;
+    if (S > 1) {
+        const long long total = (long long)M * N;
+        const int blocks = int(std::min<long long>((total + 255) / 256, (long long)dev->sm_count * 8));
+        sg::skinny_reduce_kernel<<<blocks, 256, 0, stream>>>(M, N, int(S), P, g.alpha, g.beta,
+                                                             g.C, g.ldc);
+        g_launches.fetch_add(1);
+    }
+    prof.main_end();
+    cudaError_t e = cudaGetLastError();
+    cudaError_t ef = S > 1 ? cudaFreeAsync(P, stream) : cudaSuccess;
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (ef != cudaSuccess) return cuda_fail(ef);
+    return SGEMM_OK;
+}
+
 int gemm_device(const GemmCall &g, cudaStream_t stream) {
     int st = checked_call(g);
     if (st != SGEMM_OK || g.M == 0 || g.N == 0 || g.batch == 0) return st;
@@ -649,6 +712,7 @@ int gemm_device(const GemmCall &g, cudaStream_t stream) {
     if (!extended && !drop_test && g_forced_variant.load() < 0) {
         if (small_problem(M, N, K, dev->sm_count)) return launch_small(g, stream, dev->sm_count);
         if (M <= kSkinnyRows) return launch_skinny(g, stream, dev);
+        if (N <= kSkinnyCols) return launch_skinny_n(g, stream, dev);
     }
     const bool tall = tall_batch_call(g);
     const Variant &var = tall ? tall_variant()
@@ -1467,13 +1531,19 @@ SGEMM_API int sgemm_profile_collect(double *main_ms, long long *main_launches, d
 SGEMM_API long long sgemm_kernel_launch_count(void) { return g_launches.load(); }
 
 SGEMM_API const char *sgemm_config_string(int M, int N, int K) {
-    // with a device, its SM count picks the tile for few-tile shapes, and the
+    // with a device, its SM count decides between the direct kernels and the
+    // tiled ones (as sgemm() does), picks the tile for few-tile shapes, and the
     // text says when the work split leaves the stream-K tail out
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         cudaGetLastError();   // the failure just caused here (no device) is not kept
         sms = 0;
+    }
+    if (sms > 0 && g_forced_variant.load() < 0 && M > 0 && N > 0 && K > 0) {
+        if (small_problem(M, N, K, sms)) return small_kernel_text(small_split(M, N, K, sms));
+        if (M <= kSkinnyRows) return kSkinny;
+        if (N <= kSkinnyCols) return kSkinnyN;
     }
     const Variant &v = variant_at(pick_variant(M, N, K, sms));
     if (!v.stream_k || M <= 0 || N <= 0) return v.name;

@@ -290,9 +290,16 @@ long long sgemm_kernel_launch_count(void);
  * sgemm_config_string -- the kernel configuration sgemm() would pick for the
  * given shape (tile sizes, stages, micro-kernel, work split), as text that
  * stays valid until the calling thread's next call.  With a CUDA device
- * current, it also says when the work split on that device leaves out the
- * stream-K tail (whole tiles alone would leave under 1 % of the SMs' slots
- * idle).  No GPU work.
+ * current, the choice is the one sgemm() makes on that device: the direct
+ * small-problem kernel for problems of fewer 256x128 tile slabs than SMs, the
+ * skinny-M kernel for at most 32 rows, the skinny-N kernel for at most 32
+ * columns, else a tiled variant (the 128x128 tile when the default tile makes
+ * fewer tiles than a quarter of the SMs; C whose rows are not all 16-byte
+ * aligned, read with beta != 0, takes the same tile with its staged epilogue,
+ * which the shape alone does not show); the text also says when the work
+ * split leaves out the stream-K tail (whole tiles alone would leave under 1 %
+ * of the SMs' slots idle).  Without a device: the tiled variant for the
+ * shape.  No GPU work.
  */
 const char *sgemm_config_string(int M, int N, int K);
 

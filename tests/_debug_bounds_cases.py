@@ -118,6 +118,9 @@ def main():
     plain(5, 3001, 1023, 1.5, 0.5, "skinny 5x3001x1023", exact=True, offsets=(1, 3, 2))
     plain(32, 2049, 777, 1.5, 0.5, "skinny 32x2049x777", exact=True)
     plain(4, 320000, 64, 1.5, 0.5, "skinny one k range", exact=True)
+    plain(3001, 5, 1023, 1.5, 0.5, "skinny-N 3001x5x1023", exact=True, offsets=(1, 3, 2))
+    plain(2049, 32, 777, 1.5, 0.5, "skinny-N 2049x32x777", exact=True)
+    plain(160000, 4, 64, 1.5, 0.5, "skinny-N one k range", exact=True)
     # batches run as one tall GEMM: contiguous B (48 tiles, all by stream-K),
     # and B re-pitched (rows of 203 floats) under a C with a padded pitch
     for batch, M, N, K, ldc in ((3, 512, 1000, 512, 1000), (2, 768, 203, 192, 207)):

@@ -133,8 +133,8 @@ def test_small_problem_k_split_over_clusters(M, N, K):
 # Shapes whose chosen orientation of the default tile makes fewer tiles than a
 # quarter of the SMs run the 128x128x48 tile (variant 9): twice the tiles, so
 # stream-K cuts each into half as many pieces.  All of these are above the
-# small-problem kernel's threshold.
-FEW_TILE_SHAPES = [(1024, 1024, 1024), (768, 768, 768), (1, 3001, 1023), (256, 3001, 1023),
+# small-problem kernel's threshold and have more than 32 rows and columns.
+FEW_TILE_SHAPES = [(1024, 1024, 1024), (768, 768, 768), (64, 3001, 1023), (256, 3001, 1023),
                    (512, 512, 2048), (130, 700, 4000)]
 
 
@@ -559,3 +559,87 @@ def test_skinny_rows_one_k_range_and_nan_c():
     got = run_gpu(A, B, None, 2.0, 0.0).cpu().numpy()
     assert "skinny" in binding.last_kernel()
     assert np.array_equal(got, ref)
+
+
+# GEMMs of at most 32 columns (above the small-problem threshold, more than 32
+# rows) run the skinny-N kernel: A streamed once, 256 rows per block, the k
+# range split over the grid and the partial sums added in order.  33 columns
+# runs the persistent kernel.
+SKINNY_N = [1, 2, 3, 4, 5, 8, 9, 16, 17, 31, 32, 33]
+SKINNY_MK = [(3001, 1023), (5000, 1000), (600, 4100)]
+
+
+@pytest.mark.parametrize("M,K", SKINNY_MK)
+def test_skinny_columns_bit_exact_on_integer_inputs(M, K):
+    from dense_fp32_gemm_02_gb300 import binding
+    binding.set_variant(-1)
+    for N in SKINNY_N:
+        A, B, C = make_inputs(M, N, K, "int4", "int4", "int4", seed=51 + M + N)
+        ref, _ = oracle.sgemm(A, B, C, 1.5, 0.5)
+        got = run_gpu(A, B, C, 1.5, 0.5).cpu().numpy()
+        assert np.array_equal(got, ref), (M, N, K)
+        assert ("skinny-N" in binding.last_kernel()) == (N <= 32), (N, binding.last_kernel())
+
+
+@pytest.mark.parametrize("N", [1, 7, 16, 32])
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (-0.75, 1.25)])
+def test_skinny_columns_random_parity(N, alpha, beta):
+    M, K = 2500, 3000
+    A, B, C = make_inputs(M, N, K, "upm1", "normal", "normal", seed=52 + N)
+    ref, bound = oracle.sgemm(A, B, C if beta != 0 else None, alpha, beta)
+    got = run_gpu(A, B, C if beta != 0 else None, alpha, beta).cpu().numpy()
+    assert_within_bound(got, ref, bound, f"skinny-N {M}x{N}x{K} a={alpha} b={beta}")
+
+
+@pytest.mark.parametrize("offsets,ldc_pad", [((1, 3, 2), 0), ((0, 0, 0), 5), ((3, 1, 0), 3)])
+def test_skinny_columns_misaligned_and_padded(offsets, ldc_pad):
+    import torch
+    from _helpers import to_device
+    from dense_fp32_gemm_02_gb300 import binding
+    M, N, K = 2049, 6, 1537
+    A, B, C = make_inputs(M, N, K, "int4", "int4", "int4", seed=53)
+    ref, _ = oracle.sgemm(A, B, C, 1.5, 0.5)
+    dA = to_device(A, offset_elems=offsets[0])
+    dB = to_device(B, offset_elems=offsets[1])
+    full = torch.full((M, N + ldc_pad + offsets[2]), 777.0, device="cuda")
+    full[:, offsets[2]:offsets[2] + N] = torch.from_numpy(C).cuda()
+    dC = full[:, offsets[2]:offsets[2] + N]
+    binding.sgemm_into(dA, dB, dC, 1.5, 0.5)
+    torch.cuda.synchronize()
+    assert "skinny-N" in binding.last_kernel()
+    assert np.array_equal(dC.cpu().numpy(), ref)
+    rest = torch.cat([full[:, :offsets[2]], full[:, offsets[2] + N:]], dim=1)
+    assert bool((rest == 777.0).all()), "columns outside C written"
+
+
+def test_skinny_columns_one_k_range_and_nan_c():
+    """M tall enough that every SM gets row blocks without splitting K: the
+    blocks write C themselves; beta 0 leaves NaN in C_in unread."""
+    from dense_fp32_gemm_02_gb300 import binding
+    M, N, K = 160000, 4, 64
+    A, B, _ = make_inputs(M, N, K, "int4", "int4", "int4", seed=54)
+    ref, _ = oracle.sgemm(A, B, None, 2.0, 0.0)
+    got = run_gpu(A, B, None, 2.0, 0.0).cpu().numpy()
+    assert "skinny-N" in binding.last_kernel()
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (64, 64, 200), (8, 3001, 1023), (3001, 8, 1023),
+                                   (1024, 1024, 1024), (4096, 4096, 256), (4097, 3001, 1023),
+                                   (16384, 16384, 64)])
+def test_config_string_names_the_kernel_sgemm_runs(M, N, K):
+    """With a device, sgemm_config_string makes the choice sgemm() makes: the
+    text names the kernel that the call then records as launched.  (beta 0:
+    the staged-epilogue form, which depends on C's alignment and beta, is
+    outside what the shape alone decides.)"""
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    binding.set_variant(-1)
+    A = torch.ones((M, K), device="cuda")
+    B = torch.ones((K, N), device="cuda")
+    C = torch.full((M, N), float("nan"), device="cuda")
+    binding.sgemm_into(A, B, C, 1.0, 0.0)
+    torch.cuda.synchronize()
+    assert binding.config_string(M, N, K).startswith(binding.last_kernel()), (
+        binding.config_string(M, N, K), binding.last_kernel())
+    assert bool((C == K).all())
