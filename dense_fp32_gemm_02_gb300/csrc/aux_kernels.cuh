@@ -410,16 +410,17 @@ __global__ void __launch_bounds__(SKINNY_THREADS, MINB)
 // GEMMs with at most SKINNY_COLS_MAX columns of B and C (at N = 1 a
 // matrix-vector product): A, M x K, is the operand read once from HBM, and a
 // tiled kernel would pad N up to its 128-column tile and transpose all of A
-// first.  Block (x, y) owns rows x * 256 .. x * 256 + 255, one per thread, and
-// the k range [y * kchunk, min(K, (y + 1) * kchunk)).  Per 32-deep step the
-// block stages its rows of A in shared memory (each warp reads one row's 128
-// contiguous bytes; no alignment rule) and B's 32 x N values k-major, then
-// each thread adds its row's 32 terms to its NR accumulators in k order, B
-// read four columns at a time (the same address for every thread).  Output
-// as in sgemm_skinny_kernel: alpha / beta into C with one k range, partial
-// sums to P (range y at P + y * M * N) otherwise.
+// first.  Block (x, y) owns rows x * 128 .. x * 128 + 127, one per thread, and
+// the k range [y * kchunk, min(K, (y + 1) * kchunk)).  Its 32-deep steps of A
+// (each warp copies one row's 128 contiguous bytes at a time; no alignment
+// rule) and of B (k-major) go into shared memory by asynchronous copies, two
+// steps in flight: the next step is being copied while the threads add this
+// step's 32 terms of their row to their NR accumulators in k order, B read
+// four columns at a time (the same address for every thread).  Output as in
+// sgemm_skinny_kernel: alpha / beta into C with one k range, partial sums to
+// P (range y at P + y * M * N) otherwise.
 constexpr int SKINNY_COLS_MAX = 32;
-constexpr int SKINNY_N_ROWS = 256;   // rows per block, one per thread
+constexpr int SKINNY_N_ROWS = 128;   // rows per block, one per thread
 constexpr int SKINNY_N_KC = 32;      // k values per staged step
 
 template <int NR>
@@ -428,43 +429,59 @@ __global__ void __launch_bounds__(SKINNY_N_ROWS)
                           long long lda, const float *__restrict__ B, long long ldb, float beta,
                           float *__restrict__ C, long long ldc, float *__restrict__ P) {
     static_assert(NR % 4 == 0, "B is read four columns at a time");
-    __shared__ float As[SKINNY_N_ROWS][SKINNY_N_KC + 1];        // +1: rows in distinct banks
-    __shared__ __align__(16) float Bs[SKINNY_N_KC][NR];
-    const int t = threadIdx.x;
-    const long long row0 = (long long)blockIdx.x * SKINNY_N_ROWS;
+    constexpr int KC = SKINNY_N_KC, ROWS = SKINNY_N_ROWS;
+    __shared__ float As[2][ROWS][KC + 1];                 // +1: rows in distinct banks
+    __shared__ __align__(16) float Bs[2][KC][NR];
+    const int t = threadIdx.x, lane = t % 32, warp = t / 32;
+    const long long row0 = (long long)blockIdx.x * ROWS;
     const int kb = int(blockIdx.y) * kchunk, ke = min(K, kb + kchunk);
+    const int steps = (ke - kb + KC - 1) / KC;
+    // copies of step s into buffer s % 2: warp w takes rows w, w + 4, ...,
+    // lane l column k0 + l; past M or the k range the copy reads nothing and
+    // zero-fills (its source address stays A's or B's first element)
+    auto issue = [&](int s) {
+        const int k0 = kb + s * KC, buf = s & 1;
+        const int kn = min(KC, ke - k0);
+#pragma unroll
+        for (int r = warp; r < ROWS; r += ROWS / 32) {
+            const long long row = row0 + r;
+            const bool ok = row < M && lane < kn;
+            cp_async4(smem_addr(&As[buf][r][lane]), ok ? A + row * lda + k0 + lane : A,
+                      ok ? 4u : 0u);
+        }
+        for (int e = t; e < KC * NR; e += ROWS) {
+            const int kk = e / NR, j = e % NR;
+            const bool ok = kk < kn && j < N;
+            cp_async4(smem_addr(&Bs[buf][kk][j]), ok ? B + (long long)(k0 + kk) * ldb + j : B,
+                      ok ? 4u : 0u);
+        }
+    };
     float acc[NR];
 #pragma unroll
     for (int j = 0; j < NR; ++j) acc[j] = 0.0f;
-    for (int k0 = kb; k0 < ke; k0 += SKINNY_N_KC) {
-        const int kn = min(SKINNY_N_KC, ke - k0);
-        __syncthreads();   // the previous step's reads of As and Bs are done
-        // warp w loads rows w, w + 8, ...: lane l takes column k0 + l (all 32
-        // loads of a thread in flight at once)
-#pragma unroll
-        for (int r = t / 32; r < SKINNY_N_ROWS; r += SKINNY_N_ROWS / 32) {
-            const int kk = t % 32;
-            const long long row = row0 + r;
-            As[r][kk] = (row < M && kk < kn) ? __ldcs(A + row * lda + k0 + kk) : 0.0f;
-        }
-        for (int e = t; e < SKINNY_N_KC * NR; e += SKINNY_N_ROWS) {
-            const int kk = e / NR, j = e % NR;
-            Bs[kk][j] = (kk < kn && j < N) ? B[(long long)(k0 + kk) * ldb + j] : 0.0f;
-        }
-        __syncthreads();
+    if (steps > 0) issue(0);
+    cp_async_commit();
+    for (int s = 0; s < steps; ++s) {
+        if (s + 1 < steps) issue(s + 1);
+        cp_async_commit();
+        cp_async_wait<1>();   // step s has landed (this thread's copies)
+        __syncthreads();      // and every other thread's
+        const int buf = s & 1;
 #pragma unroll 8
-        for (int kk = 0; kk < SKINNY_N_KC; ++kk) {
-            const float a = As[t][kk];
+        for (int kk = 0; kk < KC; ++kk) {
+            const float a = As[buf][t][kk];
 #pragma unroll
             for (int j = 0; j < NR; j += 4) {
-                const float4 b4 = *reinterpret_cast<const float4 *>(&Bs[kk][j]);
+                const float4 b4 = *reinterpret_cast<const float4 *>(&Bs[buf][kk][j]);
                 acc[j] = fmaf(a, b4.x, acc[j]);
                 acc[j + 1] = fmaf(a, b4.y, acc[j + 1]);
                 acc[j + 2] = fmaf(a, b4.z, acc[j + 2]);
                 acc[j + 3] = fmaf(a, b4.w, acc[j + 3]);
             }
         }
+        __syncthreads();      // buffer s % 2 is free for step s + 2
     }
+    cp_async_wait<0>();
     const long long row = row0 + t;
     if (row >= M) return;
     const bool split = gridDim.y > 1;

@@ -125,6 +125,24 @@ __device__ __forceinline__ void st_shared_flag(uint32_t addr, int v) {
     asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
+// ---------------------------------------------------------------- async copies
+// 4-byte asynchronous copy global -> shared; with src_bytes 0 nothing is read
+// and the destination is zero-filled.  Completion: cp_async_commit groups the
+// copies issued since the last commit, cp_async_wait<n> waits until at most n
+// groups of this thread are pending.
+__device__ __forceinline__ void cp_async4(uint32_t smem_dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 // Bring the 128-byte line that holds `ptr` into L2 (no register result).
 __device__ __forceinline__ void prefetch_l2(const void *ptr) {

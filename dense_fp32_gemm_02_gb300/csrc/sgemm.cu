@@ -605,8 +605,10 @@ constexpr SkinnyConfig kSkinnyConfigs[] = {
     skinny_config<1, 4, 4, 8>(), skinny_config<2, 4, 4, 4>(), skinny_config<4, 2, 4, 8>(),
     skinny_config<8, 2, 4, 8>(), skinny_config<16, 2, 2, 8>(), skinny_config<32, 2, 1, 8>(),
 };
-// k-range split: about this many blocks per SM
+// k-range split: about this many blocks per SM (skinny-M blocks of 256
+// threads, skinny-N blocks of 128)
 constexpr int kSkinnyBlocksPerSM = 4;
+constexpr int kSkinnyNBlocksPerSM = 8;
 
 // GEMMs of at most SKINNY_ROWS rows that are not small problems: B streamed
 // once by sgemm_skinny_kernel, the k range split so that about
@@ -653,14 +655,14 @@ int launch_skinny(const GemmCall &g, cudaStream_t stream, DeviceState *dev) {
 }
 
 // GEMMs of at most SKINNY_COLS_MAX columns that are not small problems (nor
-// skinny in M): A streamed once by sgemm_skinny_n_kernel, 256 rows per block,
-// the k range split so that about kSkinnyBlocksPerSM blocks per SM run, partial
-// sums added in order by skinny_reduce_kernel.
+// skinny in M): A streamed once by sgemm_skinny_n_kernel, 128 rows per block,
+// the k range split so that about kSkinnyNBlocksPerSM blocks per SM run,
+// partial sums added in order by skinny_reduce_kernel.
 int launch_skinny_n(const GemmCall &g, cudaStream_t stream, DeviceState *dev) {
     const int M = g.M, N = g.N, K = g.K;
     const long long row_blocks = (M + sg::SKINNY_N_ROWS - 1LL) / sg::SKINNY_N_ROWS;
     const long long steps = (K + sg::SKINNY_N_KC - 1LL) / sg::SKINNY_N_KC;
-    const long long want = (long long)kSkinnyBlocksPerSM * dev->sm_count;
+    const long long want = (long long)kSkinnyNBlocksPerSM * dev->sm_count;
     long long S = std::max(1LL, std::min(steps, (want + row_blocks - 1) / row_blocks));
     const int kchunk = int(((steps + S - 1) / S) * sg::SKINNY_N_KC);
     S = (K + kchunk - 1LL) / kchunk;
