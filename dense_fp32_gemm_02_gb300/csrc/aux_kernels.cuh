@@ -286,7 +286,8 @@ __global__ void __launch_bounds__(256)
     constexpr int T = TS / 16;
     __shared__ float part[T * T][256];   // [output][thread]: a warp's accesses are contiguous
     const int z = int(cluster_ctarank());
-    const int kb = z * kchunk, ke = min(K, kb + kchunk);
+    const int kb = z * kchunk;
+    const int ke = int(min((long long)K, (long long)kb + kchunk));
     float acc[T][T];
     small_tile_sum<TS>(acc, M, N, A, lda, B, ldb, kb, ke);
     if (z != 0) {
@@ -340,7 +341,9 @@ __global__ void __launch_bounds__(SKINNY_THREADS, MINB)
     __shared__ __align__(16) float As[SKINNY_KSUB][MR];
     const int t = threadIdx.x;
     const long long col0 = (long long)blockIdx.x * (SKINNY_THREADS * COLS) + t;
-    const int kb = int(blockIdx.y) * kchunk, ke = min(K, kb + kchunk);
+    // (the end in 64 bits: kb + kchunk may pass 2^31 when K is close to it)
+    const int kb = int(blockIdx.y) * kchunk;
+    const int ke = int(min((long long)K, (long long)kb + kchunk));
     float acc[MR][COLS];
 #pragma unroll
     for (int i = 0; i < MR; ++i)
@@ -434,7 +437,9 @@ __global__ void __launch_bounds__(SKINNY_N_ROWS)
     __shared__ __align__(16) float Bs[2][KC][NR];
     const int t = threadIdx.x, lane = t % 32, warp = t / 32;
     const long long row0 = (long long)blockIdx.x * ROWS;
-    const int kb = int(blockIdx.y) * kchunk, ke = min(K, kb + kchunk);
+    // (the end in 64 bits: kb + kchunk may pass 2^31 when K is close to it)
+    const int kb = int(blockIdx.y) * kchunk;
+    const int ke = int(min((long long)K, (long long)kb + kchunk));
     const int steps = (ke - kb + KC - 1) / KC;
     // copies of step s into buffer s % 2: warp w takes rows w, w + 4, ...,
     // lane l column k0 + l; past M or the k range the copy reads nothing and

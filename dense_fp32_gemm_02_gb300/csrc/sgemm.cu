@@ -270,9 +270,14 @@ int cuda_fail(cudaError_t e) {
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Largest M, N or K accepted: the kernels round sizes up to whole tiles and
+// k steps in 32-bit arithmetic, so 2^16 below 2^31 leaves them room.
+constexpr int kMaxDim = 0x7fffffff - 0xffff;
+
 int checked_args(int M, int N, int K, const float *A, int lda, const float *B, int ldb,
                  const float *C, int ldc, float alpha, float beta) {
     if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return SGEMM_ERR_TOO_LARGE;
     if (lda < std::max(1, K) || ldb < std::max(1, N) || ldc < std::max(1, N))
         return SGEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return SGEMM_OK;
@@ -1454,7 +1459,9 @@ SGEMM_API const char *sgemm_status_string(int status) {
         case SGEMM_ERR_CUDA: return "SGEMM_ERR_CUDA: a CUDA call failed (see sgemm_last_cuda_error)";
         case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT: a bounded in-kernel wait expired";
         case SGEMM_ERR_ALLOC: return "SGEMM_ERR_ALLOC: workspace allocation failed";
-        case SGEMM_ERR_TOO_LARGE: return "SGEMM_ERR_TOO_LARGE: the problem needs more scratch than the fixed array of sgemm_noalloc holds";
+        case SGEMM_ERR_TOO_LARGE:
+            return "SGEMM_ERR_TOO_LARGE: a size past 2^31 - 65536, or the problem needs more scratch "
+                   "than the fixed array of sgemm_noalloc holds";
         case SGEMM_ERR_BOUNDS: return "SGEMM_ERR_BOUNDS: the range-checked build found an index out of range (the access was skipped)";
         default: return "unknown sgemm status";
     }

@@ -15,6 +15,7 @@
  *
  * Conventions shared by every entry point:
  *  - Sizes are elements.  lda >= max(1,K), ldb >= max(1,N), ldc >= max(1,N).
+ *  - M, N and K are at most 2^31 - 65536 (SGEMM_ERR_TOO_LARGE above that).
  *  - beta == 0: C is not read on input (NaN/Inf in it do not propagate).
  *  - alpha == 0 or K == 0: A and B are not read; C = beta*C (0 when beta == 0).
  *  - M == 0 or N == 0: nothing is read or written; returns SGEMM_OK.
@@ -47,7 +48,8 @@ typedef enum {
     SGEMM_ERR_CUDA = 3,               /* a CUDA runtime/driver call failed; see sgemm_last_cuda_error() */
     SGEMM_ERR_TIMEOUT = 4,            /* a bounded in-kernel wait expired (reported by sgemm_device_status) */
     SGEMM_ERR_ALLOC = 5,              /* device or pinned workspace allocation failed */
-    SGEMM_ERR_TOO_LARGE = 6,          /* sgemm_noalloc: the problem does not fit its fixed scratch */
+    SGEMM_ERR_TOO_LARGE = 6,          /* a size past 2^31 - 65536, or (sgemm_noalloc) the problem
+                                         does not fit its fixed scratch */
     SGEMM_ERR_BOUNDS = 7              /* range-checked build only: an index was out of range
                                          (reported by sgemm_device_status) */
 } sgemm_status;

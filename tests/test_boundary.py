@@ -101,6 +101,14 @@ def test_invalid_arguments_rejected_without_gpu(lib, kw, entry):
     assert _call(lib, entry=entry, **kw) == 1  # SGEMM_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("entry", ["sgemm", "sgemm_3xtf32", "sgemm_noalloc"])
+@pytest.mark.parametrize("M,N,K", [(2 ** 31 - 1, 1, 1), (1, 2 ** 31 - 65535, 1), (1, 1, 2 ** 31 - 1000)])
+def test_sizes_past_the_limit_rejected_without_gpu(lib, M, N, K, entry):
+    """Sizes within 2^16 of 2^31 would overflow the kernels' 32-bit rounding
+    up to whole tiles: SGEMM_ERR_TOO_LARGE before any CUDA call."""
+    assert _call(lib, M, N, K, A=16, B=16, C=16, entry=entry) == 6
+
+
 def test_misaligned_pointer_rejected(lib):
     f = lib.sgemm
     f.argtypes = [ctypes.c_int] * 3 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_int,
