@@ -511,7 +511,7 @@ bool tall_batch_call(const GemmCall &g) {
     if (g.batch <= 1 || g.bias != nullptr || g.act != sg::ACT_NONE || g.stride_a == 0) return false;
     if (g.M % 256 != 0 || g.M > 16 * 256 || g.K % 64 != 0) return false;
     if (g.stride_c != (long long)g.M * g.ldc) return false;
-    if ((long long)g.batch * g.M > INT32_MAX || (long long)g.batch * g.K > INT32_MAX) return false;
+    if ((long long)g.batch * g.M > kMaxDim || (long long)g.batch * g.K > kMaxDim) return false;
     const bool b_tma = aligned16(g.B) && g.ldb % 4 == 0;
     return !b_tma || g.stride_b == 0 || g.stride_b == (long long)g.K * g.ldb;
 }
