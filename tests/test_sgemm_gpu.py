@@ -643,3 +643,24 @@ def test_config_string_names_the_kernel_sgemm_runs(M, N, K):
     assert binding.config_string(M, N, K).startswith(binding.last_kernel()), (
         binding.config_string(M, N, K), binding.last_kernel())
     assert bool((C == K).all())
+
+
+@pytest.mark.parametrize("M,N,K", [(8, 3001, 1023), (2000, 8, 2048)])
+def test_host_entry_point_on_skinny_shapes(M, N, K):
+    """Host buffers on a skinny-M and a skinny-N shape of fewer than 2048 rows:
+    the host path runs them as one row block on the same kernel as sgemm(),
+    bitwise equal to the device entry point and bit-exact against the oracle
+    on integer inputs."""
+    import torch
+    from dense_fp32_gemm_02_gb300 import binding
+    A, B, C = make_inputs(M, N, K, "int4", "int4", "int4", seed=61 + M)
+    ref, _ = oracle.sgemm(A, B, C, 1.5, 0.5)
+    dev = run_gpu(A, B, C, 1.5, 0.5).cpu()
+    assert "skinny" in binding.last_kernel()
+    hA = torch.from_numpy(np.ascontiguousarray(A)).pin_memory()
+    hB = torch.from_numpy(np.ascontiguousarray(B)).pin_memory()
+    hC = torch.from_numpy(np.ascontiguousarray(C)).pin_memory()
+    binding.sgemm_host(hA, hB, hC, 1.5, 0.5)
+    assert "skinny" in binding.last_kernel()
+    assert torch.equal(hC, dev)
+    assert np.array_equal(hC.numpy(), ref)
