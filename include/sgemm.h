@@ -310,9 +310,10 @@ const char *sgemm_config_string(int M, int N, int K);
  * same result within the tolerance above; they differ in tile sizes, pipeline
  * depth and micro-kernel.  sgemm_variant_count() gives their number,
  * sgemm_variant_name(i) a static description ("" for an invalid index), and
- * sgemm_set_variant(i) forces variant i for later calls in this process
- * (-1 restores the automatic choice; anything else out of range gives
- * SGEMM_ERR_INVALID_ARG).
+ * sgemm_set_variant(i) forces variant i for later sgemm() calls in this
+ * process, also on shapes that would otherwise take the direct small-problem
+ * or skinny kernels (-1 restores the automatic choice; anything else out of
+ * range gives SGEMM_ERR_INVALID_ARG).
  */
 int sgemm_variant_count(void);
 const char *sgemm_variant_name(int id);
