@@ -410,6 +410,16 @@ def probed_mma_fields(achieved_tflops, sms, sm_mhz=None):
     return out
 
 
+def hbm_peak_gbs():
+    """(peak GB/s, source text): the measured copy bandwidth of this machine's
+    GB300s, else the fallback figure."""
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured: MEASURED_PEAKS.json hbm_gbs (copy)"
+    except (OSError, ValueError, KeyError):
+        return HBM_FALLBACK_GBS, "fallback: 6.8 TB/s"
+
+
 def dram_use(traffic, ms):
     """{dram_gbs, dram_frac}: one launch's DRAM bytes (the ncu figure) over its
     CUDA-event duration, and that rate against the measured copy bandwidth;
@@ -417,11 +427,7 @@ def dram_use(traffic, ms):
     if not traffic or not ms or ms <= 0:
         return {"dram_gbs": None, "dram_frac": None}
     gbs = traffic / (ms * 1e-3) / 1e9
-    try:
-        with open(PEAKS_FILE) as f:
-            peak = float(json.load(f)["hbm_gbs"])
-    except (OSError, ValueError, KeyError):
-        peak = HBM_FALLBACK_GBS
+    peak, _ = hbm_peak_gbs()
     return {"dram_gbs": round(gbs, 1), "dram_frac": round(gbs / peak, 4)}
 
 
@@ -623,7 +629,21 @@ def run_ours(args):
     peak_tflops = sms * FFMA_PER_SM_PER_CLK * 2 * SM_MAX_MHZ_FALLBACK * 1e6 / 1e12
     peak_meas_clk = (sms * FFMA_PER_SM_PER_CLK * 2 * clk["sm_mhz"] * 1e6 / 1e12
                      if clk.get("sm_mhz") else None)
-    if args.path == "ffma":
+    if args.path == "ffma" and w.bound == "hbm":
+        # HBM: the large operand read once (skinny kernels)
+        alg_bytes = 4.0 * (w.M * w.K + w.K * w.N + w.M * w.N * (2 if w.beta != 0 else 1)) * w.batch
+        hbm_peak, hsrc = hbm_peak_gbs()
+        gbs = alg_bytes / (main_ms * 1e-3) / 1e9 if main_ms > 0 else None
+        roofline = {
+            "bound": "hbm", "kernel": kernel_text,
+            "achieved": round(gbs, 1) if gbs else None, "peak": round(hbm_peak, 1), "unit": "GB/s",
+            "frac": round(gbs / hbm_peak, 4) if gbs else None,
+            "traffic": load_traffic(w.name),
+            **dram_use(load_traffic(w.name), main_ms), "peak_source": hsrc,
+            "main_kernel_ms": round(main_ms, 4), "pack_kernels_ms": round(pack_ms, 4),
+            "algorithmic_bytes_per_launch": alg_bytes,
+        }
+    elif args.path == "ffma":
         # FP32 FFMA pipe
         achieved_tflops = w.flops / (main_ms * 1e-3) / 1e12 if main_ms > 0 else None
         f_meas = clk.get("sm_mhz")

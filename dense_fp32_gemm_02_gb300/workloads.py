@@ -40,6 +40,7 @@ class Workload:
     batch: int = 1              # independent GEMMs of this shape (sgemm_ex)
     bias: bool = False          # a per-column bias vector per batch (sgemm_ex)
     act: str = "none"           # none | relu | gelu (sgemm_ex)
+    bound: str = "alu"          # the roofline of its main kernel: alu (FFMA) or hbm
 
     @property
     def flops(self) -> float:
@@ -77,6 +78,11 @@ WORKLOADS = {
                                      "upm1", "upm1", None, 1007, check="rows:64",
                                      bias=True, act="gelu",
                                      note="layer form: bias per output column, then GELU"),
+    # a degenerate shape of the same operation: one column (a matrix-vector
+    # product), bound by reading A once from HBM
+    "sgemv_16384x1x16384": Workload("sgemv_16384x1x16384", 16384, 1, 16384, 1.0, 0.0, "upm1",
+                                    "upm1", None, 1008, check="full", bound="hbm",
+                                    note="N = 1: the skinny-N kernel streams A (1.07 GB) once"),
 }
 
 # The timed workload of the benchmark.
