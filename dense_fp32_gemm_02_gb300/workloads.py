@@ -83,6 +83,9 @@ WORKLOADS = {
     "sgemv_16384x1x16384": Workload("sgemv_16384x1x16384", 16384, 1, 16384, 1.0, 0.0, "upm1",
                                     "upm1", None, 1008, check="full", bound="hbm",
                                     note="N = 1: the skinny-N kernel streams A (1.07 GB) once"),
+    "sgemv_1x16384x16384": Workload("sgemv_1x16384x16384", 1, 16384, 16384, 1.0, 0.0, "upm1",
+                                    "upm1", None, 1009, check="full", bound="hbm",
+                                    note="M = 1: the skinny-M kernel streams B (1.07 GB) once"),
 }
 
 # The timed workload of the benchmark.
