@@ -615,22 +615,22 @@ constexpr SkinnyConfig kSkinnyConfigs[] = {
 constexpr int kSkinnyBlocksPerSM = 4;
 constexpr int kSkinnyNBlocksPerSM = 8;
 
-// GEMMs of at most SKINNY_ROWS rows that are not small problems: B streamed
-// once by sgemm_skinny_kernel, the k range split so that about
-// kSkinnyBlocksPerSM blocks per SM run (whole 128-deep sub-ranges), partial
-// sums added in order by skinny_reduce_kernel.
-int launch_skinny(const GemmCall &g, cudaStream_t stream, DeviceState *dev) {
+// The split-K launch shared by the skinny kernels: `blocks` blocks along the
+// grid's x dimension, K cut into S ranges of whole `step`-deep steps along y so
+// that about `per_sm` blocks per SM run; with S > 1 the kernel writes S
+// partial sums per output to pool memory and skinny_reduce_kernel adds them in
+// range order and applies alpha and beta.  launch(grid, kchunk, P) issues the
+// kernel on `stream`.
+template <class Launch>
+int run_split_k(const GemmCall &g, cudaStream_t stream, DeviceState *dev, long long blocks,
+                int step, int per_sm, const char *text, Launch &&launch) {
     const int M = g.M, N = g.N, K = g.K;
-    const SkinnyConfig *cfg = &kSkinnyConfigs[0];
-    while (cfg->rows < M) ++cfg;
-    const long long block_cols = (long long)sg::SKINNY_THREADS * cfg->cols;
-    const long long col_blocks = (N + block_cols - 1) / block_cols;
-    const long long subs = (K + sg::SKINNY_KSUB - 1LL) / sg::SKINNY_KSUB;
-    const long long want = (long long)kSkinnyBlocksPerSM * dev->sm_count;
-    long long S = std::max(1LL, std::min(subs, (want + col_blocks - 1) / col_blocks));
-    const int kchunk = int(((subs + S - 1) / S) * sg::SKINNY_KSUB);
+    const long long steps = (K + step - 1LL) / step;
+    const long long want = (long long)per_sm * dev->sm_count;
+    long long S = std::max(1LL, std::min(steps, (want + blocks - 1) / blocks));
+    const int kchunk = int(((steps + S - 1) / S) * step);
     S = (K + kchunk - 1LL) / kchunk;
-    if (col_blocks > 0x7fffffffLL || S > 65535) return SGEMM_ERR_TOO_LARGE;
+    if (blocks > 0x7fffffffLL || S > 65535) return SGEMM_ERR_TOO_LARGE;
     float *P = nullptr;
     if (S > 1) {
         cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&P),
@@ -639,16 +639,14 @@ int launch_skinny(const GemmCall &g, cudaStream_t stream, DeviceState *dev) {
     }
     ProfCall prof(stream);
     prof.main_begin();
-    const dim3 grid(static_cast<unsigned>(col_blocks), static_cast<unsigned>(S));
-    cfg->kernel<<<grid, sg::SKINNY_THREADS, 0, stream>>>(M, N, K, kchunk, g.alpha, g.A, g.lda, g.B,
-                                                         g.ldb, g.beta, g.C, g.ldc, P);
+    launch(dim3(static_cast<unsigned>(blocks), static_cast<unsigned>(S)), kchunk, P);
     g_launches.fetch_add(1);
-    t_last_kernel = kSkinny;
+    t_last_kernel = text;
     if (S > 1) {
         const long long total = (long long)M * N;
-        const int blocks = int(std::min<long long>((total + 255) / 256, (long long)dev->sm_count * 8));
-        sg::skinny_reduce_kernel<<<blocks, 256, 0, stream>>>(M, N, int(S), P, g.alpha, g.beta,
-                                                             g.C, g.ldc);
+        const int rblocks = int(std::min<long long>((total + 255) / 256, (long long)dev->sm_count * 8));
+        sg::skinny_reduce_kernel<<<rblocks, 256, 0, stream>>>(M, N, int(S), P, g.alpha, g.beta,
+                                                              g.C, g.ldc);
         g_launches.fetch_add(1);
     }
     prof.main_end();
@@ -659,49 +657,38 @@ int launch_skinny(const GemmCall &g, cudaStream_t stream, DeviceState *dev) {
     return SGEMM_OK;
 }
 
+// GEMMs of at most SKINNY_ROWS rows that are not small problems: B streamed
+// once by sgemm_skinny_kernel, the k range split so that about
+// kSkinnyBlocksPerSM blocks per SM run (whole 128-deep sub-ranges), partial
+// sums added in order by skinny_reduce_kernel.
+int launch_skinny(const GemmCall &g, cudaStream_t stream, DeviceState *dev) {
+    const SkinnyConfig *cfg = &kSkinnyConfigs[0];
+    while (cfg->rows < g.M) ++cfg;
+    const long long block_cols = (long long)sg::SKINNY_THREADS * cfg->cols;
+    return run_split_k(g, stream, dev, (g.N + block_cols - 1) / block_cols, sg::SKINNY_KSUB,
+                       kSkinnyBlocksPerSM, kSkinny, [&](dim3 grid, int kchunk, float *P) {
+                           cfg->kernel<<<grid, sg::SKINNY_THREADS, 0, stream>>>(
+                               g.M, g.N, g.K, kchunk, g.alpha, g.A, g.lda, g.B, g.ldb, g.beta,
+                               g.C, g.ldc, P);
+                       });
+}
+
 // GEMMs of at most SKINNY_COLS_MAX columns that are not small problems (nor
 // skinny in M): A streamed once by sgemm_skinny_n_kernel, 128 rows per block,
 // the k range split so that about kSkinnyNBlocksPerSM blocks per SM run,
 // partial sums added in order by skinny_reduce_kernel.
 int launch_skinny_n(const GemmCall &g, cudaStream_t stream, DeviceState *dev) {
-    const int M = g.M, N = g.N, K = g.K;
-    const long long row_blocks = (M + sg::SKINNY_N_ROWS - 1LL) / sg::SKINNY_N_ROWS;
-    const long long steps = (K + sg::SKINNY_N_KC - 1LL) / sg::SKINNY_N_KC;
-    const long long want = (long long)kSkinnyNBlocksPerSM * dev->sm_count;
-    long long S = std::max(1LL, std::min(steps, (want + row_blocks - 1) / row_blocks));
-    const int kchunk = int(((steps + S - 1) / S) * sg::SKINNY_N_KC);
-    S = (K + kchunk - 1LL) / kchunk;
-    if (row_blocks > 0x7fffffffLL || S > 65535) return SGEMM_ERR_TOO_LARGE;
-    float *P = nullptr;
-    if (S > 1) {
-        cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&P),
-                                                size_t(S) * M * N * 4, dev->pool, stream);
-        if (e != cudaSuccess) return cuda_fail(e);
-    }
-    ProfCall prof(stream);
-    prof.main_begin();
-    const dim3 grid(static_cast<unsigned>(row_blocks), static_cast<unsigned>(S));
-    auto kernel = N <= 4 ? &sg::sgemm_skinny_n_kernel<4>
-                  : N <= 8 ? &sg::sgemm_skinny_n_kernel<8>
-                  : N <= 16 ? &sg::sgemm_skinny_n_kernel<16>
-                            : &sg::sgemm_skinny_n_kernel<32>;
-    kernel<<<grid, sg::SKINNY_N_ROWS, 0, stream>>>(M, N, K, kchunk, g.alpha, g.A, g.lda, g.B, g.ldb,
-                                                  g.beta, g.C, g.ldc, P);
-    g_launches.fetch_add(1);
-    t_last_kernel = kSkinnyN;
-    if (S > 1) {
-        const long long total = (long long)M * N;
-        const int blocks = int(std::min<long long>((total + 255) / 256, (long long)dev->sm_count * 8));
-        sg::skinny_reduce_kernel<<<blocks, 256, 0, stream>>>(M, N, int(S), P, g.alpha, g.beta,
-                                                             g.C, g.ldc);
-        g_launches.fetch_add(1);
-    }
-    prof.main_end();
-    cudaError_t e = cudaGetLastError();
-    cudaError_t ef = S > 1 ? cudaFreeAsync(P, stream) : cudaSuccess;
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (ef != cudaSuccess) return cuda_fail(ef);
-    return SGEMM_OK;
+    auto kernel = g.N <= 4    ? &sg::sgemm_skinny_n_kernel<4>
+                  : g.N <= 8  ? &sg::sgemm_skinny_n_kernel<8>
+                  : g.N <= 16 ? &sg::sgemm_skinny_n_kernel<16>
+                              : &sg::sgemm_skinny_n_kernel<32>;
+    return run_split_k(g, stream, dev, (g.M + sg::SKINNY_N_ROWS - 1LL) / sg::SKINNY_N_ROWS,
+                       sg::SKINNY_N_KC, kSkinnyNBlocksPerSM, kSkinnyN,
+                       [&](dim3 grid, int kchunk, float *P) {
+                           kernel<<<grid, sg::SKINNY_N_ROWS, 0, stream>>>(
+                               g.M, g.N, g.K, kchunk, g.alpha, g.A, g.lda, g.B, g.ldb, g.beta,
+                               g.C, g.ldc, P);
+                       });
 }
 
 int gemm_device(const GemmCall &g, cudaStream_t stream) {
